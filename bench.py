@@ -1,0 +1,553 @@
+#!/usr/bin/env python
+"""Decode-step weight-stream benchmark.
+
+Default workload: one decode step's weight stream of a 28-layer, 1536-wide
+fp16 decoder (Qwen2.5-1.5B shape: q/k/v/o/gate/up/down, 196 matrices,
+2,620,391,424 weight bytes), M = 1, all inputs resident in HBM.  A step is one
+dg_decode_step_weights pass, replayed from a CUDA graph.  Metric: weight bytes
+streamed per second (GB/s, 1e9), with microseconds per step alongside.
+
+Prints ONE JSON line on rank 0.  Other workloads (--workload) print the same
+line for their own unit of work (one call or one step).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dg|reference]
+                  [--workload NAME]
+
+--impl reference times the CPU oracle (fp64 / exact-integer C, all host cores)
+on a bounded sample of the same workload: the deliberately slow checker, not a
+tuned CPU GEMV.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 126 * 1024 * 1024   # GB300 L2 (nvidia reports ~126 MiB usable)
+FALLBACK_HBM_GBS = 6800.0
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ---- environment facts --------------------------------------------------------
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def csrc_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "quantized_skinny_gemm_gb300", "csrc")
+    for n in sorted(os.listdir(d)):
+        with open(os.path.join(d, n), "rb") as f:
+            h.update(n.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch from a committed ncu capture, only if the kernel
+    sources are unchanged since it was taken; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    e = d.get(kernel)
+    if not e or e.get("csrc_hash") != csrc_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while running."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if not self.p:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.p.terminate()
+        out, _ = self.p.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---- workloads ----------------------------------------------------------------
+
+class Workload:
+    """Device state for one workload: step() enqueues one unit of work."""
+    name = ""
+    unit_bytes = 0          # algorithmic weight bytes per unit
+    launches = 0            # kernels per unit
+    dtype = "f16"
+    config = {}
+
+
+def build_workload(name, dev, torch):
+    import quantized_skinny_gemm_gb300 as dg
+    from quantized_skinny_gemm_gb300 import plans, synth
+
+    w = Workload()
+    w.name = name
+    s = torch.cuda.Stream(device=dev)
+    w.stream = s
+    if name == "decode_fp16":
+        layers = synth.decode_fp16_workload(seed=0)
+        st = plans.fp16_decode_step(layers, dev)
+        w.host = layers
+        w.in_arena, w.out_arena = st.in_arena, st.out_arena
+        w.unit_bytes = st.weight_bytes
+        w.launches = st.n_launches
+        w.run = lambda: dg.decode_step_weights(st.plan, st.ws, stream=s)
+        w.config = {"workload": "decode-step weight stream, 28-layer 1536-wide fp16 decoder "
+                                "(Qwen2.5-1.5B shape), 196 matrices, M=1",
+                    "weight_bytes_per_step": st.weight_bytes,
+                    "l2": "inputs 2.62 GB > 126 MB L2 (no flush)"}
+        # dominant kernel: the fused gate|up launch of every layer
+        ops = [op for op in st.plan.array if op.N == 8960 and op.K == 1536]
+        dplan = plans.StepPlan(ops, [])
+        w.dominant = ("gate|up 17920x1536 fp16",
+                      lambda: dg.decode_step_weights(dplan, None, stream=s), len(ops) // 2,
+                      2 * 8960 * 1536 * 2)
+        w.cpu_sample = ("fp", layers)
+        w.dtype = "f16"
+    elif name in ("decode_int4_a16", "decode_int4_a8"):
+        act = name[-3:]
+        layers, head, xh = synth.decode_int4_workload(seed=0)
+        st = plans.int4_decode_step(layers, head, xh, dev, act=act)
+        w.host = (layers, head, xh)
+        w.in_arena, w.out_arena = st.in_arena, st.out_arena
+        w.unit_bytes = st.weight_bytes
+        w.launches = st.n_launches
+        w.run = lambda: dg.decode_step_weights(st.plan, st.ws, stream=s)
+        w.config = {"workload": "decode-step weight stream, 32-layer 4096-wide int4 g32 decoder "
+                                "(Llama-3.1-8B shape) + 128256-row lm_head with argmax, W4%s, M=1"
+                                % act[1:].upper(),
+                    "weight_bytes_per_step": st.weight_bytes,
+                    "l2": "inputs 4.22 GB > 126 MB L2 (no flush)"}
+        ops = [op for op in st.plan.array if op.N == 14336 and op.K == 4096 and not op.token]
+        for op in ops:
+            op.x = None  # codes already quantized by the step; time the GEMV alone
+        dplan = plans.StepPlan(ops, [])
+        w.dominant = ("gate|up 28672x4096 int4",
+                      lambda: dg.decode_step_weights(dplan, None, stream=s), len(ops) // 2,
+                      2 * 14336 * 4096 // 2 + 2 * 14336 * (4096 // 32) * 2)
+        w.cpu_sample = ("w4" + act, (layers, head, xh))
+        w.dtype = "int4xf16" if act == "a16" else "int4xi8"
+    elif name == "lm_head":
+        W, x = synth.lm_head_workload(seed=0)
+        ain, aout = plans.Arena(), plans.Arena()
+        ix = ain.reserve(x.shape, torch.float16)
+        il, it = aout.reserve((W.shape[0],), torch.float32), aout.reserve((1,), torch.int32)
+        xin, outs = ain.build(dev), aout.build(dev)
+        xd = xin[ix]
+        xd.copy_(x)
+        logits, token = outs[il], outs[it]
+        Wd = W.to(dev)
+        head = dg.linear(dg.LINEAR_F16, Wd, 1, W.shape[0], W.shape[1], x=xd, logits=logits,
+                         token=token)
+        plan = dg.StepPlan([head], [Wd, ain.buf, aout.buf])
+        ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=dev)
+        w.host = (W, x)
+        w.in_arena, w.out_arena = ain.buf, aout.buf
+        w.unit_bytes = W.numel() * 2
+        w.launches = 2
+        w.run = lambda: dg.decode_step_weights(plan, ws, stream=s)
+        w.config = {"workload": "lm_head 248320x2048 fp16 with fused greedy argmax, M=1",
+                    "weight_bytes_per_call": w.unit_bytes,
+                    "l2": "inputs 1.02 GB > 126 MB L2 (no flush)"}
+        w.dominant = ("lm_head 248320x2048 fp16", w.run, 1, w.unit_bytes)
+        w.cpu_sample = ("head", (W, x))
+    elif name == "gateup_fp16":
+        # the dominant launch of the fp16 decoder alone: 4 distinct gate|up pairs
+        # (220 MB, larger than L2), one fused launch each
+        g = synth.generator(0)
+        pairs = [(synth.normal((8960, 1536), synth.W_STD, g), synth.normal((8960, 1536), synth.W_STD, g))
+                 for _ in range(4)]
+        x = synth.normal((1, 1536), 1.0, g)
+        ain, aout = plans.Arena(), plans.Arena()
+        ix = ain.reserve(x.shape, torch.float16)
+        iy = [aout.reserve((1, 8960), torch.float16) for _ in range(8)]
+        xin, outs = ain.build(dev), aout.build(dev)
+        xd = xin[ix]
+        xd.copy_(x)
+        keep, ops = [ain.buf, aout.buf], []
+        for i, (Wg, Wu) in enumerate(pairs):
+            for j, Wh in enumerate((Wg, Wu)):
+                Wd = Wh.to(dev)
+                keep.append(Wd)
+                ops.append(dg.linear(dg.LINEAR_F16, Wd, 1, 8960, 1536, x=xd, y=outs[iy[2 * i + j]]))
+        plan = dg.StepPlan(ops, keep)
+        w.host = (pairs, x)
+        w.in_arena, w.out_arena = ain.buf, aout.buf
+        w.unit_bytes = 4 * 2 * 8960 * 1536 * 2
+        w.launches = 4
+        w.run = lambda: dg.decode_step_weights(plan, None, stream=s)
+        w.config = {"workload": "fused gate|up 17920x1536 fp16 (4 distinct pairs per step), M=1",
+                    "weight_bytes_per_step": w.unit_bytes,
+                    "l2": "inputs 220 MB > 126 MB L2 (no flush)"}
+        w.dominant = ("gate|up 17920x1536 fp16", w.run, 4, 2 * 8960 * 1536 * 2)
+        w.cpu_sample = ("pairs", (pairs, x))
+    else:
+        raise SystemExit("unknown workload %s" % name)
+    return w
+
+
+def graph_of(fn, stream, torch):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # first launch outside capture (one-time setup)
+    stream.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def time_graph(g, stream, n, torch):
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / 1e3  # seconds
+
+
+# ---- CPU oracle (baseline / reference arm) ------------------------------------------
+
+def oracle_sample(w, budget_s):
+    """Times the oracle on whole matrices of the workload until budget_s has
+    passed.  Returns (weight bytes done, seconds, description)."""
+    import numpy as np
+    import oracle
+    kind, data = w.cpu_sample
+    done, t0 = 0, time.perf_counter()
+    mats = 0
+
+    def bits(t):
+        return t.contiguous().view(__import__("torch").int16).numpy().view(np.uint16)
+
+    if kind == "fp":
+        for L in data:
+            for lin in L.linears:
+                oracle.gemv_fp(bits(lin.W), bits(L.inputs[lin.x_name]))
+                done += lin.W.numel() * 2
+                mats += 1
+                if time.perf_counter() - t0 > budget_s:
+                    break
+            if time.perf_counter() - t0 > budget_s:
+                break
+        desc = "%d whole fp16 matrices of the decoder in layer order" % mats
+    elif kind.startswith("w4"):
+        layers, head, xh = data
+        for L in layers:
+            for lin in L.linears:
+                x = L.inputs[lin.x_name]
+                if kind == "w4a16":
+                    oracle.gemv_w4a16(lin.W.numpy(), bits(lin.scales), bits(x))
+                else:
+                    q, s = oracle.quant_act(bits(x))
+                    oracle.gemv_w4a8(lin.W.numpy(), bits(lin.scales), q, s)
+                done += lin.W.numel() + lin.scales.numel() * 2
+                mats += 1
+                if time.perf_counter() - t0 > budget_s:
+                    break
+            if time.perf_counter() - t0 > budget_s:
+                break
+        desc = "%d whole int4 matrices of the decoder in layer order" % mats
+    elif kind == "pairs":
+        pairs, x = data
+        for Wg, Wu in pairs:
+            for Wh in (Wg, Wu):
+                oracle.gemv_fp(bits(Wh), bits(x))
+                done += Wh.numel() * 2
+                mats += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        desc = "%d whole 8960x1536 fp16 matrices" % mats
+    else:
+        W, x = data
+        rows = W.shape[0]
+        step = 15520
+        for lo in range(0, rows, step):
+            oracle.gemv_fp(bits(W[lo:lo + step]), bits(x))
+            done += step * W.shape[1] * 2
+            mats += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        desc = "%d 15520-row slices of the lm_head" % mats
+    return done, time.perf_counter() - t0, desc
+
+
+# ---- main ----------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="dg", choices=["dg", "reference"])
+    ap.add_argument("--workload", default="decode_fp16",
+                    choices=["decode_fp16", "decode_int4_a16", "decode_int4_a8", "lm_head",
+                             "gateup_fp16"])
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return run_reference(args, world)
+
+    import torch
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl", device_id=dev)
+
+    import quantized_skinny_gemm_gb300 as dg
+    dg.load()
+    log("building workload", args.workload)
+    w = build_workload(args.workload, dev, torch)
+    s = w.stream
+    g = graph_of(w.run, s, torch)
+    for _ in range(args.warmup):
+        with torch.cuda.stream(s):
+            g.replay()
+    torch.cuda.synchronize()
+
+    peak, peak_src = measured_peaks()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    secs = time_graph(g, s, args.steps, torch)
+    torch.cuda.synchronize()
+    if dist:
+        t = torch.tensor([secs], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        secs = float(t.item())
+        dist.barrier()
+
+    # dominant kernel alone: its launches for every layer, replayed
+    dname, dfn, dlaunch, dbytes = w.dominant
+    gd = graph_of(dfn, s, torch)
+    nrep = max(20, args.steps // 10)
+    dsecs = time_graph(gd, s, nrep, torch)
+    d_launch_s = dsecs / (nrep * dlaunch)
+    clk = clocks.stop()
+
+    # end to end through the public API with host buffers
+    e2e = measure_e2e(w, args, torch, dg, g)
+
+    units = args.steps * world
+    value = w.unit_bytes * units / secs / 1e9
+    out = {
+        "metric": "decode weight-stream GB/s",
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 6),
+        "us_per_step": round(secs / args.steps * 1e6, 3),
+        "frac_of_hbm_peak": round(value / world / peak, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic (seeded, torch.Generator seed 0)",
+        "config": dict(w.config, parallelism="replicas" if world > 1 else "single GPU",
+                       graph="CUDA graph replay of the step", pdl=True),
+        "gpu_launches": w.launches * args.steps,
+        "roofline": {"bound": "hbm", "kernel": dname, "achieved": round(dbytes / d_launch_s / 1e9, 1),
+                     "peak": peak, "peak_source": peak_src + " (MEASURED_PEAKS hbm_gbs, copy)",
+                     "unit": "GB/s", "frac": round(dbytes / d_launch_s / 1e9 / peak, 4),
+                     "us_per_launch": round(d_launch_s * 1e6, 3),
+                     "bytes_per_launch": dbytes,
+                     "traffic": recorded_traffic(dname)},
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0:
+        out["hbm_probe"] = probe_hbm(torch, dg, s)
+        if world == 1 or rank == 0:
+            done, cs, desc = oracle_sample(w, args.cpu_budget)
+            out["cpu_baseline"] = {"value": round(done / cs / 1e9, 4), "unit": "GB/s",
+                                   "cores": os.cpu_count(), "kind": "oracle",
+                                   "sample": desc + " (%.1f s)" % cs}
+        print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_e2e(w, args, torch, dg, g):
+    """Per step, through the public API: the step's inputs from pinned host
+    memory into the device input arena, the step (its CUDA graph, as captured
+    from dg_decode_step_weights), and its results back into pinned host
+    memory; one copy each way on the step's stream."""
+    s = w.stream
+    h_in = w.in_arena.detach().cpu().pin_memory()
+    h_out = torch.empty(w.out_arena.shape, dtype=w.out_arena.dtype).pin_memory()
+    n = max(10, min(args.steps // 5, 1000))
+
+    def one(replay):
+        with torch.cuda.stream(s):
+            w.in_arena.copy_(h_in, non_blocking=True)
+            if replay:
+                g.replay()
+            else:
+                w.run()
+            h_out.copy_(w.out_arena, non_blocking=True)
+
+    res = {}
+    for mode in ("graph", "eager"):
+        for _ in range(3):
+            one(mode == "graph")
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record(s)
+        for _ in range(n):
+            one(mode == "graph")
+        e1.record(s)
+        s.synchronize()
+        res[mode] = max(time.perf_counter() - t0, e0.elapsed_time(e1) / 1e3)
+    secs = res["graph"]
+    return {"value": round(w.unit_bytes * n / secs / 1e9, 1), "unit": "GB/s",
+            "us_per_step": round(secs / n * 1e6, 2), "h2d_bytes_per_step": h_in.numel(),
+            "d2h_bytes_per_step": h_out.numel(), "steps": n,
+            "eager_us_per_step": round(res["eager"] / n * 1e6, 2),
+            "path": "pinned host inputs -> device arena, graph of dg_decode_step_weights, "
+                    "device results -> pinned host (one copy each way, wall clock)"}
+
+
+def probe_hbm(torch, dg, s):
+    n = 2 * 1024 ** 3
+    a = torch.empty(n, dtype=torch.uint8, device=s.device)
+    b = torch.empty(n, dtype=torch.uint8, device=s.device)
+    sink = torch.zeros(1024, dtype=torch.int32, device=s.device)
+    res = {}
+    for name, fn, nbytes in (("copy", lambda: dg.probe_copy(a, b, stream=s), 2 * n),
+                             ("read", lambda: dg.probe_read(a, sink, stream=s), n)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        best = 1e9
+        for _ in range(10):
+            e0.record(s)
+            fn()
+            e1.record(s)
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1) / 1e3)
+        res[name + "_gbs"] = round(nbytes / best / 1e9, 1)
+    del a, b
+    return res
+
+
+def run_reference(args, world):
+    """The oracle on the host cores, same workload / metric / unit."""
+    import torch  # noqa: F401  (synthetic inputs)
+    from quantized_skinny_gemm_gb300 import synth
+
+    class W:
+        pass
+
+    w = W()
+    if args.workload == "decode_fp16":
+        w.cpu_sample = ("fp", synth.decode_fp16_workload(seed=0, layers=1))
+        cfg = "decode-step weight stream, 28-layer 1536-wide fp16 decoder (Qwen2.5-1.5B shape), 196 matrices, M=1"
+    elif args.workload.startswith("decode_int4"):
+        act = args.workload[-3:]
+        layers, head, xh = synth.decode_int4_workload(seed=0, layers=1, vocab=0)
+        w.cpu_sample = ("w4" + act, (layers, head, xh))
+        cfg = "decode-step weight stream, 32-layer 4096-wide int4 g32 decoder (Llama-3.1-8B shape), W4%s, M=1" % act[1:].upper()
+    else:
+        W, x = synth.fp_case(15520, 2048, 1, seed=0)
+        w.cpu_sample = ("head", (W, x))
+        cfg = "lm_head 248320x2048 fp16 with fused greedy argmax, M=1"
+    # each step: one bounded sample (~1 s of oracle work)
+    for _ in range(args.warmup):
+        oracle_sample(w, 0.0)
+    done = secs = 0.0
+    desc = ""
+    for _ in range(args.steps if args.steps <= 50 else 50):
+        d, s, desc = oracle_sample(w, 1.0)
+        done += d
+        secs += s
+    v = done / secs / 1e9
+    out = {"impl": "reference", "metric": "decode weight-stream GB/s", "value": round(v, 4),
+           "unit": "GB/s", "n_gpus": world, "steps": min(args.steps, 50), "warmup": args.warmup,
+           "ms_per_step": round(secs / min(args.steps, 50) * 1e3, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": cfg, "sample": "first layer's matrices per step"},
+           "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": os.cpu_count(),
+                            "kind": "oracle", "sample": desc},
+           "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

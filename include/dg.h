@@ -1,0 +1,181 @@
+/*
+ * dg.h -- C ABI of the GB300 (sm_103a) decode-step skinny GEMV library (libdg.so).
+ *
+ * What it computes: the weight-streaming matrix-vector product of single-request
+ * LLM decoding, y = x * W^T with x holding M = 1 token (or a few draft/verify
+ * tokens), in three forms:
+ *   - FP16 / BF16 weights                 (dg_gemv_f16)
+ *   - a very wide lm_head + greedy argmax (dg_lm_head_argmax)
+ *   - weight-quantized: W8A8 per-channel int8 (dg_gemv_w8a8) and groupwise
+ *     int4 with fp16 or int8 activations (dg_gemv_w4), dequantized in registers.
+ * Sources: the M=1 custom cube matmul, the 16-slice lm_head with a host reduce
+ * and the weight-bandwidth floor of "MiniCPM-V on Orange Pi AIPro (Ascend 310B)";
+ * single-request decode and graph-replayed decode steps of "EdgeFM: Efficient
+ * Edge Inference for Vision-Language Models" (sections 2.B and 2.C); W8A8 and
+ * W4A8 of "vLLM Arm CPU optimizations" (sections "INT8 W8A8", "INT8 W4A8").
+ * The pages give no formulas: the definitions below are the plain readings.
+ *
+ * Conventions (every entry point):
+ *  - Layout.  W is [N][K] row-major (output features x input features, K
+ *    contiguous).  x is [M][K] and y is [M][N], row-major.
+ *    y[m][n] = sum_k W[n][k] * x[m][k].
+ *  - Pointers.  All tensor pointers are DEVICE pointers owned by the caller.
+ *    The library allocates and frees nothing; scratch comes from the caller's
+ *    workspace (ws, ws_bytes), sized by dg_workspace_bytes.
+ *  - Streams.  Work is enqueued on `stream` (NULL = legacy default stream);
+ *    calls never synchronize and can be captured into a CUDA graph.  Kernels
+ *    are launched with programmatic dependent launch: a kernel may prefetch its
+ *    weights into L2 while the previous kernel on the stream finishes, and
+ *    touches activations, outputs and workspace only after it completed.
+ *  - Errors.  Arguments are validated on the host before anything is launched;
+ *    on failure nothing is enqueued and a dg_status other than DG_OK returns.
+ *    A failed launch returns DG_ERR_CUDA.  No C++ exception crosses the ABI.
+ *  - Determinism.  Each output is summed in a fixed order that depends only on
+ *    K and the element format (never on N, M, the row offset or the launch
+ *    grid), so repeated calls are bitwise identical and a row slice of W gives
+ *    bitwise the same rows as the whole matrix.
+ *  - Alignment.  W, x, xq and y must be 16-byte aligned; K must be a multiple
+ *    of 8 (fp16/bf16), 16 (int8) or 32 (int4).
+ */
+#ifndef DG_H_
+#define DG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* dg_stream; /* same type as cudaStream_t */
+
+typedef enum {
+    DG_OK = 0,
+    DG_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, bad enum */
+    DG_ERR_UNSUPPORTED = 2, /* shape or option outside what the kernels handle */
+    DG_ERR_MISALIGNED = 3,  /* a pointer or K breaks the alignment rules */
+    DG_ERR_WORKSPACE = 4,   /* ws smaller than dg_workspace_bytes asks for */
+    DG_ERR_CUDA = 5,        /* a CUDA call or launch failed */
+    DG_ERR_TIMEOUT = 6      /* a bounded device-side wait gave up */
+} dg_status;
+
+typedef enum { DG_F16 = 0, DG_BF16 = 1 } dg_ftype;
+
+/* Kind of one linear op in a decode step (dg_linear.kind). */
+typedef enum {
+    DG_LINEAR_F16 = 0,   /* W fp16 [N][K], x fp16 [M][K], y fp16 */
+    DG_LINEAR_BF16 = 1,  /* W bf16, x bf16, y bf16 */
+    DG_LINEAR_W8A8 = 2,  /* W int8 [N][K] + float w_scale[N]; x_i8 + x_scale; y fp16 */
+    DG_LINEAR_W4A16 = 3, /* W packed int4 [N][K/2] + half w_scale[N][K/group]; x fp16; y fp16 */
+    DG_LINEAR_W4A8 = 4   /* as W4A16 but x_i8 + x_scale; y fp16 */
+} dg_kind;
+
+/* One linear op: y = x * W^T in the format `kind`.
+ * For the quantized-activation kinds (W8A8, W4A8), x_i8 [M][K] and x_scale[M]
+ * are read; if `x` (fp16 [M][K]) is also given, dg_decode_step_weights first
+ * quantizes x into x_i8 / x_scale (see dg_quantize_act_i8).
+ * An op with token != NULL is an lm_head: M must be 1, logits (fp32 [N]) and
+ * the greedy token are written and y may be NULL. */
+typedef struct {
+    int32_t kind;
+    int32_t M, N, K;
+    int32_t group_size;    /* int4 kinds: multiple of 32 dividing K (32 in the workloads) */
+    const void* W;
+    const void* w_scale;
+    const void* x;
+    const int8_t* x_i8;
+    const float* x_scale;
+    void* y;
+    float* logits;
+    int32_t* token;
+    int32_t* acc_out;      /* W8A8 only, optional: exact int32 accumulators [M][N] */
+} dg_linear;
+
+/* FP16 / BF16 weights (paragraph on the custom M=1 cube matmul of the Orange
+ * Pi AIPro post; the vector-matrix product at M=1).
+ * W [N][K], x [M][K], y [M][N], all of type t; 1 <= M <= 16.
+ * Products are exact in fp32 and summed in fp32; y = round-to-nearest-even of
+ * the fp32 sum.  ws may be NULL (this call needs no workspace). */
+dg_status dg_gemv_f16(const void* W, const void* x, void* y, dg_ftype t, int M, int N, int K,
+                      void* ws, size_t ws_bytes, dg_stream stream);
+
+/* W8A8 ("vLLM Arm CPU optimizations", section "INT8 W8A8").
+ * W int8 [N][K], w_scale float [N] (per output channel), x int8 [M][K],
+ * x_scale float [M] (per token), 1 <= M <= 16.
+ * acc[m][n] = sum_k W[n][k] x[m][k] exactly in int32 (|acc| <= K*128*128
+ * must fit: K <= 131072); y[m][n] = fp16(float(acc) * w_scale[n] * x_scale[m]).
+ * acc_out (int32 [M][N]) receives acc when non-NULL. */
+dg_status dg_gemv_w8a8(const int8_t* W, const float* w_scale, const int8_t* x,
+                       const float* x_scale, void* y, int32_t* acc_out, int M, int N, int K,
+                       void* ws, size_t ws_bytes, dg_stream stream);
+
+/* Groupwise int4 weights ("vLLM Arm CPU optimizations", section "INT8 W4A8";
+ * fused INT4 dequantization of the Orange Pi AIPro post's closing paragraph).
+ * Wq uint8 [N][K/2]: byte j of a row holds k = 2j in bits 0-3 and k = 2j+1 in
+ * bits 4-7 as 4-bit two's complement (codes -8..7).  scales fp16
+ * [N][K/group_size]; group_size a multiple of 32 that divides K.
+ * W4A16 when x_i8 == NULL:  y = fp16( sum_g s[n][g] * P_g ),
+ *                           P_g = sum_{k in g} q[n][k] * x[m][k]   (fp32)
+ * W4A8 when x_i8 != NULL:   acc_g = sum_{k in g} q * x_i8 (exact int32),
+ *                           y = fp16( x_scale[m] * sum_g s[n][g] * acc_g ).
+ * x_f16 [M][K] is read for W4A16 and ignored for W4A8.  1 <= M <= 16. */
+dg_status dg_gemv_w4(const uint8_t* Wq, const void* scales, int group_size, const void* x_f16,
+                     const int8_t* x_i8, const float* x_scale, void* y, int M, int N, int K,
+                     void* ws, size_t ws_bytes, dg_stream stream);
+
+/* Per-token symmetric int8 activations for W8A8 / W4A8 (same page, same
+ * sections).  x fp16 [M][K] -> xq int8 [M][K], x_scale float [M]:
+ *   amax = max_k |x[m][k]|,  s = amax / 127 (IEEE fp32 division),
+ *   q = clamp(round-half-even(x / s), -127, 127);  s = 1, q = 0 if amax = 0. */
+dg_status dg_quantize_act_i8(const void* x, int8_t* xq, float* x_scale, int M, int K,
+                             dg_stream stream);
+
+/* Wide lm_head with fused greedy argmax (paragraph on the ~248k-vocabulary
+ * lm_head of the Orange Pi AIPro post, which splits it into 16 slices and
+ * reduces on the host; here one launch plus a tiny second pass).
+ * head->kind is DG_LINEAR_F16, DG_LINEAR_BF16, DG_LINEAR_W4A16 or
+ * DG_LINEAR_W4A8; head->M must be 1.  Writes fp32 logits[N] and
+ * token = the index of the largest logit, the lowest index on exact ties
+ * (+0 equals -0); a NaN logit never wins.  Needs dg_workspace_bytes(head, 1)
+ * bytes of workspace (per-CTA (value, index) partials). */
+dg_status dg_lm_head_argmax(const dg_linear* head, void* ws, size_t ws_bytes, dg_stream stream);
+
+/* One decode step's weight stream (graph-accelerated decode of EdgeFM,
+ * section 2.C): runs ops[0..n_ops) in order.  Consecutive ops of the same
+ * kind that read the same activations (same x / x_i8 pointers, same M and K)
+ * and are not lm_heads run as one launch (q|k|v, gate|up); every other
+ * boundary is a dependency: an op reads its activations only after every
+ * earlier op finished.  Weights and scales must stay unchanged during the
+ * step (they may be prefetched early).  Needs dg_workspace_bytes(ops, n_ops)
+ * bytes of workspace. */
+dg_status dg_decode_step_weights(const dg_linear* ops, int n_ops, void* ws, size_t ws_bytes,
+                                 dg_stream stream);
+
+/* Workspace bytes that dg_lm_head_argmax / dg_decode_step_weights need for
+ * these ops (0 when none is needed).  Host-only; touches no device. */
+size_t dg_workspace_bytes(const dg_linear* ops, int n_ops);
+
+/* Synchronizes `stream`, then reports DG_ERR_CUDA for a sticky CUDA error or
+ * DG_ERR_TIMEOUT if a bounded device-side wait gave up since the last call
+ * (clearing that flag).  DG_OK otherwise. */
+dg_status dg_check_device_status(dg_stream stream);
+
+/* Static, human-readable name of a status. */
+const char* dg_status_string(dg_status s);
+
+/* Measurement probes (not part of the method): stream `bytes` through HBM.
+ * dg_probe_copy copies src to dst (bytes read + bytes written);
+ * dg_probe_read reads src and writes one word per CTA to sink[0..1023].
+ * bytes must be a multiple of 16; pointers 16-byte aligned. */
+dg_status dg_probe_copy(const void* src, void* dst, size_t bytes, dg_stream stream);
+dg_status dg_probe_read(const void* src, size_t bytes, uint32_t* sink, dg_stream stream);
+
+/* Library version string. */
+const char* dg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DG_H_ */

@@ -1,0 +1,481 @@
+// C ABI of libdg.so: host-side validation, launch configuration and the
+// decode-step sequencer.  Nothing here allocates device memory or
+// synchronizes (except dg_check_device_status).
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "dg_internal.cuh"
+
+namespace dg {
+
+// ---- device facts ------------------------------------------------------------------
+
+static constexpr int kMaxDevices = 64;
+
+int sm_count() {
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDevices) {
+        const int v = cache[dev].load(std::memory_order_relaxed);
+        if (v) return v;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+size_t smem_optin_limit() {
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDevices) {
+        const int v = cache[dev].load(std::memory_order_relaxed);
+        if (v) return (size_t)v;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return 0;
+    if (dev >= 0 && dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
+    return (size_t)n;
+}
+
+// ---- tuning knobs ------------------------------------------------------------------
+// DG_TUNE="R=2,KS=1,CPS=4,PF=32768,PDL=1" overrides the launch heuristic (for
+// configuration sweeps); an unset key keeps the heuristic's choice.
+struct Tune {
+    int R = 0, KS = 0, CPS = 0, PF = -1, PDL = -1;
+};
+
+static Tune read_tune() {
+    Tune t;
+    const char* e = std::getenv("DG_TUNE");
+    if (!e) return t;
+    char buf[256];
+    std::strncpy(buf, e, sizeof buf - 1);
+    buf[sizeof buf - 1] = 0;
+    for (char* tok = std::strtok(buf, ","); tok; tok = std::strtok(nullptr, ",")) {
+        int v = 0;
+        if (std::sscanf(tok, "R=%d", &v) == 1) t.R = v;
+        else if (std::sscanf(tok, "KS=%d", &v) == 1) t.KS = v;
+        else if (std::sscanf(tok, "CPS=%d", &v) == 1) t.CPS = v;
+        else if (std::sscanf(tok, "PF=%d", &v) == 1) t.PF = v;
+        else if (std::sscanf(tok, "PDL=%d", &v) == 1) t.PDL = v;
+    }
+    return t;
+}
+
+static const Tune& tune() {
+    static Tune t = read_tune();
+    return t;
+}
+
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       void** args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = tune().PDL == 0 ? 0 : 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+// ---- launch configuration ------------------------------------------------------------
+
+static size_t elem_row_bytes(Fmt f, int K) {
+    switch (f) {
+        case F_F16:
+        case F_BF16: return (size_t)K * 2;
+        case F_I8: return (size_t)K;
+        default: return (size_t)K / 2;
+    }
+}
+
+static int pick_mt(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
+
+// Warps per row: a function of the row length only, so that a row's summation
+// order never depends on N (see the kernel's header comment).
+static int pick_ks(Fmt f, int K) {
+    const int t = tune().KS;
+    if (t == 1 || t == 2 || t == 4 || t == 8) return t;
+    const size_t rb = elem_row_bytes(f, K);
+    if (rb >= 16384) return 4;
+    if (rb >= 8192) return 2;
+    return 1;
+}
+
+static int pick_r(Fmt f, int MT) {
+    const int t = tune().R;
+    if (t == 1 || t == 2 || t == 4) return t;
+    if (MT <= 4) return 2;
+    if (f == F_I8) return MT >= 16 ? 4 : 2;
+    return 1;
+}
+
+static cudaError_t family(const GemvLaunch& L, const GemvParams* p, cudaStream_t s, int* occ) {
+    switch (L.fmt) {
+        case F_F16:
+        case F_BF16: return gemv_fp(L, p, s, occ);
+        case F_I8: return gemv_i8(L, p, s, occ);
+        case F_W4A16: return gemv_w4a16(L, p, s, occ);
+        case F_W4A8: return gemv_w4a8(L, p, s, occ);
+    }
+    return cudaErrorInvalidValue;
+}
+
+static int occupancy(const GemvLaunch& L) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, int, int, int, int>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_tuple(dev, (int)L.fmt, L.MT, L.R, (int)L.argmax, L.K, L.group);
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    int occ = 0;
+    if (family(L, nullptr, nullptr, &occ) != cudaSuccess) occ = 1;
+    if (occ < 1) occ = 1;
+    std::lock_guard<std::mutex> g(mu);
+    cache[key] = occ;
+    return occ;
+}
+
+// Fills L.grid and p.iters / ksplit / prefetch for a launch over p.N rows.
+static void configure(GemvLaunch& L, GemvParams& p) {
+    const int ks = pick_ks(L.fmt, p.K);
+    const int slots = kWarps / ks;
+    const int n_rg = (p.N + L.R - 1) / L.R;
+    const int need = (n_rg + slots - 1) / slots;
+    int cps = occupancy(L);
+    const int tc = tune().CPS;
+    cps = tc > 0 ? (tc < cps ? tc : cps) : (cps < 4 ? cps : 4);
+    int maxg = sm_count() * cps;
+    if (maxg < 1) maxg = 1;
+    if (L.argmax && maxg > kMaxArgCtas) maxg = kMaxArgCtas;
+    int grid = need < maxg ? need : maxg;
+    const int iters = (n_rg + grid * slots - 1) / (grid * slots);
+    grid = (n_rg + slots * iters - 1) / (slots * iters);  // even out the last pass
+    L.grid = grid;
+    p.ksplit = ks;
+    p.iters = iters;
+    p.prefetch_bytes = tune().PF >= 0 ? tune().PF : 32768;
+}
+
+static dg_status to_status(cudaError_t e) { return e == cudaSuccess ? DG_OK : DG_ERR_CUDA; }
+
+static bool al16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+static bool al2(const void* p) { return ((uintptr_t)p & 1u) == 0; }
+static bool al4(const void* p) { return ((uintptr_t)p & 3u) == 0; }
+
+// ---- op description shared by the entry points ------------------------------------------
+
+static Fmt fmt_of(int kind) {
+    switch (kind) {
+        case DG_LINEAR_F16: return F_F16;
+        case DG_LINEAR_BF16: return F_BF16;
+        case DG_LINEAR_W8A8: return F_I8;
+        case DG_LINEAR_W4A16: return F_W4A16;
+        default: return F_W4A8;
+    }
+}
+
+static bool quantized_act(int kind) { return kind == DG_LINEAR_W8A8 || kind == DG_LINEAR_W4A8; }
+
+// Validates one op without touching the device.  `quantize_here` is set when
+// the op carries fp16 activations that the caller wants quantized first.
+static dg_status validate(const dg_linear& op, bool allow_quant_input) {
+    if (op.kind < DG_LINEAR_F16 || op.kind > DG_LINEAR_W4A8) return DG_ERR_INVALID_ARG;
+    if (op.M < 1 || op.N < 1 || op.K < 1) return DG_ERR_INVALID_ARG;
+    if (op.M > 16) return DG_ERR_UNSUPPORTED;
+    if (!op.W) return DG_ERR_INVALID_ARG;
+    const bool head = op.token != nullptr;
+    if (head) {
+        if (op.M != 1 || !op.logits) return DG_ERR_INVALID_ARG;
+        if (op.kind == DG_LINEAR_W8A8) return DG_ERR_UNSUPPORTED;
+        if (!al4(op.logits) || !al4(op.token)) return DG_ERR_MISALIGNED;
+    } else if (op.kind == DG_LINEAR_W8A8) {
+        if (!op.y && !op.acc_out) return DG_ERR_INVALID_ARG;
+    } else if (!op.y) {
+        return DG_ERR_INVALID_ARG;
+    }
+    if (op.y && !al2(op.y)) return DG_ERR_MISALIGNED;
+    if (op.acc_out && !al4(op.acc_out)) return DG_ERR_MISALIGNED;
+    if (!al16(op.W)) return DG_ERR_MISALIGNED;
+    switch (op.kind) {
+        case DG_LINEAR_F16:
+        case DG_LINEAR_BF16:
+            if (op.K % 8) return DG_ERR_MISALIGNED;
+            break;
+        case DG_LINEAR_W8A8:
+            if (op.K % 16) return DG_ERR_MISALIGNED;
+            if (op.K > 131072) return DG_ERR_UNSUPPORTED;  // int32 accumulator range
+            if (!op.w_scale) return DG_ERR_INVALID_ARG;
+            if (!al4(op.w_scale)) return DG_ERR_MISALIGNED;
+            break;
+        default:  // int4
+            if (op.K % 32) return DG_ERR_MISALIGNED;
+            if (op.group_size < 32 || op.group_size % 32 || op.K % op.group_size)
+                return DG_ERR_UNSUPPORTED;
+            if (!op.w_scale) return DG_ERR_INVALID_ARG;
+            if (!al2(op.w_scale)) return DG_ERR_MISALIGNED;
+            break;
+    }
+    if (quantized_act(op.kind)) {
+        if (!op.x_i8 || !op.x_scale) return DG_ERR_INVALID_ARG;
+        if (!al16(op.x_i8) || !al4(op.x_scale)) return DG_ERR_MISALIGNED;
+        if (op.x && !allow_quant_input) return DG_ERR_INVALID_ARG;
+        if (op.x && (!al16(op.x) || op.K % 8)) return DG_ERR_MISALIGNED;
+    } else {
+        if (!op.x) return DG_ERR_INVALID_ARG;
+        if (!al16(op.x)) return DG_ERR_MISALIGNED;
+    }
+    return DG_OK;
+}
+
+static dg_status check_smem(const dg_linear& op) {
+    const size_t need = gemv_smem(fmt_of(op.kind), pick_mt(op.M), op.K, op.group_size);
+    const size_t lim = smem_optin_limit();
+    if (lim == 0) return DG_ERR_CUDA;
+    return need <= lim ? DG_OK : DG_ERR_UNSUPPORTED;
+}
+
+static void fill_common(GemvParams& p, const dg_linear& op) {
+    std::memset(&p, 0, sizeof p);
+    p.K = op.K;
+    p.M = op.M;
+    p.group = op.group_size >= 32 ? op.group_size : 32;
+    p.x = op.x;
+    p.xq = op.x_i8;
+    p.x_scale = op.x_scale;
+}
+
+// Launches ops[0..n) (same kind, same activations) as one kernel.
+static dg_status launch_group(const dg_linear* ops, int n, cudaStream_t s) {
+    GemvParams p;
+    fill_common(p, ops[0]);
+    int rows = 0;
+    for (int i = 0; i < n; ++i) {
+        Segment& g = p.seg[i];
+        g.W = ops[i].W;
+        g.scale = ops[i].w_scale;
+        g.y = ops[i].y;
+        g.acc_out = ops[i].acc_out;
+        g.row_begin = rows;
+        g.rows = ops[i].N;
+        rows += ops[i].N;
+    }
+    p.nseg = n;
+    p.N = rows;
+    GemvLaunch L{fmt_of(ops[0].kind), pick_mt(ops[0].M), 0, false, ops[0].K, p.group, 0};
+    L.R = pick_r(L.fmt, L.MT);
+    configure(L, p);
+    return to_status(family(L, &p, s, nullptr));
+}
+
+static dg_status launch_head(const dg_linear& op, void* ws, cudaStream_t s) {
+    GemvParams p;
+    fill_common(p, op);
+    p.seg[0].W = op.W;
+    p.seg[0].scale = op.w_scale;
+    p.seg[0].y = nullptr;
+    p.seg[0].row_begin = 0;
+    p.seg[0].rows = op.N;
+    p.nseg = 1;
+    p.N = op.N;
+    p.logits = op.logits;
+    p.part = static_cast<ArgPart*>(ws);
+    GemvLaunch L{fmt_of(op.kind), 1, 0, true, op.K, p.group, 0};
+    L.R = pick_r(L.fmt, 1);
+    configure(L, p);
+    cudaError_t e = family(L, &p, s, nullptr);
+    if (e != cudaSuccess) return DG_ERR_CUDA;
+    return to_status(launch_argmax_pass2(p.part, L.grid, op.token, s));
+}
+
+static size_t head_ws_bytes() { return (size_t)kMaxArgCtas * sizeof(ArgPart); }
+
+}  // namespace dg
+
+using namespace dg;
+
+extern "C" {
+
+const char* dg_status_string(dg_status s) {
+    switch (s) {
+        case DG_OK: return "DG_OK";
+        case DG_ERR_INVALID_ARG: return "DG_ERR_INVALID_ARG";
+        case DG_ERR_UNSUPPORTED: return "DG_ERR_UNSUPPORTED";
+        case DG_ERR_MISALIGNED: return "DG_ERR_MISALIGNED";
+        case DG_ERR_WORKSPACE: return "DG_ERR_WORKSPACE";
+        case DG_ERR_CUDA: return "DG_ERR_CUDA";
+        case DG_ERR_TIMEOUT: return "DG_ERR_TIMEOUT";
+    }
+    return "DG_ERR_UNKNOWN";
+}
+
+const char* dg_version(void) { return "dg 0.1 (sm_103a)"; }
+
+size_t dg_workspace_bytes(const dg_linear* ops, int n_ops) {
+    if (!ops || n_ops <= 0) return 0;
+    for (int i = 0; i < n_ops; ++i)
+        if (ops[i].token) return head_ws_bytes();
+    return 0;
+}
+
+dg_status dg_gemv_f16(const void* W, const void* x, void* y, dg_ftype t, int M, int N, int K,
+                      void* ws, size_t ws_bytes, dg_stream stream) {
+    (void)ws;
+    (void)ws_bytes;
+    if (t != DG_F16 && t != DG_BF16) return DG_ERR_INVALID_ARG;
+    dg_linear op;
+    std::memset(&op, 0, sizeof op);
+    op.kind = t == DG_F16 ? DG_LINEAR_F16 : DG_LINEAR_BF16;
+    op.M = M;
+    op.N = N;
+    op.K = K;
+    op.W = W;
+    op.x = x;
+    op.y = y;
+    dg_status st = validate(op, false);
+    if (st != DG_OK) return st;
+    if ((st = check_smem(op)) != DG_OK) return st;
+    return launch_group(&op, 1, stream);
+}
+
+dg_status dg_gemv_w8a8(const int8_t* W, const float* w_scale, const int8_t* x, const float* x_scale,
+                       void* y, int32_t* acc_out, int M, int N, int K, void* ws, size_t ws_bytes,
+                       dg_stream stream) {
+    (void)ws;
+    (void)ws_bytes;
+    dg_linear op;
+    std::memset(&op, 0, sizeof op);
+    op.kind = DG_LINEAR_W8A8;
+    op.M = M;
+    op.N = N;
+    op.K = K;
+    op.W = W;
+    op.w_scale = w_scale;
+    op.x_i8 = x;
+    op.x_scale = x_scale;
+    op.y = y;
+    op.acc_out = acc_out;
+    dg_status st = validate(op, false);
+    if (st != DG_OK) return st;
+    if ((st = check_smem(op)) != DG_OK) return st;
+    return launch_group(&op, 1, stream);
+}
+
+dg_status dg_gemv_w4(const uint8_t* Wq, const void* scales, int group_size, const void* x_f16,
+                     const int8_t* x_i8, const float* x_scale, void* y, int M, int N, int K,
+                     void* ws, size_t ws_bytes, dg_stream stream) {
+    (void)ws;
+    (void)ws_bytes;
+    dg_linear op;
+    std::memset(&op, 0, sizeof op);
+    op.kind = x_i8 ? DG_LINEAR_W4A8 : DG_LINEAR_W4A16;
+    op.M = M;
+    op.N = N;
+    op.K = K;
+    op.group_size = group_size;
+    op.W = Wq;
+    op.w_scale = scales;
+    op.x = x_i8 ? nullptr : x_f16;
+    op.x_i8 = x_i8;
+    op.x_scale = x_scale;
+    op.y = y;
+    dg_status st = validate(op, false);
+    if (st != DG_OK) return st;
+    if ((st = check_smem(op)) != DG_OK) return st;
+    return launch_group(&op, 1, stream);
+}
+
+dg_status dg_quantize_act_i8(const void* x, int8_t* xq, float* x_scale, int M, int K,
+                             dg_stream stream) {
+    if (!x || !xq || !x_scale || M < 1 || K < 1) return DG_ERR_INVALID_ARG;
+    if (K % 8 || !al16(x) || !al16(xq) || !al4(x_scale)) return DG_ERR_MISALIGNED;
+    return to_status(launch_quant_act(static_cast<const __half*>(x), xq, x_scale, M, K, stream));
+}
+
+dg_status dg_lm_head_argmax(const dg_linear* head, void* ws, size_t ws_bytes, dg_stream stream) {
+    if (!head || !head->token) return DG_ERR_INVALID_ARG;
+    dg_status st = validate(*head, false);
+    if (st != DG_OK) return st;
+    if (!ws) return DG_ERR_WORKSPACE;
+    if (ws_bytes < head_ws_bytes()) return DG_ERR_WORKSPACE;
+    if (!al16(ws)) return DG_ERR_MISALIGNED;
+    if ((st = check_smem(*head)) != DG_OK) return st;
+    return launch_head(*head, ws, stream);
+}
+
+dg_status dg_decode_step_weights(const dg_linear* ops, int n_ops, void* ws, size_t ws_bytes,
+                                 dg_stream stream) {
+    if (!ops || n_ops < 1) return DG_ERR_INVALID_ARG;
+    for (int i = 0; i < n_ops; ++i) {
+        dg_status st = validate(ops[i], true);
+        if (st != DG_OK) return st;
+    }
+    const size_t need = dg_workspace_bytes(ops, n_ops);
+    if (need && (!ws || ws_bytes < need)) return DG_ERR_WORKSPACE;
+    if (need && !al16(ws)) return DG_ERR_MISALIGNED;
+    for (int i = 0; i < n_ops; ++i) {
+        dg_status st = check_smem(ops[i]);
+        if (st != DG_OK) return st;
+    }
+    int i = 0;
+    while (i < n_ops) {
+        const dg_linear& a = ops[i];
+        int j = i + 1;
+        if (!a.token) {
+            while (j < n_ops && j - i < kMaxSeg) {
+                const dg_linear& b = ops[j];
+                if (b.token || b.kind != a.kind || b.M != a.M || b.K != a.K || b.x != a.x ||
+                    b.x_i8 != a.x_i8 || b.x_scale != a.x_scale || b.group_size != a.group_size)
+                    break;
+                ++j;
+            }
+        }
+        if (quantized_act(a.kind) && a.x) {
+            cudaError_t e = launch_quant_act(static_cast<const __half*>(a.x),
+                                             const_cast<int8_t*>(a.x_i8),
+                                             const_cast<float*>(a.x_scale), a.M, a.K, stream);
+            if (e != cudaSuccess) return DG_ERR_CUDA;
+        }
+        dg_status st = a.token ? launch_head(a, ws, stream) : launch_group(ops + i, j - i, stream);
+        if (st != DG_OK) return st;
+        i = j;
+    }
+    return DG_OK;
+}
+
+dg_status dg_check_device_status(dg_stream stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return DG_ERR_CUDA;
+    if (cudaPeekAtLastError() != cudaSuccess) return DG_ERR_CUDA;
+    return DG_OK;
+}
+
+dg_status dg_probe_copy(const void* src, void* dst, size_t bytes, dg_stream stream) {
+    if (!src || !dst || bytes == 0) return DG_ERR_INVALID_ARG;
+    if (bytes % 16 || !al16(src) || !al16(dst)) return DG_ERR_MISALIGNED;
+    return to_status(launch_probe_copy(src, dst, bytes, stream));
+}
+
+dg_status dg_probe_read(const void* src, size_t bytes, uint32_t* sink, dg_stream stream) {
+    if (!src || !sink || bytes == 0) return DG_ERR_INVALID_ARG;
+    if (bytes % 16 || !al16(src) || !al4(sink)) return DG_ERR_MISALIGNED;
+    return to_status(launch_probe_read(src, bytes, sink, stream));
+}
+
+}  // extern "C"

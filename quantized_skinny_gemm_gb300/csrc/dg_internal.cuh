@@ -1,0 +1,179 @@
+// Internal definitions shared by the sm_103a kernels of libdg.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dg.h"
+
+namespace dg {
+
+constexpr int kThreads = 256;          // one CTA = 8 warps
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxSeg = 4;             // matrices fused into one launch (q|k|v, gate|up)
+constexpr int kMaxArgCtas = 4096;      // cap on lm_head CTAs (bounds the partials buffer)
+
+// Element formats of the weight stream.
+enum Fmt : int { F_F16 = 0, F_BF16 = 1, F_I8 = 2, F_W4A16 = 3, F_W4A8 = 4 };
+
+// One matrix of a fused launch.  Global row r of the launch belongs to the
+// segment with row_begin <= r < row_begin + rows.
+struct Segment {
+    const void* W;       // row 0 of this matrix
+    const void* scale;   // W8A8: float [rows]; int4: half [rows][K/group]
+    void* y;             // [M][rows] (fp16 / bf16); may be null for an lm_head
+    int32_t* acc_out;    // W8A8 only, optional [M][rows]
+    int32_t row_begin;
+    int32_t rows;
+};
+
+// (value, index) partial of the greedy argmax.
+struct ArgPart {
+    float v;
+    int32_t i;
+};
+
+struct GemvParams {
+    Segment seg[kMaxSeg];
+    int nseg;
+    int N;                   // rows over all segments
+    int K;
+    int M;                   // real tokens (<= the kernel's MT)
+    int group;               // int4 group size (multiple of 32)
+    int ksplit;              // warps sharing one row group (splits K), 1/2/4/8
+    int iters;               // row-group loop trip count, uniform over the grid
+    int prefetch_bytes;      // per-CTA L2 prefetch issued before the dependency wait
+    const void* x;           // fp16 / bf16 [M][K]
+    const int8_t* xq;        // int8 [M][K]
+    const float* x_scale;    // [M]
+    float* logits;           // lm_head: fp32 [N]
+    ArgPart* part;           // lm_head: one partial per CTA
+};
+
+// ---- PTX helpers ------------------------------------------------------------
+
+// Streaming 16-byte load of weights: read-only path, not kept in L1.
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint16_t ld_stream_u16(const void* p) {
+    uint16_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+// Hint L2 to fetch [p, p + bytes); bytes a multiple of 16, p 16-byte aligned.
+// A prefetch never changes what a later load returns (L2 is the point of
+// coherence), so it is safe before the dependency wait.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel on the stream be
+// scheduled, and wait until the previous one completed (memory visible).
+// Both are no-ops when the launch carried no programmatic dependency.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// acc + a * b with a, b fp16 (or bf16) and acc fp32: the product is exact in
+// fp32 and one rounding happens, as in converting both and using fmaf.
+__device__ __forceinline__ float fma_f16(uint16_t a, uint16_t b, float acc) {
+    asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(acc) : "h"(a), "h"(b));
+    return acc;
+}
+__device__ __forceinline__ float fma_bf16(uint16_t a, uint16_t b, float acc) {
+    asm("fma.rn.f32.bf16 %0, %1, %2, %0;" : "+f"(acc) : "h"(a), "h"(b));
+    return acc;
+}
+
+__device__ __forceinline__ uint16_t lo16(uint32_t v) { return (uint16_t)(v & 0xFFFFu); }
+__device__ __forceinline__ uint16_t hi16(uint32_t v) { return (uint16_t)(v >> 16); }
+
+// Dot products of four byte lanes.
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// d = (a & b) ^ c in one LOP3.
+__device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) {
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) {
+    return *reinterpret_cast<__half2*>(&u);
+}
+
+// Total order of the greedy argmax: larger value first, then lower index; a
+// NaN value is never better.
+__device__ __forceinline__ bool arg_better(float v, int i, float bv, int bi) {
+    if (v != v) return false;
+    if (bv != bv) return true;
+    return v > bv || (v == bv && i < bi);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// ---- host-side launch helpers (defined in api.cu) ---------------------------
+
+int sm_count();                      // SMs of the current device (cached per device)
+size_t smem_optin_limit();           // max dynamic shared memory per CTA
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       void** args);
+
+// Which kernel instantiation a launch uses, and its grid.
+struct GemvLaunch {
+    Fmt fmt;
+    int MT;        // token tile: 1, 2, 4, 8 or 16 (>= M)
+    int R;         // rows per slot: 1, 2 or 4
+    bool argmax;   // lm_head epilogue (MT == 1)
+    int K, group;
+    int grid;
+};
+
+// Kernel families, one translation unit each.  With occ != nullptr they
+// report CTAs per SM instead of launching.
+cudaError_t gemv_fp(const GemvLaunch& L, const GemvParams* p, cudaStream_t s, int* occ);
+cudaError_t gemv_i8(const GemvLaunch& L, const GemvParams* p, cudaStream_t s, int* occ);
+cudaError_t gemv_w4a16(const GemvLaunch& L, const GemvParams* p, cudaStream_t s, int* occ);
+cudaError_t gemv_w4a8(const GemvLaunch& L, const GemvParams* p, cudaStream_t s, int* occ);
+size_t gemv_smem(Fmt f, int MT, int K, int group);
+
+cudaError_t launch_argmax_pass2(const ArgPart* part, int nparts, int32_t* token, cudaStream_t s);
+cudaError_t launch_quant_act(const __half* x, int8_t* xq, float* s, int M, int K,
+                             cudaStream_t st);
+cudaError_t launch_probe_copy(const void* src, void* dst, size_t bytes, cudaStream_t s);
+cudaError_t launch_probe_read(const void* src, size_t bytes, uint32_t* sink, cudaStream_t s);
+
+}  // namespace dg

@@ -1,0 +1,561 @@
+// Weight-streaming skinny GEMV: one kernel skeleton, one policy per weight format.
+//
+// Work decomposition.  A CTA is 8 warps.  `ksplit` consecutive warps form a
+// slot that owns one row group of R rows; the slot's warps split the row's
+// 16-byte chunks: warp kw of the slot, lane l, visits chunks
+//     c_j = (j * ksplit + kw) * 32 + l,   j = 0, 1, ...
+// so each warp-wide load reads 512 contiguous bytes of a weight row, and one
+// lane accumulates its chunks in ascending j.  Lane sums meet in a fixed
+// xor-butterfly, then the slot's warps add in kw order.  The order depends
+// only on K and ksplit (which the host picks from K alone), never on N, the
+// row's offset or the grid, so a row slice of W reproduces the full matrix's
+// rows bit for bit (the 16-slice lm_head split of the Orange Pi AIPro post
+// holds exactly).
+//
+// Row groups are dealt to slots grid-stride, with a uniform trip count so that
+// every warp reaches the CTA-wide barriers.  Activations are staged once per
+// CTA in shared memory (permuted where the int4 unpack wants it); weights
+// bypass L1 and are read with 16-byte vector loads, U chunks per lane in
+// flight per row.
+#pragma once
+
+#include <climits>
+#include <cmath>
+
+#include "dg_internal.cuh"
+
+namespace dg {
+
+// ---- per-row addressing -------------------------------------------------------
+
+struct RowRef {
+    const unsigned char* w;   // weight row
+    const void* scale;        // segment scale base
+    void* y;                  // segment output base
+    int32_t* acc_out;
+    int local;                // row index inside its segment
+    int seg_rows;             // rows of its segment (output row stride)
+    int global;               // row index over all segments
+    bool valid;
+};
+
+__device__ __forceinline__ RowRef locate(const GemvParams& p, int r, size_t row_bytes,
+                                         const RowRef& fallback) {
+    RowRef rr = fallback;
+    rr.valid = false;
+    if (r >= p.N) return rr;
+    int s = 0;
+#pragma unroll
+    for (int i = 1; i < kMaxSeg; ++i)
+        if (i < p.nseg && r >= p.seg[i].row_begin) s = i;
+    const Segment& sg = p.seg[s];
+    rr.local = r - sg.row_begin;
+    rr.w = static_cast<const unsigned char*>(sg.W) + (size_t)rr.local * row_bytes;
+    rr.scale = sg.scale;
+    rr.y = sg.y;
+    rr.acc_out = sg.acc_out;
+    rr.seg_rows = sg.rows;
+    rr.global = r;
+    rr.valid = true;
+    return rr;
+}
+
+template <typename T>
+__device__ __forceinline__ int to_bits(T v);
+template <>
+__device__ __forceinline__ int to_bits<float>(float v) { return __float_as_int(v); }
+template <>
+__device__ __forceinline__ int to_bits<int>(int v) { return v; }
+template <typename T>
+__device__ __forceinline__ T from_bits(int v);
+template <>
+__device__ __forceinline__ float from_bits<float>(int v) { return __int_as_float(v); }
+template <>
+__device__ __forceinline__ int from_bits<int>(int v) { return v; }
+
+// ---- format policies ------------------------------------------------------------
+
+// fp16 / bf16 weights and activations; 8 elements per chunk.
+template <bool BF16>
+struct PolicyFP {
+    static constexpr int kElems = 8;
+    using Acc = float;
+    struct Chunk { uint4 w; };
+
+    __host__ __device__ static size_t row_bytes(int K) { return (size_t)K * 2; }
+    __host__ __device__ static size_t x_bytes(int MT, int K, int) { return (size_t)MT * K * 2; }
+
+    __device__ static void stage_x(const GemvParams& p, unsigned char* xs, int MT) {
+        const int per_row = p.K / 8;
+        const uint4* src = static_cast<const uint4*>(p.x);
+        uint4* dst = reinterpret_cast<uint4*>(xs);
+        for (int i = threadIdx.x; i < MT * per_row; i += kThreads) {
+            const int m = i / per_row;
+            dst[i] = m < p.M ? src[i] : make_uint4(0, 0, 0, 0);
+        }
+    }
+    __device__ __forceinline__ static void load(Chunk& ch, const RowRef& r, int c, int, int) {
+        ch.w = ld_stream16(r.w + (size_t)c * 16);
+    }
+    __device__ __forceinline__ static float mac2(uint32_t w, uint32_t x, float a) {
+        if (BF16) {
+            a = fma_bf16(lo16(w), lo16(x), a);
+            return fma_bf16(hi16(w), hi16(x), a);
+        }
+        a = fma_f16(lo16(w), lo16(x), a);
+        return fma_f16(hi16(w), hi16(x), a);
+    }
+    template <int MT>
+    __device__ __forceinline__ static void mac(Acc (&acc)[MT], const Chunk& ch,
+                                               const unsigned char* xs, int c, int K) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            const uint4 xv = *reinterpret_cast<const uint4*>(xs + ((size_t)m * K + (size_t)c * 8) * 2);
+            float a = acc[m];
+            a = mac2(ch.w.x, xv.x, a);
+            a = mac2(ch.w.y, xv.y, a);
+            a = mac2(ch.w.z, xv.z, a);
+            a = mac2(ch.w.w, xv.w, a);
+            acc[m] = a;
+        }
+    }
+    __device__ static float finish(const GemvParams&, const RowRef&, int, Acc a) { return a; }
+    __device__ static void store(const GemvParams& p, const RowRef& r, int m, Acc a) {
+        const size_t o = (size_t)m * r.seg_rows + r.local;
+        if (BF16)
+            static_cast<__nv_bfloat16*>(r.y)[o] = __float2bfloat16_rn(a);
+        else
+            static_cast<__half*>(r.y)[o] = __float2half_rn(a);
+        (void)p;
+    }
+};
+
+// int8 weights x int8 activations, exact int32 sums; 16 elements per chunk.
+struct PolicyI8 {
+    static constexpr int kElems = 16;
+    using Acc = int;
+    struct Chunk { uint4 w; };
+
+    __host__ __device__ static size_t row_bytes(int K) { return (size_t)K; }
+    __host__ __device__ static size_t x_bytes(int MT, int K, int) { return (size_t)MT * K; }
+
+    __device__ static void stage_x(const GemvParams& p, unsigned char* xs, int MT) {
+        const int per_row = p.K / 16;
+        const uint4* src = reinterpret_cast<const uint4*>(p.xq);
+        uint4* dst = reinterpret_cast<uint4*>(xs);
+        for (int i = threadIdx.x; i < MT * per_row; i += kThreads) {
+            const int m = i / per_row;
+            dst[i] = m < p.M ? src[i] : make_uint4(0, 0, 0, 0);
+        }
+    }
+    __device__ __forceinline__ static void load(Chunk& ch, const RowRef& r, int c, int, int) {
+        ch.w = ld_stream16(r.w + (size_t)c * 16);
+    }
+    template <int MT>
+    __device__ __forceinline__ static void mac(Acc (&acc)[MT], const Chunk& ch,
+                                               const unsigned char* xs, int c, int K) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)m * K + (size_t)c * 16);
+            int a = acc[m];
+            a = dp4a_ss(ch.w.x, xv.x, a);
+            a = dp4a_ss(ch.w.y, xv.y, a);
+            a = dp4a_ss(ch.w.z, xv.z, a);
+            a = dp4a_ss(ch.w.w, xv.w, a);
+            acc[m] = a;
+        }
+    }
+    __device__ static float finish(const GemvParams& p, const RowRef& r, int m, Acc a) {
+        const float sw = __ldg(static_cast<const float*>(r.scale) + r.local);
+        return (float)a * sw * __ldg(p.x_scale + m);
+    }
+    __device__ static void store(const GemvParams& p, const RowRef& r, int m, Acc a) {
+        const size_t o = (size_t)m * r.seg_rows + r.local;
+        if (r.acc_out) r.acc_out[o] = a;
+        if (r.y) static_cast<__half*>(r.y)[o] = __float2half_rn(finish(p, r, m, a));
+    }
+};
+
+// Unpacks one word of 8 int4 codes (k0..k7: byte j holds k = 2j in bits 0-3
+// and k = 2j+1 in bits 4-7) into four fp16 pairs (c0,c4) (c1,c5) (c2,c6)
+// (c3,c7), exactly.  A nibble n stands for c = n - 16*(n >= 8), so n ^ 8 =
+// c + 8 in [0, 15].  Placing n ^ 8 in the low mantissa bits of the fp16 1024
+// gives 1024 + (c + 8); subtracting 1032 leaves c.  For the nibbles in bits
+// 4-7 of a half the mantissa holds 16 * (c + 8), so (1024 + 16(c+8)) / 16 - 72
+// = c, computed by one fused multiply-add with an exact result.
+__device__ __forceinline__ void unpack_int4x8_f16(uint32_t w, uint32_t (&q)[4]) {
+    const uint32_t w8 = w >> 8;
+    const __half2 k1032 = __floats2half2_rn(1032.f, 1032.f);
+    const __half2 k16th = __floats2half2_rn(0.0625f, 0.0625f);
+    const __half2 k72 = __floats2half2_rn(-72.f, -72.f);
+    q[0] = h2_as_u32(__hsub2(u32_as_h2(and_xor(w, 0x000F000Fu, 0x64086408u)), k1032));
+    q[1] = h2_as_u32(__hfma2(u32_as_h2(and_xor(w, 0x00F000F0u, 0x64806480u)), k16th, k72));
+    q[2] = h2_as_u32(__hsub2(u32_as_h2(and_xor(w8, 0x000F000Fu, 0x64086408u)), k1032));
+    q[3] = h2_as_u32(__hfma2(u32_as_h2(and_xor(w8, 0x00F000F0u, 0x64806480u)), k16th, k72));
+}
+
+// Groupwise int4 weights with fp16 activations; 32 codes (one 32-group) per chunk.
+// Activations are staged per 8-block in the order x0 x4 x1 x5 x2 x6 x3 x7 so
+// that a 16-byte shared load lines up with the unpacked pairs.
+struct PolicyW4A16 {
+    static constexpr int kElems = 32;
+    using Acc = float;
+    struct Chunk { uint4 w; uint16_t s; };
+
+    __host__ __device__ static size_t row_bytes(int K) { return (size_t)K / 2; }
+    __host__ __device__ static size_t x_bytes(int MT, int K, int) { return (size_t)MT * K * 2; }
+
+    __device__ static void stage_x(const GemvParams& p, unsigned char* xs, int MT) {
+        const int per_row = p.K / 8;
+        const uint4* src = static_cast<const uint4*>(p.x);
+        uint4* dst = reinterpret_cast<uint4*>(xs);
+        for (int i = threadIdx.x; i < MT * per_row; i += kThreads) {
+            const int m = i / per_row;
+            uint4 v = m < p.M ? src[i] : make_uint4(0, 0, 0, 0);
+            // halves h0..h7 -> h0 h4 h1 h5 h2 h6 h3 h7
+            uint4 o;
+            o.x = __byte_perm(v.x, v.z, 0x5410);  // h0, h4
+            o.y = __byte_perm(v.x, v.z, 0x7632);  // h1, h5
+            o.z = __byte_perm(v.y, v.w, 0x5410);  // h2, h6
+            o.w = __byte_perm(v.y, v.w, 0x7632);  // h3, h7
+            dst[i] = o;
+        }
+    }
+    // Chunk c covers codes [32c, 32c + 32) of the row: group c / cpg, where
+    // cpg = group / 32 chunks share one scale; a row holds gk scales.
+    __device__ __forceinline__ static void load(Chunk& ch, const RowRef& r, int c, int gk, int cpg) {
+        ch.w = ld_stream16(r.w + (size_t)c * 16);
+        ch.s = ld_stream_u16(static_cast<const uint16_t*>(r.scale) + (size_t)r.local * gk + c / cpg);
+    }
+    template <int MT>
+    __device__ __forceinline__ static void mac(Acc (&acc)[MT], const Chunk& ch,
+                                               const unsigned char* xs, int c, int K) {
+        uint32_t q[4][4];
+        unpack_int4x8_f16(ch.w.x, q[0]);
+        unpack_int4x8_f16(ch.w.y, q[1]);
+        unpack_int4x8_f16(ch.w.z, q[2]);
+        unpack_int4x8_f16(ch.w.w, q[3]);
+        const float s = __half2float(__ushort_as_half(ch.s));
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            const unsigned char* xb = xs + ((size_t)m * K + (size_t)c * 32) * 2;
+            float P = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 xv = *reinterpret_cast<const uint4*>(xb + i * 16);
+                P = fma_f16(lo16(q[i][0]), lo16(xv.x), P);
+                P = fma_f16(hi16(q[i][0]), hi16(xv.x), P);
+                P = fma_f16(lo16(q[i][1]), lo16(xv.y), P);
+                P = fma_f16(hi16(q[i][1]), hi16(xv.y), P);
+                P = fma_f16(lo16(q[i][2]), lo16(xv.z), P);
+                P = fma_f16(hi16(q[i][2]), hi16(xv.z), P);
+                P = fma_f16(lo16(q[i][3]), lo16(xv.w), P);
+                P = fma_f16(hi16(q[i][3]), hi16(xv.w), P);
+            }
+            acc[m] = fmaf(P, s, acc[m]);
+        }
+    }
+    __device__ static float finish(const GemvParams&, const RowRef&, int, Acc a) { return a; }
+    __device__ static void store(const GemvParams& p, const RowRef& r, int m, Acc a) {
+        static_cast<__half*>(r.y)[(size_t)m * r.seg_rows + r.local] = __float2half_rn(a);
+        (void)p;
+    }
+};
+
+// Groupwise int4 weights with int8 activations.  Codes are biased to c + 8 in
+// [0, 15] (one LOP3 per four codes) and multiplied with dp4a (unsigned x
+// signed); the bias is removed exactly with the chunk's activation sum:
+// sum (c+8) x - 8 sum x = sum c x.  Activations are staged per 8-block as
+// x0 x2 x4 x6 | x1 x3 x5 x7 (even codes sit in low nibbles), followed by
+// the int32 sum of each 32-chunk.
+struct PolicyW4A8 {
+    static constexpr int kElems = 32;
+    using Acc = float;
+    struct Chunk { uint4 w; uint16_t s; };
+
+    __host__ __device__ static size_t row_bytes(int K) { return (size_t)K / 2; }
+    __host__ __device__ static size_t x_bytes(int MT, int K, int) {
+        return (size_t)MT * K + (size_t)MT * (K / 32) * 4;
+    }
+
+    __device__ static void stage_x(const GemvParams& p, unsigned char* xs, int MT) {
+        const int K = p.K;
+        const int per_row = K / 8;
+        const uint2* src = reinterpret_cast<const uint2*>(p.xq);
+        uint2* dst = reinterpret_cast<uint2*>(xs);
+        for (int i = threadIdx.x; i < MT * per_row; i += kThreads) {
+            const int m = i / per_row;
+            uint2 v = m < p.M ? src[i] : make_uint2(0, 0);
+            uint2 o;
+            o.x = __byte_perm(v.x, v.y, 0x6420);  // x0 x2 x4 x6
+            o.y = __byte_perm(v.x, v.y, 0x7531);  // x1 x3 x5 x7
+            dst[i] = o;
+        }
+        int* xsum = reinterpret_cast<int*>(xs + (size_t)MT * K);
+        const int nch = K / 32;
+        const uint4* src16 = reinterpret_cast<const uint4*>(p.xq);
+        for (int i = threadIdx.x; i < MT * nch; i += kThreads) {
+            const int m = i / nch;
+            int s = 0;
+            if (m < p.M) {
+                const uint4 a = src16[2 * i], b = src16[2 * i + 1];
+                s = dp4a_ss(a.x, 0x01010101u, s);
+                s = dp4a_ss(a.y, 0x01010101u, s);
+                s = dp4a_ss(a.z, 0x01010101u, s);
+                s = dp4a_ss(a.w, 0x01010101u, s);
+                s = dp4a_ss(b.x, 0x01010101u, s);
+                s = dp4a_ss(b.y, 0x01010101u, s);
+                s = dp4a_ss(b.z, 0x01010101u, s);
+                s = dp4a_ss(b.w, 0x01010101u, s);
+            }
+            xsum[i] = s;
+        }
+    }
+    __device__ __forceinline__ static void load(Chunk& ch, const RowRef& r, int c, int gk, int cpg) {
+        ch.w = ld_stream16(r.w + (size_t)c * 16);
+        ch.s = ld_stream_u16(static_cast<const uint16_t*>(r.scale) + (size_t)r.local * gk + c / cpg);
+    }
+    template <int MT>
+    __device__ __forceinline__ static void mac(Acc (&acc)[MT], const Chunk& ch,
+                                               const unsigned char* xs, int c, int K) {
+        uint32_t lo[4], hi[4];
+        const uint32_t wv[4] = {ch.w.x, ch.w.y, ch.w.z, ch.w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            lo[i] = and_xor(wv[i], 0x0F0F0F0Fu, 0x08080808u);
+            hi[i] = and_xor(wv[i] >> 4, 0x0F0F0F0Fu, 0x08080808u);
+        }
+        const float s = __half2float(__ushort_as_half(ch.s));
+        const int* xsum = reinterpret_cast<const int*>(xs + (size_t)MT * K);
+        const int nch = K / 32;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            const unsigned char* xb = xs + (size_t)m * K + (size_t)c * 32;
+            const uint4 x0 = *reinterpret_cast<const uint4*>(xb);
+            const uint4 x1 = *reinterpret_cast<const uint4*>(xb + 16);
+            int a = -8 * xsum[m * nch + c];
+            a = dp4a_us(lo[0], x0.x, a);
+            a = dp4a_us(hi[0], x0.y, a);
+            a = dp4a_us(lo[1], x0.z, a);
+            a = dp4a_us(hi[1], x0.w, a);
+            a = dp4a_us(lo[2], x1.x, a);
+            a = dp4a_us(hi[2], x1.y, a);
+            a = dp4a_us(lo[3], x1.z, a);
+            a = dp4a_us(hi[3], x1.w, a);
+            acc[m] = fmaf((float)a, s, acc[m]);
+        }
+    }
+    __device__ static float finish(const GemvParams& p, const RowRef&, int m, Acc a) {
+        return __ldg(p.x_scale + m) * a;
+    }
+    __device__ static void store(const GemvParams& p, const RowRef& r, int m, Acc a) {
+        static_cast<__half*>(r.y)[(size_t)m * r.seg_rows + r.local] =
+            __float2half_rn(finish(p, r, m, a));
+    }
+};
+
+// ---- the kernel -----------------------------------------------------------------
+
+// Chunks in flight per lane and row, by the number of accumulators.
+template <int MT, int R>
+struct Unroll {
+    static constexpr int v = (MT * R <= 2) ? 8 : (MT * R <= 8 ? 4 : 2);
+};
+
+template <class P, int MT, int R, bool ARGMAX>
+__global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvParams p) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    using Acc = typename P::Acc;
+    constexpr int U = Unroll<MT, R>::v;
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int ks = p.ksplit;
+    const int slots = kWarps / ks;
+    const int slot = warp / ks, kw = warp - slot * ks;
+    const int K = p.K;
+    const size_t rb = P::row_bytes(K);
+    const int nchunks = K / P::kElems;
+    const int gk = K / p.group;   // scale entries per row (int4)
+    const int cpg = p.group / 32; // 32-code chunks per scale group (int4)
+    const int n_rg = (p.N + R - 1) / R;
+
+    // Weights do not depend on the previous kernel: warm L2 with the rows this
+    // CTA streams first while that kernel drains.
+    if (p.prefetch_bytes > 0 && threadIdx.x < slots * R) {
+        const int r = blockIdx.x * slots * R + threadIdx.x;
+        RowRef z{};
+        const RowRef rr = locate(p, r, rb, z);
+        if (rr.valid) {
+            const size_t cap = (size_t)p.prefetch_bytes / (size_t)(slots * R);
+            uint32_t n = (uint32_t)(rb < cap ? rb : cap);
+            n &= ~15u;
+            if (n) prefetch_l2(rr.w, n);
+        }
+    }
+    griddep_launch_dependents();
+    griddep_wait();
+
+    P::stage_x(p, smem, MT);
+    __syncthreads();
+    int* red = reinterpret_cast<int*>(smem + ((P::x_bytes(MT, K, p.group) + 15) & ~(size_t)15));
+
+    float best_v = NAN;
+    int best_i = INT_MAX;
+
+    for (int it = 0; it < p.iters; ++it) {
+        const int rg = (it * (int)gridDim.x + (int)blockIdx.x) * slots + slot;
+        const bool active = rg < n_rg;
+        RowRef rows[R];
+        {
+            RowRef z{};
+            const RowRef first = active ? locate(p, rg * R, rb, z) : z;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                rows[r] = active ? locate(p, rg * R + r, rb, first) : first;
+                if (!rows[r].valid) rows[r].w = first.w;  // load a valid row, drop its result
+            }
+        }
+        Acc acc[R][MT];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) acc[r][m] = Acc(0);
+
+        if (active) {
+            const int step = ks * 32;
+            int c = kw * 32 + lane;
+            for (; c + (U - 1) * step < nchunks; c += U * step) {
+                typename P::Chunk ch[U][R];
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int r = 0; r < R; ++r) P::load(ch[u][r], rows[r], c + u * step, gk, cpg);
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int r = 0; r < R; ++r)
+                        P::template mac<MT>(acc[r], ch[u][r], smem, c + u * step, K);
+            }
+            for (; c < nchunks; c += step) {
+                typename P::Chunk ch[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) P::load(ch[r], rows[r], c, gk, cpg);
+#pragma unroll
+                for (int r = 0; r < R; ++r) P::template mac<MT>(acc[r], ch[r], smem, c, K);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) acc[r][m] = warp_sum(acc[r][m]);
+
+        if (ks > 1) {
+            if (lane == 0) {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) red[(warp * R + r) * MT + m] = to_bits(acc[r][m]);
+            }
+            __syncthreads();
+            if (kw == 0) {
+                for (int j = 1; j < ks; ++j) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r)
+#pragma unroll
+                        for (int m = 0; m < MT; ++m)
+                            acc[r][m] += from_bits<Acc>(red[((warp + j) * R + r) * MT + m]);
+                }
+            }
+            __syncthreads();
+        }
+
+        if (kw == 0 && active) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                if (!rows[r].valid) continue;
+                if (ARGMAX) {
+                    const float v = P::finish(p, rows[r], 0, acc[r][0]);
+                    if (lane == 0) {
+                        p.logits[rows[r].global] = v;
+                        if (arg_better(v, rows[r].global, best_v, best_i)) {
+                            best_v = v;
+                            best_i = rows[r].global;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int m = 0; m < MT; ++m)
+                        if (m < p.M && lane == ((r * MT + m) & 31)) P::store(p, rows[r], m, acc[r][m]);
+                }
+            }
+        }
+    }
+
+    if (ARGMAX) {
+        ArgPart* cta = reinterpret_cast<ArgPart*>(red + kWarps * 4 * MT);
+        if (lane == 0) {
+            cta[warp].v = best_v;
+            cta[warp].i = best_i;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float bv = NAN;
+            int bi = INT_MAX;
+            for (int w = 0; w < kWarps; ++w)
+                if (arg_better(cta[w].v, cta[w].i, bv, bi)) {
+                    bv = cta[w].v;
+                    bi = cta[w].i;
+                }
+            p.part[blockIdx.x].v = bv;
+            p.part[blockIdx.x].i = bi;
+        }
+    }
+}
+
+template <class P>
+size_t smem_bytes_for(int MT, int K, int group) {
+    size_t x = (P::x_bytes(MT, K, group) + 15) & ~(size_t)15;
+    return x + (size_t)kWarps * 4 * MT * 4 + (size_t)kWarps * sizeof(ArgPart);
+}
+
+// Launches one instantiation, or (occ != nullptr) reports how many of its CTAs
+// fit on one SM with this much dynamic shared memory.
+template <class P, int MT, int R, bool ARGMAX>
+cudaError_t run_one(const GemvParams* p, int grid, size_t smem, cudaStream_t s, int* occ) {
+    auto fn = k_gemv<P, MT, R, ARGMAX>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    if (occ) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, fn, kThreads, smem);
+    void* args[] = {const_cast<GemvParams*>(p)};
+    return launch_pdl(reinterpret_cast<const void*>(fn), dim3(grid), dim3(kThreads), smem, s, args);
+}
+
+template <class P, int MT, bool ARGMAX>
+cudaError_t run_r(int R, const GemvParams* p, int grid, size_t smem, cudaStream_t s, int* occ) {
+    switch (R) {
+        case 1: return run_one<P, MT, 1, ARGMAX>(p, grid, smem, s, occ);
+        case 2: return run_one<P, MT, 2, ARGMAX>(p, grid, smem, s, occ);
+        case 4: return run_one<P, MT, 4, ARGMAX>(p, grid, smem, s, occ);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <class P>
+cudaError_t run_family(const GemvLaunch& L, const GemvParams* p, cudaStream_t s, int* occ) {
+    const size_t smem = smem_bytes_for<P>(L.MT, L.K, L.group);
+    if (L.argmax)
+        return L.MT == 1 ? run_r<P, 1, true>(L.R, p, L.grid, smem, s, occ) : cudaErrorInvalidValue;
+    switch (L.MT) {
+        case 1: return run_r<P, 1, false>(L.R, p, L.grid, smem, s, occ);
+        case 2: return run_r<P, 2, false>(L.R, p, L.grid, smem, s, occ);
+        case 4: return run_r<P, 4, false>(L.R, p, L.grid, smem, s, occ);
+        case 8: return run_r<P, 8, false>(L.R, p, L.grid, smem, s, occ);
+        case 16: return run_r<P, 16, false>(L.R, p, L.grid, smem, s, occ);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace dg

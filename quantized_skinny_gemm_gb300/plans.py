@@ -1,0 +1,183 @@
+"""Decode-step plans: a decoder's weights, inputs and outputs on the device,
+marshalled once into the dg_linear array that dg_decode_step_weights runs.
+
+The op order is the decoder's: per layer q, k, v (sharing x_attn), o, gate, up
+(sharing x_mlp), down, then the lm_head.  The library fuses each run of ops
+that share an input into one launch (q|k|v, gate|up).
+
+Memory layout: weights (and scales) are separate, resident tensors, loaded
+once; every activation a step reads lives in one input arena and every result
+it writes in one output arena (256-byte aligned views), so moving a step's
+inputs in and its results out is one copy each way.
+"""
+from dataclasses import dataclass, field
+from typing import Dict, List, Optional
+
+import torch
+
+from . import LINEAR_F16, LINEAR_W4A16, LINEAR_W4A8, StepPlan, linear
+
+
+class Arena:
+    """One device buffer carved into aligned views: reserve(), then build()."""
+
+    def __init__(self, align=256):
+        self.align = align
+        self.specs = []
+        self.size = 0
+        self.buf = None
+
+    def reserve(self, shape, dtype):
+        n = 1
+        for s in shape:
+            n *= s
+        nbytes = n * torch.tensor([], dtype=dtype).element_size()
+        off = self.size
+        self.size = (off + nbytes + self.align - 1) // self.align * self.align
+        self.specs.append((off, tuple(shape), dtype, nbytes))
+        return len(self.specs) - 1
+
+    def build(self, device):
+        self.buf = torch.zeros(max(self.size, self.align), dtype=torch.uint8, device=device)
+        return [self.buf[o:o + nb].view(dt).view(shape) for o, shape, dt, nb in self.specs]
+
+
+@dataclass
+class DeviceStep:
+    plan: StepPlan
+    ws: Optional[torch.Tensor]
+    inputs: List[Dict[str, torch.Tensor]]      # per layer: name -> device fp16 [M][K]
+    outputs: List[Dict[str, torch.Tensor]]     # per layer: matrix name -> device y [M][N]
+    in_arena: torch.Tensor                     # every input of the step (uint8 bytes)
+    out_arena: torch.Tensor                    # every result of the step (uint8 bytes)
+    weight_bytes: int                          # weights + scales streamed per step
+    n_launches: int                            # kernel launches per step
+    head_logits: Optional[torch.Tensor] = None
+    head_token: Optional[torch.Tensor] = None
+    head_input: Optional[torch.Tensor] = None
+    keep: list = field(default_factory=list)
+
+
+def _nbytes(t):
+    return t.numel() * t.element_size()
+
+
+def count_launches(ops):
+    """Launches dg_decode_step_weights issues for these ops (its fusion rule:
+    same kind, M, K, group and activation pointers, up to 4 ops, no lm_head;
+    an lm_head adds its second argmax pass; fp16 inputs of the quantized-
+    activation kinds add one quantization launch per fused run)."""
+    n, i = 0, 0
+    while i < len(ops):
+        a = ops[i]
+        j = i + 1
+        if not a.token:
+            while j < len(ops) and j - i < 4:
+                b = ops[j]
+                if (b.token or b.kind != a.kind or b.M != a.M or b.K != a.K or b.x != a.x
+                        or b.x_i8 != a.x_i8 or b.x_scale != a.x_scale
+                        or b.group_size != a.group_size):
+                    break
+                j += 1
+        n += 1
+        if a.token:
+            n += 1
+        if a.kind == LINEAR_W4A8 and a.x:
+            n += 1
+        i = j
+    return n
+
+
+def fp16_decode_step(layers, device, M=1) -> DeviceStep:
+    """layers: synth.decode_fp16_workload(...) output (host tensors)."""
+    ain, aout = Arena(), Arena()
+    in_ids = [{k: ain.reserve(v.shape, torch.float16) for k, v in L.inputs.items()}
+              for L in layers]
+    out_ids = [{lin.name: aout.reserve((M, lin.N), torch.float16) for lin in L.linears}
+               for L in layers]
+    in_views, out_views = ain.build(device), aout.build(device)
+    ops, keep, ins, outs = [], [], [], []
+    wbytes = 0
+    for L, iid, oid in zip(layers, in_ids, out_ids):
+        xin = {}
+        for k, v in L.inputs.items():
+            xin[k] = in_views[iid[k]]
+            xin[k].copy_(v)
+        ys = {}
+        for lin in L.linears:
+            W = lin.W.to(device)
+            y = out_views[oid[lin.name]]
+            ops.append(linear(LINEAR_F16, W, M, lin.N, lin.K, x=xin[lin.x_name], y=y))
+            keep.append(W)
+            ys[lin.name] = y
+            wbytes += _nbytes(W)
+        ins.append(xin)
+        outs.append(ys)
+    keep += [ain.buf, aout.buf]
+    plan = StepPlan(ops, keep)
+    return DeviceStep(plan, None, ins, outs, ain.buf, aout.buf, wbytes, count_launches(ops),
+                      keep=keep)
+
+
+def int4_decode_step(layers, head, x_head, device, act="a16", M=1, group=32) -> DeviceStep:
+    """layers/head/x_head: synth.decode_int4_workload(...) output (host tensors).
+    act="a16": fp16 activations; act="a8": per-token int8 activations, quantized
+    inside the step from the fp16 inputs (scratch codes live in the workspace
+    tensors kept by the plan)."""
+    kind = LINEAR_W4A16 if act == "a16" else LINEAR_W4A8
+    ain, aout = Arena(), Arena()
+    in_ids = [{k: ain.reserve(v.shape, torch.float16) for k, v in L.inputs.items()}
+              for L in layers]
+    out_ids = [{lin.name: aout.reserve((M, lin.N), torch.float16) for lin in L.linears}
+               for L in layers]
+    head_ids = None
+    if head is not None:
+        head_ids = (ain.reserve(x_head.shape, torch.float16),
+                    aout.reserve((head.N,), torch.float32), aout.reserve((1,), torch.int32))
+    in_views, out_views = ain.build(device), aout.build(device)
+    ops, keep, ins, outs = [], [], [], []
+    wbytes = 0
+
+    def qbufs(x):
+        if act == "a16":
+            return None, None
+        xq = torch.empty(x.shape, dtype=torch.int8, device=device)
+        xs = torch.empty(x.shape[0], dtype=torch.float32, device=device)
+        keep.extend([xq, xs])
+        return xq, xs
+
+    for L, iid, oid in zip(layers, in_ids, out_ids):
+        xin = {}
+        for k, v in L.inputs.items():
+            xin[k] = in_views[iid[k]]
+            xin[k].copy_(v)
+        qin = {k: qbufs(v) for k, v in xin.items()}
+        ys = {}
+        for lin in L.linears:
+            W, S = lin.W.to(device), lin.scales.to(device)
+            y = out_views[oid[lin.name]]
+            xq, xs = qin[lin.x_name]
+            ops.append(linear(kind, W, M, lin.N, lin.K, w_scale=S, x=xin[lin.x_name], x_i8=xq,
+                              x_scale=xs, y=y, group_size=group))
+            keep += [W, S]
+            ys[lin.name] = y
+            wbytes += _nbytes(W) + _nbytes(S)
+        ins.append(xin)
+        outs.append(ys)
+    logits = token = xh = None
+    if head is not None:
+        W, S = head.W.to(device), head.scales.to(device)
+        xh = in_views[head_ids[0]]
+        xh.copy_(x_head)
+        logits, token = out_views[head_ids[1]], out_views[head_ids[2]]
+        xq, xs = qbufs(xh)
+        ops.append(linear(kind, W, 1, head.N, head.K, w_scale=S, x=xh, x_i8=xq, x_scale=xs,
+                          logits=logits, token=token, group_size=group))
+        keep += [W, S]
+        wbytes += _nbytes(W) + _nbytes(S)
+    keep += [ain.buf, aout.buf]
+    plan = StepPlan(ops, keep)
+    nws = plan.workspace_bytes()
+    ws = torch.empty(nws, dtype=torch.uint8, device=device) if nws else None
+    return DeviceStep(plan, ws, ins, outs, ain.buf, aout.buf, wbytes, count_launches(ops),
+                      logits, token, xh, keep=keep)

@@ -1,0 +1,129 @@
+"""The C ABI on a host without a GPU: libdg.so loads, exports every entry point
+include/dg.h declares, and rejects bad arguments on the host with the
+documented status before any CUDA call (fake, never-dereferenced pointers)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quantized_skinny_gemm_gb300 as dg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA, TIMEOUT = range(7)
+A = 0x100000          # a fake 16-byte-aligned device address (never dereferenced)
+B = 0x200000
+ODD = 0x100008        # 8-byte but not 16-byte aligned
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from quantized_skinny_gemm_gb300 import build
+    build.build()
+    return dg.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "dg.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dg_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 12, names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for i, name in enumerate(["DG_OK", "DG_ERR_INVALID_ARG", "DG_ERR_UNSUPPORTED",
+                              "DG_ERR_MISALIGNED", "DG_ERR_WORKSPACE", "DG_ERR_CUDA",
+                              "DG_ERR_TIMEOUT"]):
+        assert dg.status_string(i) == name
+    assert dg.version().startswith("dg ")
+
+
+def test_linear_struct_layout_matches_header():
+    # 5 int32 then 9 pointers: 20 bytes + 4 bytes padding + 72
+    assert ctypes.sizeof(dg.Linear) == 96
+    assert dg.Linear.W.offset == 24
+
+
+def test_gemv_f16_validation(lib):
+    f = lib.dg_gemv_f16
+    assert f(None, A, B, 0, 1, 8, 8, None, 0, None) == INVALID
+    assert f(A, A, B, 5, 1, 8, 8, None, 0, None) == INVALID         # bad dtype
+    assert f(A, A, B, 0, 0, 8, 8, None, 0, None) == INVALID         # M = 0
+    assert f(A, A, B, 0, 1, 0, 8, None, 0, None) == INVALID         # N = 0
+    assert f(A, A, B, 0, 17, 8, 8, None, 0, None) == UNSUPPORTED    # M > 16
+    assert f(A, A, B, 0, 1, 8, 12, None, 0, None) == MISALIGNED     # K % 8
+    assert f(ODD, A, B, 0, 1, 8, 8, None, 0, None) == MISALIGNED    # W
+    assert f(A, ODD, B, 0, 1, 8, 8, None, 0, None) == MISALIGNED    # x
+    assert f(A, A, B + 1, 0, 1, 8, 8, None, 0, None) == MISALIGNED  # y odd
+
+
+def test_gemv_w8a8_validation(lib):
+    f = lib.dg_gemv_w8a8
+    assert f(A, A, A, A, None, None, 1, 8, 16, None, 0, None) == INVALID    # no output
+    assert f(A, None, A, A, B, None, 1, 8, 16, None, 0, None) == INVALID    # no w_scale
+    assert f(A, A, A, None, B, None, 1, 8, 16, None, 0, None) == INVALID    # no x_scale
+    assert f(A, A, A, A, B, None, 1, 8, 24, None, 0, None) == MISALIGNED    # K % 16
+    assert f(A, A, A, A, B, None, 1, 8, 262144, None, 0, None) == UNSUPPORTED
+
+
+def test_gemv_w4_validation(lib):
+    f = lib.dg_gemv_w4
+    assert f(A, A, 32, None, None, None, B, 1, 8, 64, None, 0, None) == INVALID  # no x
+    assert f(A, A, 48, A, None, None, B, 1, 8, 96, None, 0, None) == UNSUPPORTED  # group 48
+    assert f(A, A, 64, A, None, None, B, 1, 8, 96, None, 0, None) == UNSUPPORTED  # K % group
+    assert f(A, A, 32, A, None, None, B, 1, 8, 48, None, 0, None) == MISALIGNED   # K % 32
+    assert f(A, A, 32, None, A, None, B, 1, 8, 64, None, 0, None) == INVALID      # a8 no scale
+    assert f(A, None, 32, A, None, None, B, 1, 8, 64, None, 0, None) == INVALID   # no scales
+
+
+def test_quantize_validation(lib):
+    f = lib.dg_quantize_act_i8
+    assert f(None, A, A, 1, 8, None) == INVALID
+    assert f(A, A, A, 1, 12, None) == MISALIGNED
+    assert f(A, ODD, A, 1, 8, None) == MISALIGNED
+
+
+def _head(**kw):
+    d = dict(kind=dg.LINEAR_F16, M=1, N=100, K=64, group_size=32, W=A, x=A, logits=B,
+             token=B + 64)
+    d.update(kw)
+    return dg.Linear(**d)
+
+
+def test_lm_head_validation_and_workspace(lib):
+    h = _head()
+    need = dg.workspace_bytes([h])
+    assert need > 0 and need % 16 == 0
+    assert lib.dg_lm_head_argmax(ctypes.byref(h), None, 0, None) == WORKSPACE
+    assert lib.dg_lm_head_argmax(ctypes.byref(h), A, need - 16, None) == WORKSPACE
+    assert lib.dg_lm_head_argmax(ctypes.byref(_head(M=2)), A, need, None) == INVALID
+    assert lib.dg_lm_head_argmax(ctypes.byref(_head(logits=None)), A, need, None) == INVALID
+    assert lib.dg_lm_head_argmax(ctypes.byref(_head(kind=dg.LINEAR_W8A8, w_scale=A, x_i8=A,
+                                                    x_scale=A, x=None)), A, need,
+                                 None) == UNSUPPORTED
+    plain = dg.Linear(kind=dg.LINEAR_F16, M=1, N=8, K=8, W=A, x=A, y=B)
+    assert dg.workspace_bytes([plain]) == 0
+
+
+def test_decode_step_validates_every_op_first(lib):
+    good = [dg.Linear(kind=dg.LINEAR_F16, M=1, N=8, K=8, W=A, x=A, y=B) for _ in range(6)]
+    bad = list(good)
+    bad[5] = dg.Linear(kind=dg.LINEAR_F16, M=1, N=8, K=12, W=A, x=A, y=B)
+    arr = (dg.Linear * 6)(*bad)
+    assert lib.dg_decode_step_weights(ctypes.cast(arr, ctypes.c_void_p), 6, None, 0,
+                                      None) == MISALIGNED
+    assert lib.dg_decode_step_weights(None, 0, None, 0, None) == INVALID
+    withhead = (dg.Linear * 2)(good[0], _head())
+    assert lib.dg_decode_step_weights(ctypes.cast(withhead, ctypes.c_void_p), 2, None, 0,
+                                      None) == WORKSPACE
+
+
+def test_probe_validation(lib):
+    assert lib.dg_probe_copy(A, B, 24, None) == MISALIGNED
+    assert lib.dg_probe_read(None, 16, A, None) == INVALID

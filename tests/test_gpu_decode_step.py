@@ -1,0 +1,92 @@
+"""Decode-step weight streams (dg_decode_step_weights) in the launch
+configuration the benchmark times: the 28-layer 1536-wide fp16 decoder (every
+output of every matrix checked) and the 32-layer 4096-wide int4 decoder with
+its 128256-row lm_head (sampled rows of every matrix, the whole lm_head)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import tolerance as tol
+import quantized_skinny_gemm_gb300 as dg
+from quantized_skinny_gemm_gb300 import plans, synth
+from gpu_util import DEV, bits, need_gpu, sync
+
+pytestmark = pytest.mark.gpu
+
+
+def test_fp16_decoder_step_all_outputs():
+    need_gpu()
+    layers = synth.decode_fp16_workload(seed=0)
+    step = plans.fp16_decode_step(layers, DEV)
+    assert step.weight_bytes == 2620391424
+    assert step.n_launches == 28 * 4
+    dg.decode_step_weights(step.plan, step.ws)
+    sync()
+    for li, L in enumerate(layers):
+        for lin in L.linears:
+            yr, A = oracle.gemv_fp(bits(lin.W), bits(L.inputs[lin.x_name]))
+            y = step.outputs[li][lin.name].cpu().double().numpy()
+            tol.assert_close(y, yr, A, "f16", "layer %d %s" % (li, lin.name))
+
+
+def test_fp16_decoder_step_is_deterministic_and_graph_replayable():
+    need_gpu()
+    layers = synth.decode_fp16_workload(seed=1, layers=3)
+    step = plans.fp16_decode_step(layers, DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        dg.decode_step_weights(step.plan, step.ws, stream=s)
+    s.synchronize()
+    ref = [{k: v.clone() for k, v in o.items()} for o in step.outputs]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        dg.decode_step_weights(step.plan, step.ws, stream=s)
+    for _ in range(3):
+        for o in step.outputs:
+            for v in o.values():
+                v.fill_(0)
+        g.replay()
+        torch.cuda.synchronize()
+        for o, r in zip(step.outputs, ref):
+            for k in o:
+                assert torch.equal(o[k], r[k]), k
+
+
+@pytest.fixture(scope="module")
+def int4_workload():
+    need_gpu()
+    return synth.decode_int4_workload(seed=0)
+
+
+@pytest.mark.parametrize("act", ["a16", "a8"])
+def test_int4_decoder_step(int4_workload, act):
+    layers, head, x_head = int4_workload
+    step = plans.int4_decode_step(layers, head, x_head, DEV, act=act)
+    assert step.weight_bytes == 4221370368
+    dg.decode_step_weights(step.plan, step.ws)
+    sync()
+    rng = np.random.default_rng(0)
+    for li in (0, 13, 31):
+        L = layers[li]
+        for lin in L.linears:
+            rows = rng.integers(0, lin.N, 96)
+            x = L.inputs[lin.x_name]
+            if act == "a16":
+                yr, A = oracle.gemv_w4a16(lin.W.numpy(), bits(lin.scales), bits(x), rows=rows)
+            else:
+                q, s = oracle.quant_act(bits(x))
+                yr, A, _ = oracle.gemv_w4a8(lin.W.numpy(), bits(lin.scales), q, s, rows=rows)
+            y = step.outputs[li][lin.name].cpu().double().numpy()[:, rows]
+            tol.assert_close(y, yr, A, "f16", "%s layer %d %s" % (act, li, lin.name))
+    if act == "a16":
+        lr, A = oracle.gemv_w4a16(head.W.numpy(), bits(head.scales), bits(x_head))
+    else:
+        q, s = oracle.quant_act(bits(x_head))
+        lr, A, _ = oracle.gemv_w4a8(head.W.numpy(), bits(head.scales), q, s)
+    logits = step.head_logits.cpu().double().numpy()
+    tol.assert_close(logits, lr[0], A[0], "f32", "%s lm_head" % act)
+    tok = int(step.head_token.item())
+    ok, _ = tol.argmax_check(tok, lr[0], A[0])
+    assert ok
+    assert tok == int(np.argmax(step.head_logits.cpu().numpy()))
