@@ -141,6 +141,25 @@ dg_status dg_quantize_act_i8(const void* x, int8_t* xq, float* x_scale, int M, i
  * bytes of workspace (per-CTA (value, index) partials). */
 dg_status dg_lm_head_argmax(const dg_linear* head, void* ws, size_t ws_bytes, dg_stream stream);
 
+/* dg_lm_head_argmax without a workspace argument, for callers that cannot
+ * allocate device memory: a decode loop that must not allocate once running,
+ * a plugin whose host runtime owns all device memory through its own pool, or
+ * code whose memory plan was fixed ahead of time.  (The pages have no
+ * counterpart to this entry point.)  Same inputs, outputs and results as
+ * dg_lm_head_argmax; the per-CTA partials live in a fixed 8 KB array inside
+ * the library (1024 partials; every GPU that loads the library keeps it until
+ * the process exits).
+ *  - The first call on a device looks up that array's address (with the
+ *    device current) and caches it: make that first call before any stream
+ *    capture.  No call allocates or frees memory.
+ *  - A head that would need more than 1024 partials returns DG_ERR_WORKSPACE
+ *    and launches nothing.
+ *  - Every call shares the array; nothing in it needs to start at zero (each
+ *    call writes every partial it reads).  Calls that can overlap on the GPU
+ *    (different streams, or different host threads on one device) race on the
+ *    array: serialize them. */
+dg_status dg_lm_head_argmax_noalloc(const dg_linear* head, dg_stream stream);
+
 /* One decode step's weight stream (graph-accelerated decode of EdgeFM,
  * section 2.C): runs ops[0..n_ops) in order.  Consecutive ops of the same
  * kind that read the same activations (same x / x_i8 pointers, same M and K)

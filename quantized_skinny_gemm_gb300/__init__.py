@@ -13,7 +13,7 @@ import os
 __all__ = [
     "DGError", "Linear", "StepPlan", "F16", "BF16", "LINEAR_F16", "LINEAR_BF16",
     "LINEAR_W8A8", "LINEAR_W4A16", "LINEAR_W4A8", "gemv_f16", "gemv_w8a8", "gemv_w4",
-    "quantize_act_i8", "lm_head_argmax", "decode_step_weights", "workspace_bytes",
+    "quantize_act_i8", "lm_head_argmax", "lm_head_argmax_noalloc", "decode_step_weights", "workspace_bytes",
     "check_device_status", "status_string", "probe_copy", "probe_read", "version",
     "library_path", "load",
 ]
@@ -67,6 +67,7 @@ def load():
         "dg_gemv_w4": [P, P, I, P, P, P, P, I, I, I, P, Z, P],
         "dg_quantize_act_i8": [P, P, P, I, I, P],
         "dg_lm_head_argmax": [P, P, Z, P],
+        "dg_lm_head_argmax_noalloc": [P, P],
         "dg_decode_step_weights": [P, I, P, Z, P],
         "dg_check_device_status": [P],
         "dg_probe_copy": [P, P, Z, P],
@@ -150,6 +151,11 @@ def linear(kind, W, M, N, K, w_scale=None, x=None, x_i8=None, x_scale=None, y=No
 
 def lm_head_argmax(head, ws, stream=None):
     _call("dg_lm_head_argmax", ctypes.byref(head), _ptr(ws), _nbytes(ws), _stream(stream))
+
+
+def lm_head_argmax_noalloc(head, stream=None):
+    """lm_head + argmax with the library's own fixed scratch (no workspace)."""
+    _call("dg_lm_head_argmax_noalloc", ctypes.byref(head), _stream(stream))
 
 
 class StepPlan:

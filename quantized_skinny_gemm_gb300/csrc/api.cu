@@ -196,7 +196,7 @@ static bool quantized_act(int kind) { return kind == DG_LINEAR_W8A8 || kind == D
 
 // Validates one op without touching the device.  `quantize_here` is set when
 // the op carries fp16 activations that the caller wants quantized first.
-static dg_status validate(const dg_linear& op, bool allow_quant_input) {
+dg_status validate(const dg_linear& op, bool allow_quant_input) {
     if (op.kind < DG_LINEAR_F16 || op.kind > DG_LINEAR_W4A8) return DG_ERR_INVALID_ARG;
     if (op.M < 1 || op.N < 1 || op.K < 1) return DG_ERR_INVALID_ARG;
     if (op.M > 16) return DG_ERR_UNSUPPORTED;
@@ -245,7 +245,7 @@ static dg_status validate(const dg_linear& op, bool allow_quant_input) {
     return DG_OK;
 }
 
-static dg_status check_smem(const dg_linear& op) {
+dg_status check_smem(const dg_linear& op) {
     const size_t need = gemv_smem(fmt_of(op.kind), pick_mt(op.M), op.K, op.group_size);
     const size_t lim = smem_optin_limit();
     if (lim == 0) return DG_ERR_CUDA;
@@ -285,7 +285,7 @@ static dg_status launch_group(const dg_linear* ops, int n, cudaStream_t s) {
     return to_status(family(L, &p, s, nullptr));
 }
 
-static dg_status launch_head(const dg_linear& op, void* ws, cudaStream_t s) {
+dg_status launch_head(const dg_linear& op, void* ws, cudaStream_t s) {
     GemvParams p;
     fill_common(p, op);
     p.seg[0].W = op.W;
@@ -303,6 +303,18 @@ static dg_status launch_head(const dg_linear& op, void* ws, cudaStream_t s) {
     cudaError_t e = family(L, &p, s, nullptr);
     if (e != cudaSuccess) return DG_ERR_CUDA;
     return to_status(launch_argmax_pass2(p.part, L.grid, op.token, s));
+}
+
+// CTAs (and so argmax partials) launch_head uses for this op.
+int head_grid(const dg_linear& op) {
+    GemvParams p;
+    fill_common(p, op);
+    p.nseg = 1;
+    p.N = op.N;
+    GemvLaunch L{fmt_of(op.kind), 1, 0, true, op.K, p.group, 0};
+    L.R = pick_r(L.fmt, 1);
+    configure(L, p);
+    return L.grid;
 }
 
 static size_t head_ws_bytes() { return (size_t)kMaxArgCtas * sizeof(ArgPart); }

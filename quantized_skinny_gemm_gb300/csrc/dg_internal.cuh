@@ -170,6 +170,12 @@ cudaError_t gemv_w4a16(const GemvLaunch& L, const GemvParams* p, cudaStream_t s,
 cudaError_t gemv_w4a8(const GemvLaunch& L, const GemvParams* p, cudaStream_t s, int* occ);
 size_t gemv_smem(Fmt f, int MT, int K, int group);
 
+// Host helpers of api.cu shared with the static-scratch lm_head entry point.
+dg_status validate(const dg_linear& op, bool allow_quant_input);
+dg_status check_smem(const dg_linear& op);
+dg_status launch_head(const dg_linear& op, void* parts, cudaStream_t s);
+int head_grid(const dg_linear& op);
+
 cudaError_t launch_argmax_pass2(const ArgPart* part, int nparts, int32_t* token, cudaStream_t s);
 cudaError_t launch_quant_act(const __half* x, int8_t* xq, float* s, int M, int K,
                              cudaStream_t st);
