@@ -152,8 +152,9 @@ def build_workload(name, dev, torch):
         # dominant kernel: the fused gate|up launch of every layer
         ops = [op for op in st.plan.array if op.N == 8960 and op.K == 1536]
         dplan = plans.StepPlan(ops, [])
+        dws = torch.empty(dplan.workspace_bytes(), dtype=torch.uint8, device=dev)
         w.dominant = ("gate|up 17920x1536 fp16",
-                      lambda: dg.decode_step_weights(dplan, None, stream=s), len(ops) // 2,
+                      lambda: dg.decode_step_weights(dplan, dws, stream=s), len(ops) // 2,
                       2 * 8960 * 1536 * 2)
         w.cpu_sample = ("fp", layers)
         w.dtype = "f16"
@@ -175,8 +176,9 @@ def build_workload(name, dev, torch):
         for op in ops:
             op.x = None  # codes already quantized by the step; time the GEMV alone
         dplan = plans.StepPlan(ops, [])
+        dws = torch.empty(dplan.workspace_bytes(), dtype=torch.uint8, device=dev)
         w.dominant = ("gate|up 28672x4096 int4",
-                      lambda: dg.decode_step_weights(dplan, None, stream=s), len(ops) // 2,
+                      lambda: dg.decode_step_weights(dplan, dws, stream=s), len(ops) // 2,
                       2 * 14336 * 4096 // 2 + 2 * 14336 * (4096 // 32) * 2)
         w.cpu_sample = ("w4" + act, (layers, head, xh))
         w.dtype = "int4xf16" if act == "a16" else "int4xi8"
@@ -224,11 +226,12 @@ def build_workload(name, dev, torch):
                 keep.append(Wd)
                 ops.append(dg.linear(dg.LINEAR_F16, Wd, 1, 8960, 1536, x=xd, y=outs[iy[2 * i + j]]))
         plan = dg.StepPlan(ops, keep)
+        gws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=dev)
         w.host = (pairs, x)
         w.in_arena, w.out_arena = ain.buf, aout.buf
         w.unit_bytes = 4 * 2 * 8960 * 1536 * 2
-        w.launches = 4
-        w.run = lambda: dg.decode_step_weights(plan, None, stream=s)
+        w.launches = plans.count_launches(list(plan.array))
+        w.run = lambda: dg.decode_step_weights(plan, gws, stream=s)
         w.config = {"workload": "fused gate|up 17920x1536 fp16 (4 distinct pairs per step), M=1",
                     "weight_bytes_per_step": w.unit_bytes,
                     "l2": "inputs 220 MB > 126 MB L2 (no flush)"}
@@ -339,6 +342,9 @@ def main():
                     choices=["decode_fp16", "decode_int4_a16", "decode_int4_a8", "lm_head",
                              "gateup_fp16"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--quick", action="store_true",
+                    help="time the step only (no dominant-kernel, e2e, probe or CPU legs); "
+                         "for configuration sweeps")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -386,6 +392,14 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         secs = float(t.item())
         dist.barrier()
+
+    if args.quick:
+        clk = clocks.stop()
+        if rank == 0:
+            print(json.dumps({"workload": args.workload, "us_per_step": secs / args.steps * 1e6,
+                              "value": w.unit_bytes * args.steps * world / secs / 1e9,
+                              "tune": os.environ.get("DG_TUNE", ""), "clocks": clk}), flush=True)
+        return 0
 
     # dominant kernel alone: its launches for every layer, replayed
     dname, dfn, dlaunch, dbytes = w.dominant

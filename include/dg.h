@@ -162,23 +162,43 @@ dg_status dg_lm_head_argmax_noalloc(const dg_linear* head, dg_stream stream);
 
 /* One decode step's weight stream (graph-accelerated decode of EdgeFM,
  * section 2.C): runs ops[0..n_ops) in order.  Consecutive ops of the same
- * kind that read the same activations (same x / x_i8 pointers, same M and K)
- * and are not lm_heads run as one launch (q|k|v, gate|up); every other
- * boundary is a dependency: an op reads its activations only after every
- * earlier op finished.  Weights and scales must stay unchanged during the
- * step (they may be prefetched early).  Needs dg_workspace_bytes(ops, n_ops)
- * bytes of workspace. */
+ * kind that read the same activations (same x / x_i8 / x_scale pointers,
+ * same M, K and group) and are not lm_heads are fused (q|k|v, gate|up); every
+ * other boundary is a dependency: an op reads its activations only after
+ * every earlier op finished.
+ * Runs of single-token ops (M = 1, no acc_out) of one kind execute as ONE
+ * persistent cooperative launch: one CTA per SM takes a contiguous row slice
+ * of every fused group, groups meet at a grid-wide barrier, and each CTA
+ * prefetches its upcoming weight rows into L2 ahead of use, across group
+ * boundaries.  Other ops run as one launch per fused group.  Both give the
+ * same bits as calling dg_gemv_* / dg_lm_head_argmax op by op.
+ * For W8A8 / W4A8 ops that carry fp16 `x`, the step quantizes x exactly as
+ * dg_quantize_act_i8 does and also writes the codes / scale to x_i8 / x_scale.
+ * Weights and scales must stay unchanged during the step (they are read
+ * early).  ws: dg_workspace_bytes(ops, n_ops) bytes, 16-byte aligned, owned
+ * by the caller; the step overwrites it (nothing needs to be zeroed first).
+ * A barrier wait that exceeds its bound (about a second) makes the launch
+ * end early; dg_check_device_status then reports DG_ERR_TIMEOUT. */
 dg_status dg_decode_step_weights(const dg_linear* ops, int n_ops, void* ws, size_t ws_bytes,
                                  dg_stream stream);
 
-/* Workspace bytes that dg_lm_head_argmax / dg_decode_step_weights need for
- * these ops (0 when none is needed).  Host-only; touches no device. */
+/* Workspace bytes that dg_decode_step_weights needs for these ops (256 for
+ * the persistent kernel's barrier, plus 32 KB of argmax partials when an op is
+ * an lm_head); for a single lm_head this also covers dg_lm_head_argmax.
+ * 0 for n_ops <= 0.  Host-only; touches no device. */
 size_t dg_workspace_bytes(const dg_linear* ops, int n_ops);
 
 /* Synchronizes `stream`, then reports DG_ERR_CUDA for a sticky CUDA error or
- * DG_ERR_TIMEOUT if a bounded device-side wait gave up since the last call
- * (clearing that flag).  DG_OK otherwise. */
+ * DG_ERR_TIMEOUT if a bounded device-side wait gave up on the current device
+ * since the last call (clearing that flag).  DG_OK otherwise. */
 dg_status dg_check_device_status(dg_stream stream);
+
+/* Diagnostic (not part of the method): launches one tiny kernel that waits on
+ * a device word nothing ever sets, with the same bounded wait the step
+ * kernel's barriers use, giving up after `spin_limit` polls (1..10^7, ~100 ns
+ * each).  The following dg_check_device_status reports DG_ERR_TIMEOUT: the
+ * failure path can be exercised without hanging or faulting anything. */
+dg_status dg_selftest_wait_timeout(unsigned spin_limit, dg_stream stream);
 
 /* Static, human-readable name of a status. */
 const char* dg_status_string(dg_status s);

@@ -14,7 +14,7 @@ __all__ = [
     "DGError", "Linear", "StepPlan", "F16", "BF16", "LINEAR_F16", "LINEAR_BF16",
     "LINEAR_W8A8", "LINEAR_W4A16", "LINEAR_W4A8", "gemv_f16", "gemv_w8a8", "gemv_w4",
     "quantize_act_i8", "lm_head_argmax", "lm_head_argmax_noalloc", "decode_step_weights", "workspace_bytes",
-    "check_device_status", "status_string", "probe_copy", "probe_read", "version",
+    "check_device_status", "selftest_wait_timeout", "status_string", "probe_copy", "probe_read", "version",
     "library_path", "load",
 ]
 
@@ -70,6 +70,7 @@ def load():
         "dg_lm_head_argmax_noalloc": [P, P],
         "dg_decode_step_weights": [P, I, P, Z, P],
         "dg_check_device_status": [P],
+        "dg_selftest_wait_timeout": [ctypes.c_uint, P],
         "dg_probe_copy": [P, P, Z, P],
         "dg_probe_read": [P, Z, P, P],
     }
@@ -182,6 +183,11 @@ def workspace_bytes(ops):
 
 def check_device_status(stream=None):
     _call("dg_check_device_status", _stream(stream))
+
+
+def selftest_wait_timeout(spin_limit, stream=None):
+    """Launches the bounded-wait self test (see include/dg.h)."""
+    _call("dg_selftest_wait_timeout", spin_limit, _stream(stream))
 
 
 def status_string(s):

@@ -46,11 +46,31 @@ size_t smem_optin_limit() {
     return (size_t)n;
 }
 
+// The library's device error word (bounded waits record kErrTimeout here),
+// located once per device.
+static __device__ int g_dg_error = 0;
+
+int* device_error_word() {
+    static std::mutex mu;
+    static int* cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> g(mu);
+    if (!cache[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_dg_error) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<int*>(p);
+    }
+    return cache[dev];
+}
+
 // ---- tuning knobs ------------------------------------------------------------------
-// DG_TUNE="R=2,KS=1,CPS=4,PF=32768,PDL=1" overrides the launch heuristic (for
-// configuration sweeps); an unset key keeps the heuristic's choice.
+// DG_TUNE="R=2,KS=1,CPS=4,PF=32768,PDL=1,STEP=1,WIN=262144,SPIN=20000000"
+// overrides the launch heuristic (for configuration sweeps); an unset key
+// keeps the heuristic's choice.  STEP=0 runs decode steps as one launch per
+// fused group instead of the persistent step kernel.
 struct Tune {
-    int R = 0, KS = 0, CPS = 0, PF = -1, PDL = -1;
+    int R = 0, KS = 0, CPS = 0, PF = -1, PDL = -1, STEP = -1, WIN = -1, SPIN = -1;
 };
 
 static Tune read_tune() {
@@ -67,6 +87,9 @@ static Tune read_tune() {
         else if (std::sscanf(tok, "CPS=%d", &v) == 1) t.CPS = v;
         else if (std::sscanf(tok, "PF=%d", &v) == 1) t.PF = v;
         else if (std::sscanf(tok, "PDL=%d", &v) == 1) t.PDL = v;
+        else if (std::sscanf(tok, "STEP=%d", &v) == 1) t.STEP = v;
+        else if (std::sscanf(tok, "WIN=%d", &v) == 1) t.WIN = v;
+        else if (std::sscanf(tok, "SPIN=%d", &v) == 1) t.SPIN = v;
     }
     return t;
 }
@@ -155,9 +178,9 @@ static int occupancy(const GemvLaunch& L) {
 
 // Fills L.grid and p.iters / ksplit / prefetch for a launch over p.N rows.
 static void configure(GemvLaunch& L, GemvParams& p) {
-    const int ks = pick_ks(L.fmt, p.K);
+    const int ks = pick_ks(L.fmt, p.a.K);
     const int slots = kWarps / ks;
-    const int n_rg = (p.N + L.R - 1) / L.R;
+    const int n_rg = (p.t.N + L.R - 1) / L.R;
     const int need = (n_rg + slots - 1) / slots;
     int cps = occupancy(L);
     const int tc = tune().CPS;
@@ -254,12 +277,12 @@ dg_status check_smem(const dg_linear& op) {
 
 static void fill_common(GemvParams& p, const dg_linear& op) {
     std::memset(&p, 0, sizeof p);
-    p.K = op.K;
-    p.M = op.M;
+    p.a.K = op.K;
+    p.a.M = op.M;
     p.group = op.group_size >= 32 ? op.group_size : 32;
-    p.x = op.x;
-    p.xq = op.x_i8;
-    p.x_scale = op.x_scale;
+    p.a.x = op.x;
+    p.a.xq = op.x_i8;
+    p.a.x_scale = op.x_scale;
 }
 
 // Launches ops[0..n) (same kind, same activations) as one kernel.
@@ -268,7 +291,7 @@ static dg_status launch_group(const dg_linear* ops, int n, cudaStream_t s) {
     fill_common(p, ops[0]);
     int rows = 0;
     for (int i = 0; i < n; ++i) {
-        Segment& g = p.seg[i];
+        Segment& g = p.t.seg[i];
         g.W = ops[i].W;
         g.scale = ops[i].w_scale;
         g.y = ops[i].y;
@@ -277,8 +300,8 @@ static dg_status launch_group(const dg_linear* ops, int n, cudaStream_t s) {
         g.rows = ops[i].N;
         rows += ops[i].N;
     }
-    p.nseg = n;
-    p.N = rows;
+    p.t.nseg = n;
+    p.t.N = rows;
     GemvLaunch L{fmt_of(ops[0].kind), pick_mt(ops[0].M), 0, false, ops[0].K, p.group, 0};
     L.R = pick_r(L.fmt, L.MT);
     configure(L, p);
@@ -288,13 +311,13 @@ static dg_status launch_group(const dg_linear* ops, int n, cudaStream_t s) {
 dg_status launch_head(const dg_linear& op, void* ws, cudaStream_t s) {
     GemvParams p;
     fill_common(p, op);
-    p.seg[0].W = op.W;
-    p.seg[0].scale = op.w_scale;
-    p.seg[0].y = nullptr;
-    p.seg[0].row_begin = 0;
-    p.seg[0].rows = op.N;
-    p.nseg = 1;
-    p.N = op.N;
+    p.t.seg[0].W = op.W;
+    p.t.seg[0].scale = op.w_scale;
+    p.t.seg[0].y = nullptr;
+    p.t.seg[0].row_begin = 0;
+    p.t.seg[0].rows = op.N;
+    p.t.nseg = 1;
+    p.t.N = op.N;
     p.logits = op.logits;
     p.part = static_cast<ArgPart*>(ws);
     GemvLaunch L{fmt_of(op.kind), 1, 0, true, op.K, p.group, 0};
@@ -309,8 +332,8 @@ dg_status launch_head(const dg_linear& op, void* ws, cudaStream_t s) {
 int head_grid(const dg_linear& op) {
     GemvParams p;
     fill_common(p, op);
-    p.nseg = 1;
-    p.N = op.N;
+    p.t.nseg = 1;
+    p.t.N = op.N;
     GemvLaunch L{fmt_of(op.kind), 1, 0, true, op.K, p.group, 0};
     L.R = pick_r(L.fmt, 1);
     configure(L, p);
@@ -318,6 +341,102 @@ int head_grid(const dg_linear& op) {
 }
 
 static size_t head_ws_bytes() { return (size_t)kMaxArgCtas * sizeof(ArgPart); }
+
+// Decode-step workspace: [0, 256) the persistent kernel's barrier words,
+// then the argmax partials when the step has an lm_head.
+constexpr size_t kStepHeader = 256;
+
+// ---- the persistent decode-step path -----------------------------------------------
+
+static bool same_group(const dg_linear& a, const dg_linear& b) {
+    return !b.token && b.kind == a.kind && b.M == a.M && b.K == a.K && b.x == a.x &&
+           b.x_i8 == a.x_i8 && b.x_scale == a.x_scale && b.group_size == a.group_size;
+}
+
+// Ops the persistent kernel runs: one token, no int32 accumulator output.
+static bool step_eligible(const dg_linear& op) { return op.M == 1 && !op.acc_out; }
+
+static int step_occupancy(Fmt f, int max_k, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_tuple(dev, (int)f, max_k);
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    StepParams* none = nullptr;
+    int occ = 0;
+    if (step_launch(f, none, 0, smem, nullptr, &occ) != cudaSuccess) occ = 0;
+    std::lock_guard<std::mutex> g(mu);
+    cache[key] = occ;
+    return occ;
+}
+
+// Runs ops[0..n) (all of one kind, all step-eligible) with the persistent
+// kernel, in launches of at most kMaxStepPhases phases.
+static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStream_t s) {
+    static thread_local StepParams sp;
+    const Fmt f = fmt_of(ops[0].kind);
+    int i = 0;
+    while (i < n) {
+        std::memset(&sp, 0, sizeof sp);
+        int max_k = 0;
+        while (i < n && sp.nphase < kMaxStepPhases) {
+            const dg_linear& a = ops[i];
+            int j = i + 1;
+            if (!a.token)
+                while (j < n && j - i < kMaxSeg && same_group(a, ops[j])) ++j;
+            StepPhase& ph = sp.ph[sp.nphase++];
+            int rows = 0;
+            for (int k = i; k < j; ++k) {
+                StepSeg& sg = ph.seg[k - i];
+                sg.W = ops[k].W;
+                sg.scale = ops[k].w_scale;
+                sg.y = ops[k].y;
+                sg.rows = ops[k].N;
+                sg.row_begin = rows;
+                rows += ops[k].N;
+            }
+            ph.nseg = j - i;
+            ph.N = rows;
+            ph.K = a.K;
+            ph.ks = pick_ks(f, a.K);
+            ph.x = a.x;
+            ph.xq = a.x_i8;
+            ph.x_scale = const_cast<float*>(a.x_scale);
+            if (quantized_act(a.kind) && a.x) {
+                ph.flags |= kPhaseQuantize;
+                ph.xq_out = const_cast<int8_t*>(a.x_i8);
+            }
+            if (a.token) {
+                ph.flags |= kPhaseHead;
+                ph.logits = a.logits;
+                ph.token = a.token;
+            }
+            if (a.K > max_k) max_k = a.K;
+            i = j;
+        }
+        sp.group = ops[0].group_size >= 32 ? ops[0].group_size : 32;
+        sp.window = tune().WIN >= 0 ? tune().WIN : 262144;
+        sp.spin_limit = tune().SPIN > 0 ? (unsigned)tune().SPIN : 20000000u;
+        sp.bar = static_cast<unsigned*>(ws);
+        sp.part = reinterpret_cast<ArgPart*>(static_cast<unsigned char*>(ws) + kStepHeader);
+        sp.err = device_error_word();
+        if (!sp.err) return DG_ERR_CUDA;
+        const size_t smem = step_smem(f, max_k);
+        if (smem > smem_optin_limit()) return DG_ERR_UNSUPPORTED;
+        const int occ = step_occupancy(f, max_k, smem);
+        if (occ < 1) return DG_ERR_UNSUPPORTED;
+        const int grid = sm_count() * occ;
+        if (grid > kMaxArgCtas) return DG_ERR_UNSUPPORTED;
+        if (cudaMemsetAsync(ws, 0, 2 * sizeof(unsigned), s) != cudaSuccess) return DG_ERR_CUDA;
+        if (step_launch(f, &sp, grid, smem, s, nullptr) != cudaSuccess) return DG_ERR_CUDA;
+    }
+    return DG_OK;
+}
 
 }  // namespace dg
 
@@ -343,8 +462,8 @@ const char* dg_version(void) { return "dg 0.1 (sm_103a)"; }
 size_t dg_workspace_bytes(const dg_linear* ops, int n_ops) {
     if (!ops || n_ops <= 0) return 0;
     for (int i = 0; i < n_ops; ++i)
-        if (ops[i].token) return head_ws_bytes();
-    return 0;
+        if (ops[i].token) return kStepHeader + head_ws_bytes();
+    return kStepHeader;
 }
 
 dg_status dg_gemv_f16(const void* W, const void* x, void* y, dg_ftype t, int M, int N, int K,
@@ -426,7 +545,7 @@ dg_status dg_lm_head_argmax(const dg_linear* head, void* ws, size_t ws_bytes, dg
     dg_status st = validate(*head, false);
     if (st != DG_OK) return st;
     if (!ws) return DG_ERR_WORKSPACE;
-    if (ws_bytes < head_ws_bytes()) return DG_ERR_WORKSPACE;
+    if (ws_bytes < dg_workspace_bytes(head, 1)) return DG_ERR_WORKSPACE;
     if (!al16(ws)) return DG_ERR_MISALIGNED;
     if ((st = check_smem(*head)) != DG_OK) return st;
     return launch_head(*head, ws, stream);
@@ -440,32 +559,37 @@ dg_status dg_decode_step_weights(const dg_linear* ops, int n_ops, void* ws, size
         if (st != DG_OK) return st;
     }
     const size_t need = dg_workspace_bytes(ops, n_ops);
-    if (need && (!ws || ws_bytes < need)) return DG_ERR_WORKSPACE;
-    if (need && !al16(ws)) return DG_ERR_MISALIGNED;
+    if (!ws || ws_bytes < need) return DG_ERR_WORKSPACE;
+    if (!al16(ws)) return DG_ERR_MISALIGNED;
     for (int i = 0; i < n_ops; ++i) {
         dg_status st = check_smem(ops[i]);
         if (st != DG_OK) return st;
     }
+    const bool persistent = tune().STEP != 0;
     int i = 0;
     while (i < n_ops) {
-        const dg_linear& a = ops[i];
-        int j = i + 1;
-        if (!a.token) {
-            while (j < n_ops && j - i < kMaxSeg) {
-                const dg_linear& b = ops[j];
-                if (b.token || b.kind != a.kind || b.M != a.M || b.K != a.K || b.x != a.x ||
-                    b.x_i8 != a.x_i8 || b.x_scale != a.x_scale || b.group_size != a.group_size)
-                    break;
-                ++j;
-            }
+        // a maximal run of step-eligible ops of one kind goes to the persistent kernel
+        int j = i;
+        while (persistent && j < n_ops && ops[j].kind == ops[i].kind && step_eligible(ops[j])) ++j;
+        if (j > i) {
+            dg_status st = launch_step_run(ops + i, j - i, ws, stream);
+            if (st != DG_OK) return st;
+            i = j;
+            continue;
         }
+        // otherwise one launch per fused group
+        const dg_linear& a = ops[i];
+        j = i + 1;
+        if (!a.token)
+            while (j < n_ops && j - i < kMaxSeg && same_group(a, ops[j])) ++j;
         if (quantized_act(a.kind) && a.x) {
             cudaError_t e = launch_quant_act(static_cast<const __half*>(a.x),
                                              const_cast<int8_t*>(a.x_i8),
                                              const_cast<float*>(a.x_scale), a.M, a.K, stream);
             if (e != cudaSuccess) return DG_ERR_CUDA;
         }
-        dg_status st = a.token ? launch_head(a, ws, stream) : launch_group(ops + i, j - i, stream);
+        void* parts = static_cast<unsigned char*>(ws) + kStepHeader;
+        dg_status st = a.token ? launch_head(a, parts, stream) : launch_group(ops + i, j - i, stream);
         if (st != DG_OK) return st;
         i = j;
     }
@@ -475,7 +599,21 @@ dg_status dg_decode_step_weights(const dg_linear* ops, int n_ops, void* ws, size
 dg_status dg_check_device_status(dg_stream stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return DG_ERR_CUDA;
     if (cudaPeekAtLastError() != cudaSuccess) return DG_ERR_CUDA;
-    return DG_OK;
+    int* w = device_error_word();
+    if (!w) return DG_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return DG_ERR_CUDA;
+    if (v == 0) return DG_OK;
+    const int zero = 0;
+    if (cudaMemcpy(w, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return DG_ERR_CUDA;
+    return DG_ERR_TIMEOUT;
+}
+
+dg_status dg_selftest_wait_timeout(unsigned spin_limit, dg_stream stream) {
+    if (spin_limit == 0 || spin_limit > 10000000u) return DG_ERR_INVALID_ARG;
+    int* w = device_error_word();
+    if (!w) return DG_ERR_CUDA;
+    return to_status(launch_wait_selftest(spin_limit, w, stream));
 }
 
 dg_status dg_probe_copy(const void* src, void* dst, size_t bytes, dg_stream stream) {

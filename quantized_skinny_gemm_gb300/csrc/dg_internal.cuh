@@ -29,6 +29,21 @@ struct Segment {
     int32_t rows;
 };
 
+// The matrices of one fused launch (same activations, K and format).
+struct SegTable {
+    Segment seg[kMaxSeg];
+    int nseg;
+    int N;               // rows over all segments
+};
+
+// Activations of a launch or phase.
+struct ActIn {
+    const void* x;          // fp16 / bf16 [M][K]
+    const int8_t* xq;       // int8 [M][K] (global or shared memory)
+    const float* x_scale;   // [M] or null
+    int K, M;
+};
+
 // (value, index) partial of the greedy argmax.
 struct ArgPart {
     float v;
@@ -36,21 +51,55 @@ struct ArgPart {
 };
 
 struct GemvParams {
-    Segment seg[kMaxSeg];
-    int nseg;
-    int N;                   // rows over all segments
-    int K;
-    int M;                   // real tokens (<= the kernel's MT)
+    SegTable t;
+    ActIn a;
     int group;               // int4 group size (multiple of 32)
     int ksplit;              // warps sharing one row group (splits K), 1/2/4/8
     int iters;               // row-group loop trip count, uniform over the grid
     int prefetch_bytes;      // per-CTA L2 prefetch issued before the dependency wait
-    const void* x;           // fp16 / bf16 [M][K]
-    const int8_t* xq;        // int8 [M][K]
-    const float* x_scale;    // [M]
     float* logits;           // lm_head: fp32 [N]
     ArgPart* part;           // lm_head: one partial per CTA
 };
+
+// ---- the persistent decode-step kernel's work list --------------------------------
+
+constexpr int kMaxStepPhases = 144;   // phases per launch (kernel parameter space)
+
+enum StepFlags : int { kPhaseHead = 1, kPhaseQuantize = 2 };
+
+struct StepSeg {
+    const void* W;
+    const void* scale;
+    void* y;
+    int32_t rows;
+    int32_t row_begin;
+};
+
+// One phase = one fused group of ops; phases run in order, separated by a
+// grid-wide barrier (a phase may read what the previous one wrote).
+struct StepPhase {
+    StepSeg seg[kMaxSeg];
+    const void* x;        // fp16 / bf16 activations (or the fp16 source to quantize)
+    const int8_t* xq;     // given int8 codes
+    float* x_scale;       // given per-token scale, or where the quantization writes it
+    int8_t* xq_out;       // where the quantization writes its codes (may be null)
+    float* logits;        // lm_head
+    int32_t* token;       // lm_head
+    int32_t K, N, nseg, flags, ks, pad;
+};
+
+struct StepParams {
+    StepPhase ph[kMaxStepPhases];
+    int nphase;
+    int group;
+    int window;           // L2 prefetch lookahead per CTA, bytes
+    unsigned spin_limit;  // bound on every barrier wait
+    unsigned* bar;        // 2 zeroed words: arrivals, generation
+    ArgPart* part;        // one partial per CTA (lm_head phases)
+    int* err;             // device error word
+};
+
+constexpr int kErrTimeout = 1;
 
 // ---- PTX helpers ------------------------------------------------------------
 
@@ -145,9 +194,30 @@ __device__ __forceinline__ int warp_sum(int v) {
     return v;
 }
 
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Spins while *flag == old, at most `limit` polls (~100 ns apart).  On giving
+// up it records kErrTimeout in *err and returns false; it never waits longer.
+__device__ __forceinline__ bool bounded_wait_change(const unsigned* flag, unsigned old,
+                                                    unsigned limit, int* err) {
+    for (unsigned n = 0; ld_acquire_gpu(flag) == old; ++n) {
+        if (n >= limit) {
+            atomicExch(err, kErrTimeout);
+            return false;
+        }
+        __nanosleep(100);
+    }
+    return true;
+}
+
 // ---- host-side launch helpers (defined in api.cu) ---------------------------
 
 int sm_count();                      // SMs of the current device (cached per device)
+int* device_error_word();            // the library's device error word (current device)
 size_t smem_optin_limit();           // max dynamic shared memory per CTA
 cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                        void** args);
@@ -175,6 +245,13 @@ dg_status validate(const dg_linear& op, bool allow_quant_input);
 dg_status check_smem(const dg_linear& op);
 dg_status launch_head(const dg_linear& op, void* parts, cudaStream_t s);
 int head_grid(const dg_linear& op);
+
+// Persistent decode-step kernel (step_kernel.cu): one cooperative launch over
+// sp.nphase phases of format f.  occ != nullptr: report CTAs per SM instead.
+cudaError_t step_launch(Fmt f, const StepParams* sp, int grid, size_t smem, cudaStream_t s,
+                        int* occ);
+size_t step_smem(Fmt f, int max_k);
+cudaError_t launch_wait_selftest(unsigned limit, int* err, cudaStream_t s);
 
 cudaError_t launch_argmax_pass2(const ArgPart* part, int nparts, int32_t* token, cudaStream_t s);
 cudaError_t launch_quant_act(const __half* x, int8_t* xq, float* s, int M, int K,

@@ -1,22 +1,22 @@
-// Weight-streaming skinny GEMV: one kernel skeleton, one policy per weight format.
+// Weight-streaming skinny GEMV: the per-row arithmetic shared by every kernel
+// (one policy per weight format), and the per-launch kernel k_gemv.
 //
-// Work decomposition.  A CTA is 8 warps.  `ksplit` consecutive warps form a
-// slot that owns one row group of R rows; the slot's warps split the row's
-// 16-byte chunks: warp kw of the slot, lane l, visits chunks
+// Work decomposition.  `ksplit` consecutive warps of a CTA form a slot that
+// owns one row group of R rows; the slot's warps split the row's 16-byte
+// chunks: warp kw of the slot, lane l, visits chunks
 //     c_j = (j * ksplit + kw) * 32 + l,   j = 0, 1, ...
 // so each warp-wide load reads 512 contiguous bytes of a weight row, and one
 // lane accumulates its chunks in ascending j.  Lane sums meet in a fixed
 // xor-butterfly, then the slot's warps add in kw order.  The order depends
 // only on K and ksplit (which the host picks from K alone), never on N, the
-// row's offset or the grid, so a row slice of W reproduces the full matrix's
-// rows bit for bit (the 16-slice lm_head split of the Orange Pi AIPro post
-// holds exactly).
+// row's offset, the grid or the kernel (k_gemv or the persistent step kernel),
+// so a row slice of W reproduces the full matrix's rows bit for bit (the
+// 16-slice lm_head split of the Orange Pi AIPro post holds exactly), and a
+// decode step gives bitwise the results of the per-op calls.
 //
-// Row groups are dealt to slots grid-stride, with a uniform trip count so that
-// every warp reaches the CTA-wide barriers.  Activations are staged once per
-// CTA in shared memory (permuted where the int4 unpack wants it); weights
-// bypass L1 and are read with 16-byte vector loads, U chunks per lane in
-// flight per row.
+// Activations are staged once per CTA in shared memory (permuted where the
+// int4 unpack wants it); weights bypass L1 and are read with 16-byte vector
+// loads, U chunks per lane in flight per row.
 #pragma once
 
 #include <climits>
@@ -39,16 +39,16 @@ struct RowRef {
     bool valid;
 };
 
-__device__ __forceinline__ RowRef locate(const GemvParams& p, int r, size_t row_bytes,
+__device__ __forceinline__ RowRef locate(const SegTable& t, int r, size_t row_bytes,
                                          const RowRef& fallback) {
     RowRef rr = fallback;
     rr.valid = false;
-    if (r >= p.N) return rr;
+    if (r >= t.N) return rr;
     int s = 0;
 #pragma unroll
     for (int i = 1; i < kMaxSeg; ++i)
-        if (i < p.nseg && r >= p.seg[i].row_begin) s = i;
-    const Segment& sg = p.seg[s];
+        if (i < t.nseg && r >= t.seg[i].row_begin) s = i;
+    const Segment& sg = t.seg[s];
     rr.local = r - sg.row_begin;
     rr.w = static_cast<const unsigned char*>(sg.W) + (size_t)rr.local * row_bytes;
     rr.scale = sg.scale;
@@ -74,24 +74,27 @@ template <>
 __device__ __forceinline__ int from_bits<int>(int v) { return v; }
 
 // ---- format policies ------------------------------------------------------------
+// stage_x fills the CTA's activation area from `a`; the int8 policies read
+// their codes from `a.xq`, which may point to global or shared memory.
 
 // fp16 / bf16 weights and activations; 8 elements per chunk.
 template <bool BF16>
 struct PolicyFP {
     static constexpr int kElems = 8;
+    static constexpr bool kIntAct = false;
     using Acc = float;
     struct Chunk { uint4 w; };
 
     __host__ __device__ static size_t row_bytes(int K) { return (size_t)K * 2; }
-    __host__ __device__ static size_t x_bytes(int MT, int K, int) { return (size_t)MT * K * 2; }
+    __host__ __device__ static size_t x_bytes(int MT, int K) { return (size_t)MT * K * 2; }
 
-    __device__ static void stage_x(const GemvParams& p, unsigned char* xs, int MT) {
-        const int per_row = p.K / 8;
-        const uint4* src = static_cast<const uint4*>(p.x);
+    __device__ static void stage_x(const ActIn& a, unsigned char* xs, int MT) {
+        const int per_row = a.K / 8;
+        const uint4* src = static_cast<const uint4*>(a.x);
         uint4* dst = reinterpret_cast<uint4*>(xs);
-        for (int i = threadIdx.x; i < MT * per_row; i += kThreads) {
+        for (int i = threadIdx.x; i < MT * per_row; i += blockDim.x) {
             const int m = i / per_row;
-            dst[i] = m < p.M ? src[i] : make_uint4(0, 0, 0, 0);
+            dst[i] = m < a.M ? src[i] : make_uint4(0, 0, 0, 0);
         }
     }
     __device__ __forceinline__ static void load(Chunk& ch, const RowRef& r, int c, int, int) {
@@ -119,33 +122,33 @@ struct PolicyFP {
             acc[m] = a;
         }
     }
-    __device__ static float finish(const GemvParams&, const RowRef&, int, Acc a) { return a; }
-    __device__ static void store(const GemvParams& p, const RowRef& r, int m, Acc a) {
+    __device__ static float finish(const RowRef&, Acc a, float) { return a; }
+    __device__ static void store(const RowRef& r, int m, Acc a, float) {
         const size_t o = (size_t)m * r.seg_rows + r.local;
         if (BF16)
             static_cast<__nv_bfloat16*>(r.y)[o] = __float2bfloat16_rn(a);
         else
             static_cast<__half*>(r.y)[o] = __float2half_rn(a);
-        (void)p;
     }
 };
 
 // int8 weights x int8 activations, exact int32 sums; 16 elements per chunk.
 struct PolicyI8 {
     static constexpr int kElems = 16;
+    static constexpr bool kIntAct = true;
     using Acc = int;
     struct Chunk { uint4 w; };
 
     __host__ __device__ static size_t row_bytes(int K) { return (size_t)K; }
-    __host__ __device__ static size_t x_bytes(int MT, int K, int) { return (size_t)MT * K; }
+    __host__ __device__ static size_t x_bytes(int MT, int K) { return (size_t)MT * K; }
 
-    __device__ static void stage_x(const GemvParams& p, unsigned char* xs, int MT) {
-        const int per_row = p.K / 16;
-        const uint4* src = reinterpret_cast<const uint4*>(p.xq);
+    __device__ static void stage_x(const ActIn& a, unsigned char* xs, int MT) {
+        const int per_row = a.K / 16;
+        const uint4* src = reinterpret_cast<const uint4*>(a.xq);
         uint4* dst = reinterpret_cast<uint4*>(xs);
-        for (int i = threadIdx.x; i < MT * per_row; i += kThreads) {
+        for (int i = threadIdx.x; i < MT * per_row; i += blockDim.x) {
             const int m = i / per_row;
-            dst[i] = m < p.M ? src[i] : make_uint4(0, 0, 0, 0);
+            dst[i] = m < a.M ? src[i] : make_uint4(0, 0, 0, 0);
         }
     }
     __device__ __forceinline__ static void load(Chunk& ch, const RowRef& r, int c, int, int) {
@@ -165,14 +168,14 @@ struct PolicyI8 {
             acc[m] = a;
         }
     }
-    __device__ static float finish(const GemvParams& p, const RowRef& r, int m, Acc a) {
+    __device__ static float finish(const RowRef& r, Acc a, float sx) {
         const float sw = __ldg(static_cast<const float*>(r.scale) + r.local);
-        return (float)a * sw * __ldg(p.x_scale + m);
+        return (float)a * sw * sx;
     }
-    __device__ static void store(const GemvParams& p, const RowRef& r, int m, Acc a) {
+    __device__ static void store(const RowRef& r, int m, Acc a, float sx) {
         const size_t o = (size_t)m * r.seg_rows + r.local;
         if (r.acc_out) r.acc_out[o] = a;
-        if (r.y) static_cast<__half*>(r.y)[o] = __float2half_rn(finish(p, r, m, a));
+        if (r.y) static_cast<__half*>(r.y)[o] = __float2half_rn(finish(r, a, sx));
     }
 };
 
@@ -194,24 +197,27 @@ __device__ __forceinline__ void unpack_int4x8_f16(uint32_t w, uint32_t (&q)[4]) 
     q[3] = h2_as_u32(__hfma2(u32_as_h2(and_xor(w8, 0x00F000F0u, 0x64806480u)), k16th, k72));
 }
 
-// Groupwise int4 weights with fp16 activations; 32 codes (one 32-group) per chunk.
-// Activations are staged per 8-block in the order x0 x4 x1 x5 x2 x6 x3 x7 so
-// that a 16-byte shared load lines up with the unpacked pairs.
+// Groupwise int4 weights with fp16 activations; 32 codes per chunk.  Chunk c
+// covers codes [32c, 32c + 32) of the row and uses the scale of group c / cpg
+// (cpg = group / 32).  Activations are staged per 8-block in the order
+// x0 x4 x1 x5 x2 x6 x3 x7 so that a 16-byte shared load lines up with the
+// unpacked pairs.
 struct PolicyW4A16 {
     static constexpr int kElems = 32;
+    static constexpr bool kIntAct = false;
     using Acc = float;
     struct Chunk { uint4 w; uint16_t s; };
 
     __host__ __device__ static size_t row_bytes(int K) { return (size_t)K / 2; }
-    __host__ __device__ static size_t x_bytes(int MT, int K, int) { return (size_t)MT * K * 2; }
+    __host__ __device__ static size_t x_bytes(int MT, int K) { return (size_t)MT * K * 2; }
 
-    __device__ static void stage_x(const GemvParams& p, unsigned char* xs, int MT) {
-        const int per_row = p.K / 8;
-        const uint4* src = static_cast<const uint4*>(p.x);
+    __device__ static void stage_x(const ActIn& a, unsigned char* xs, int MT) {
+        const int per_row = a.K / 8;
+        const uint4* src = static_cast<const uint4*>(a.x);
         uint4* dst = reinterpret_cast<uint4*>(xs);
-        for (int i = threadIdx.x; i < MT * per_row; i += kThreads) {
+        for (int i = threadIdx.x; i < MT * per_row; i += blockDim.x) {
             const int m = i / per_row;
-            uint4 v = m < p.M ? src[i] : make_uint4(0, 0, 0, 0);
+            uint4 v = m < a.M ? src[i] : make_uint4(0, 0, 0, 0);
             // halves h0..h7 -> h0 h4 h1 h5 h2 h6 h3 h7
             uint4 o;
             o.x = __byte_perm(v.x, v.z, 0x5410);  // h0, h4
@@ -221,8 +227,6 @@ struct PolicyW4A16 {
             dst[i] = o;
         }
     }
-    // Chunk c covers codes [32c, 32c + 32) of the row: group c / cpg, where
-    // cpg = group / 32 chunks share one scale; a row holds gk scales.
     __device__ __forceinline__ static void load(Chunk& ch, const RowRef& r, int c, int gk, int cpg) {
         ch.w = ld_stream16(r.w + (size_t)c * 16);
         ch.s = ld_stream_u16(static_cast<const uint16_t*>(r.scale) + (size_t)r.local * gk + c / cpg);
@@ -255,10 +259,9 @@ struct PolicyW4A16 {
             acc[m] = fmaf(P, s, acc[m]);
         }
     }
-    __device__ static float finish(const GemvParams&, const RowRef&, int, Acc a) { return a; }
-    __device__ static void store(const GemvParams& p, const RowRef& r, int m, Acc a) {
+    __device__ static float finish(const RowRef&, Acc a, float) { return a; }
+    __device__ static void store(const RowRef& r, int m, Acc a, float) {
         static_cast<__half*>(r.y)[(size_t)m * r.seg_rows + r.local] = __float2half_rn(a);
-        (void)p;
     }
 };
 
@@ -270,22 +273,23 @@ struct PolicyW4A16 {
 // the int32 sum of each 32-chunk.
 struct PolicyW4A8 {
     static constexpr int kElems = 32;
+    static constexpr bool kIntAct = true;
     using Acc = float;
     struct Chunk { uint4 w; uint16_t s; };
 
     __host__ __device__ static size_t row_bytes(int K) { return (size_t)K / 2; }
-    __host__ __device__ static size_t x_bytes(int MT, int K, int) {
+    __host__ __device__ static size_t x_bytes(int MT, int K) {
         return (size_t)MT * K + (size_t)MT * (K / 32) * 4;
     }
 
-    __device__ static void stage_x(const GemvParams& p, unsigned char* xs, int MT) {
-        const int K = p.K;
+    __device__ static void stage_x(const ActIn& a, unsigned char* xs, int MT) {
+        const int K = a.K;
         const int per_row = K / 8;
-        const uint2* src = reinterpret_cast<const uint2*>(p.xq);
+        const uint2* src = reinterpret_cast<const uint2*>(a.xq);
         uint2* dst = reinterpret_cast<uint2*>(xs);
-        for (int i = threadIdx.x; i < MT * per_row; i += kThreads) {
+        for (int i = threadIdx.x; i < MT * per_row; i += blockDim.x) {
             const int m = i / per_row;
-            uint2 v = m < p.M ? src[i] : make_uint2(0, 0);
+            uint2 v = m < a.M ? src[i] : make_uint2(0, 0);
             uint2 o;
             o.x = __byte_perm(v.x, v.y, 0x6420);  // x0 x2 x4 x6
             o.y = __byte_perm(v.x, v.y, 0x7531);  // x1 x3 x5 x7
@@ -293,20 +297,20 @@ struct PolicyW4A8 {
         }
         int* xsum = reinterpret_cast<int*>(xs + (size_t)MT * K);
         const int nch = K / 32;
-        const uint4* src16 = reinterpret_cast<const uint4*>(p.xq);
-        for (int i = threadIdx.x; i < MT * nch; i += kThreads) {
+        const uint4* src16 = reinterpret_cast<const uint4*>(a.xq);
+        for (int i = threadIdx.x; i < MT * nch; i += blockDim.x) {
             const int m = i / nch;
             int s = 0;
-            if (m < p.M) {
-                const uint4 a = src16[2 * i], b = src16[2 * i + 1];
-                s = dp4a_ss(a.x, 0x01010101u, s);
-                s = dp4a_ss(a.y, 0x01010101u, s);
-                s = dp4a_ss(a.z, 0x01010101u, s);
-                s = dp4a_ss(a.w, 0x01010101u, s);
-                s = dp4a_ss(b.x, 0x01010101u, s);
-                s = dp4a_ss(b.y, 0x01010101u, s);
-                s = dp4a_ss(b.z, 0x01010101u, s);
-                s = dp4a_ss(b.w, 0x01010101u, s);
+            if (m < a.M) {
+                const uint4 p = src16[2 * i], q = src16[2 * i + 1];
+                s = dp4a_ss(p.x, 0x01010101u, s);
+                s = dp4a_ss(p.y, 0x01010101u, s);
+                s = dp4a_ss(p.z, 0x01010101u, s);
+                s = dp4a_ss(p.w, 0x01010101u, s);
+                s = dp4a_ss(q.x, 0x01010101u, s);
+                s = dp4a_ss(q.y, 0x01010101u, s);
+                s = dp4a_ss(q.z, 0x01010101u, s);
+                s = dp4a_ss(q.w, 0x01010101u, s);
             }
             xsum[i] = s;
         }
@@ -345,16 +349,13 @@ struct PolicyW4A8 {
             acc[m] = fmaf((float)a, s, acc[m]);
         }
     }
-    __device__ static float finish(const GemvParams& p, const RowRef&, int m, Acc a) {
-        return __ldg(p.x_scale + m) * a;
-    }
-    __device__ static void store(const GemvParams& p, const RowRef& r, int m, Acc a) {
-        static_cast<__half*>(r.y)[(size_t)m * r.seg_rows + r.local] =
-            __float2half_rn(finish(p, r, m, a));
+    __device__ static float finish(const RowRef&, Acc a, float sx) { return sx * a; }
+    __device__ static void store(const RowRef& r, int m, Acc a, float sx) {
+        static_cast<__half*>(r.y)[(size_t)m * r.seg_rows + r.local] = __float2half_rn(sx * a);
     }
 };
 
-// ---- the kernel -----------------------------------------------------------------
+// ---- the row-group computation shared by all kernels ------------------------------
 
 // Chunks in flight per lane and row, by the number of accumulators.
 template <int MT, int R>
@@ -362,32 +363,127 @@ struct Unroll {
     static constexpr int v = (MT * R <= 2) ? 8 : (MT * R <= 8 ? 4 : 2);
 };
 
+// Geometry of one launch or phase, uniform over the CTA.
+struct RowGeom {
+    int K, nchunks, gk, cpg, ks;
+    size_t rb;
+};
+
+template <class P>
+__device__ __forceinline__ RowGeom row_geom(int K, int group, int ks) {
+    RowGeom g;
+    g.K = K;
+    g.nchunks = K / P::kElems;
+    g.gk = K / group;
+    g.cpg = group / 32;
+    g.ks = ks;
+    g.rb = P::row_bytes(K);
+    return g;
+}
+
+// Fills rows[] for row group rg of table t; invalid rows alias the first row
+// (loaded but dropped) so every load stays in bounds.
+template <int R>
+__device__ __forceinline__ void rows_of(const SegTable& t, int rg, bool active, size_t rb,
+                                        RowRef (&rows)[R]) {
+    RowRef z{};
+    const RowRef first = active ? locate(t, rg * R, rb, z) : z;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        rows[r] = active ? locate(t, rg * R + r, rb, first) : first;
+        if (!rows[r].valid) rows[r].w = first.w;
+    }
+}
+
+// Streams R rows for this lane and returns the per-row sums, complete in every
+// lane of the slot's first warp (kw == 0).  Every thread of the CTA must call
+// it (ks > 1 meets at CTA barriers); inactive slots pass active = false.
+template <class P, int MT, int R>
+__device__ __forceinline__ void row_group(const RowRef (&rows)[R], bool active, const RowGeom& g,
+                                          const unsigned char* xs, int* red,
+                                          typename P::Acc (&acc)[R][MT]) {
+    using Acc = typename P::Acc;
+    constexpr int U = Unroll<MT, R>::v;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int ks = g.ks;
+    const int kw = warp % ks;
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < MT; ++m) acc[r][m] = Acc(0);
+
+    if (active) {
+        const int step = ks * 32;
+        int c = kw * 32 + lane;
+        for (; c + (U - 1) * step < g.nchunks; c += U * step) {
+            typename P::Chunk ch[U][R];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int r = 0; r < R; ++r) P::load(ch[u][r], rows[r], c + u * step, g.gk, g.cpg);
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    P::template mac<MT>(acc[r], ch[u][r], xs, c + u * step, g.K);
+        }
+        for (; c < g.nchunks; c += step) {
+            typename P::Chunk ch[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) P::load(ch[r], rows[r], c, g.gk, g.cpg);
+#pragma unroll
+            for (int r = 0; r < R; ++r) P::template mac<MT>(acc[r], ch[r], xs, c, g.K);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < MT; ++m) acc[r][m] = warp_sum(acc[r][m]);
+
+    if (ks > 1) {
+        if (lane == 0) {
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int m = 0; m < MT; ++m) red[(warp * R + r) * MT + m] = to_bits(acc[r][m]);
+        }
+        __syncthreads();
+        if (kw == 0) {
+            for (int j = 1; j < ks; ++j) {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int m = 0; m < MT; ++m)
+                        acc[r][m] += from_bits<Acc>(red[((warp + j) * R + r) * MT + m]);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ---- the per-launch kernel ---------------------------------------------------------
+
 template <class P, int MT, int R, bool ARGMAX>
 __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     using Acc = typename P::Acc;
-    constexpr int U = Unroll<MT, R>::v;
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int ks = p.ksplit;
     const int slots = kWarps / ks;
     const int slot = warp / ks, kw = warp - slot * ks;
-    const int K = p.K;
-    const size_t rb = P::row_bytes(K);
-    const int nchunks = K / P::kElems;
-    const int gk = K / p.group;   // scale entries per row (int4)
-    const int cpg = p.group / 32; // 32-code chunks per scale group (int4)
-    const int n_rg = (p.N + R - 1) / R;
+    const RowGeom g = row_geom<P>(p.a.K, p.group, ks);
+    const int n_rg = (p.t.N + R - 1) / R;
 
     // Weights do not depend on the previous kernel: warm L2 with the rows this
     // CTA streams first while that kernel drains.
     if (p.prefetch_bytes > 0 && threadIdx.x < slots * R) {
         const int r = blockIdx.x * slots * R + threadIdx.x;
         RowRef z{};
-        const RowRef rr = locate(p, r, rb, z);
+        const RowRef rr = locate(p.t, r, g.rb, z);
         if (rr.valid) {
             const size_t cap = (size_t)p.prefetch_bytes / (size_t)(slots * R);
-            uint32_t n = (uint32_t)(rb < cap ? rb : cap);
+            uint32_t n = (uint32_t)(g.rb < cap ? g.rb : cap);
             n &= ~15u;
             if (n) prefetch_l2(rr.w, n);
         }
@@ -395,9 +491,9 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvP
     griddep_launch_dependents();
     griddep_wait();
 
-    P::stage_x(p, smem, MT);
+    P::stage_x(p.a, smem, MT);
     __syncthreads();
-    int* red = reinterpret_cast<int*>(smem + ((P::x_bytes(MT, K, p.group) + 15) & ~(size_t)15));
+    int* red = reinterpret_cast<int*>(smem + ((P::x_bytes(MT, g.K) + 15) & ~(size_t)15));
 
     float best_v = NAN;
     int best_i = INT_MAX;
@@ -406,75 +502,17 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvP
         const int rg = (it * (int)gridDim.x + (int)blockIdx.x) * slots + slot;
         const bool active = rg < n_rg;
         RowRef rows[R];
-        {
-            RowRef z{};
-            const RowRef first = active ? locate(p, rg * R, rb, z) : z;
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                rows[r] = active ? locate(p, rg * R + r, rb, first) : first;
-                if (!rows[r].valid) rows[r].w = first.w;  // load a valid row, drop its result
-            }
-        }
+        rows_of<R>(p.t, rg, active, g.rb, rows);
         Acc acc[R][MT];
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int m = 0; m < MT; ++m) acc[r][m] = Acc(0);
-
-        if (active) {
-            const int step = ks * 32;
-            int c = kw * 32 + lane;
-            for (; c + (U - 1) * step < nchunks; c += U * step) {
-                typename P::Chunk ch[U][R];
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-#pragma unroll
-                    for (int r = 0; r < R; ++r) P::load(ch[u][r], rows[r], c + u * step, gk, cpg);
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-#pragma unroll
-                    for (int r = 0; r < R; ++r)
-                        P::template mac<MT>(acc[r], ch[u][r], smem, c + u * step, K);
-            }
-            for (; c < nchunks; c += step) {
-                typename P::Chunk ch[R];
-#pragma unroll
-                for (int r = 0; r < R; ++r) P::load(ch[r], rows[r], c, gk, cpg);
-#pragma unroll
-                for (int r = 0; r < R; ++r) P::template mac<MT>(acc[r], ch[r], smem, c, K);
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int m = 0; m < MT; ++m) acc[r][m] = warp_sum(acc[r][m]);
-
-        if (ks > 1) {
-            if (lane == 0) {
-#pragma unroll
-                for (int r = 0; r < R; ++r)
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) red[(warp * R + r) * MT + m] = to_bits(acc[r][m]);
-            }
-            __syncthreads();
-            if (kw == 0) {
-                for (int j = 1; j < ks; ++j) {
-#pragma unroll
-                    for (int r = 0; r < R; ++r)
-#pragma unroll
-                        for (int m = 0; m < MT; ++m)
-                            acc[r][m] += from_bits<Acc>(red[((warp + j) * R + r) * MT + m]);
-                }
-            }
-            __syncthreads();
-        }
+        row_group<P, MT, R>(rows, active, g, smem, red, acc);
 
         if (kw == 0 && active) {
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 if (!rows[r].valid) continue;
                 if (ARGMAX) {
-                    const float v = P::finish(p, rows[r], 0, acc[r][0]);
+                    const float sx = p.a.x_scale ? __ldg(p.a.x_scale) : 1.f;
+                    const float v = P::finish(rows[r], acc[r][0], sx);
                     if (lane == 0) {
                         p.logits[rows[r].global] = v;
                         if (arg_better(v, rows[r].global, best_v, best_i)) {
@@ -485,7 +523,10 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvP
                 } else {
 #pragma unroll
                     for (int m = 0; m < MT; ++m)
-                        if (m < p.M && lane == ((r * MT + m) & 31)) P::store(p, rows[r], m, acc[r][m]);
+                        if (m < p.a.M && lane == ((r * MT + m) & 31)) {
+                            const float sx = p.a.x_scale ? __ldg(p.a.x_scale + m) : 1.f;
+                            P::store(rows[r], m, acc[r][m], sx);
+                        }
                 }
             }
         }
@@ -513,8 +554,8 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvP
 }
 
 template <class P>
-size_t smem_bytes_for(int MT, int K, int group) {
-    size_t x = (P::x_bytes(MT, K, group) + 15) & ~(size_t)15;
+size_t smem_bytes_for(int MT, int K) {
+    size_t x = (P::x_bytes(MT, K) + 15) & ~(size_t)15;
     return x + (size_t)kWarps * 4 * MT * 4 + (size_t)kWarps * sizeof(ArgPart);
 }
 
@@ -543,17 +584,30 @@ cudaError_t run_r(int R, const GemvParams* p, int grid, size_t smem, cudaStream_
     }
 }
 
+// The instantiations the launch heuristic can pick.
 template <class P>
 cudaError_t run_family(const GemvLaunch& L, const GemvParams* p, cudaStream_t s, int* occ) {
-    const size_t smem = smem_bytes_for<P>(L.MT, L.K, L.group);
-    if (L.argmax)
-        return L.MT == 1 ? run_r<P, 1, true>(L.R, p, L.grid, smem, s, occ) : cudaErrorInvalidValue;
+    const size_t smem = smem_bytes_for<P>(L.MT, L.K);
+    if (L.argmax) {
+        if constexpr (P::kIntAct && P::kElems == 16) {
+            return cudaErrorInvalidValue;  // no int8 lm_head
+        } else {
+            return L.MT == 1 ? run_r<P, 1, true>(L.R, p, L.grid, smem, s, occ)
+                             : cudaErrorInvalidValue;
+        }
+    }
     switch (L.MT) {
         case 1: return run_r<P, 1, false>(L.R, p, L.grid, smem, s, occ);
         case 2: return run_r<P, 2, false>(L.R, p, L.grid, smem, s, occ);
         case 4: return run_r<P, 4, false>(L.R, p, L.grid, smem, s, occ);
-        case 8: return run_r<P, 8, false>(L.R, p, L.grid, smem, s, occ);
-        case 16: return run_r<P, 16, false>(L.R, p, L.grid, smem, s, occ);
+        case 8:
+            return L.R == 1 ? run_one<P, 8, 1, false>(p, L.grid, smem, s, occ)
+                            : run_one<P, 8, 2, false>(p, L.grid, smem, s, occ);
+        case 16:
+            if constexpr (P::kElems == 16) {
+                if (L.R == 4) return run_one<P, 16, 4, false>(p, L.grid, smem, s, occ);
+            }
+            return run_one<P, 16, 1, false>(p, L.grid, smem, s, occ);
         default: return cudaErrorInvalidValue;
     }
 }

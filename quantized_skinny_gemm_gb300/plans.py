@@ -15,7 +15,7 @@ from typing import Dict, List, Optional
 
 import torch
 
-from . import LINEAR_F16, LINEAR_W4A16, LINEAR_W4A8, StepPlan, linear
+from . import LINEAR_F16, LINEAR_W4A16, LINEAR_W4A8, LINEAR_W8A8, StepPlan, linear
 
 
 class Arena:
@@ -62,29 +62,46 @@ def _nbytes(t):
     return t.numel() * t.element_size()
 
 
-def count_launches(ops):
-    """Launches dg_decode_step_weights issues for these ops (its fusion rule:
-    same kind, M, K, group and activation pointers, up to 4 ops, no lm_head;
-    an lm_head adds its second argmax pass; fp16 inputs of the quantized-
-    activation kinds add one quantization launch per fused run)."""
+def count_launches(ops, persistent=True):
+    """Kernel launches (memsets excluded) dg_decode_step_weights issues for
+    these ops: with the persistent kernel, one per run of single-token ops of
+    one kind (per 144 fused groups); otherwise one per fused group (same kind,
+    M, K, group and activation pointers, up to 4 ops, an lm_head alone), plus
+    the lm_head's argmax pass and one quantization launch per fused group with
+    fp16 inputs to an int8-activation kind."""
+    def groups(lo, hi):
+        out, i = [], lo
+        while i < hi:
+            a = ops[i]
+            j = i + 1
+            if not a.token:
+                while j < hi and j - i < 4:
+                    b = ops[j]
+                    if (b.token or b.kind != a.kind or b.M != a.M or b.K != a.K or b.x != a.x
+                            or b.x_i8 != a.x_i8 or b.x_scale != a.x_scale
+                            or b.group_size != a.group_size):
+                        break
+                    j += 1
+            out.append((i, j))
+            i = j
+        return out
+
     n, i = 0, 0
     while i < len(ops):
-        a = ops[i]
-        j = i + 1
-        if not a.token:
-            while j < len(ops) and j - i < 4:
-                b = ops[j]
-                if (b.token or b.kind != a.kind or b.M != a.M or b.K != a.K or b.x != a.x
-                        or b.x_i8 != a.x_i8 or b.x_scale != a.x_scale
-                        or b.group_size != a.group_size):
-                    break
-                j += 1
-        n += 1
-        if a.token:
-            n += 1
-        if a.kind == LINEAR_W4A8 and a.x:
-            n += 1
-        i = j
+        j = i
+        while persistent and j < len(ops) and ops[j].kind == ops[i].kind and ops[j].M == 1 \
+                and not ops[j].acc_out:
+            j += 1
+        if j > i:
+            g = len(groups(i, j))
+            n += (g + 143) // 144
+            i = j
+            continue
+        a, b = groups(i, len(ops))[0]
+        op = ops[a]
+        int8_act = op.kind in (LINEAR_W4A8, LINEAR_W8A8)
+        n += 1 + (1 if op.token else 0) + (1 if int8_act and op.x else 0)
+        i = b
     return n
 
 
@@ -115,7 +132,8 @@ def fp16_decode_step(layers, device, M=1) -> DeviceStep:
         outs.append(ys)
     keep += [ain.buf, aout.buf]
     plan = StepPlan(ops, keep)
-    return DeviceStep(plan, None, ins, outs, ain.buf, aout.buf, wbytes, count_launches(ops),
+    ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=device)
+    return DeviceStep(plan, ws, ins, outs, ain.buf, aout.buf, wbytes, count_launches(ops),
                       keep=keep)
 
 
@@ -177,7 +195,6 @@ def int4_decode_step(layers, head, x_head, device, act="a16", M=1, group=32) -> 
         wbytes += _nbytes(W) + _nbytes(S)
     keep += [ain.buf, aout.buf]
     plan = StepPlan(ops, keep)
-    nws = plan.workspace_bytes()
-    ws = torch.empty(nws, dtype=torch.uint8, device=device) if nws else None
+    ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=device)
     return DeviceStep(plan, ws, ins, outs, ain.buf, aout.buf, wbytes, count_launches(ops),
                       logits, token, xh, keep=keep)

