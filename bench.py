@@ -150,7 +150,8 @@ def build_workload(name, dev, torch):
                     "weight_bytes_per_step": st.weight_bytes,
                     "l2": "inputs 2.62 GB > 126 MB L2 (no flush)"}
         # dominant kernel: the fused gate|up launch of every layer
-        ops = [op for op in st.plan.array if op.N == 8960 and op.K == 1536]
+        ops = [dg.Linear.from_buffer_copy(op) for op in st.plan.array
+               if op.N == 8960 and op.K == 1536]
         dplan = plans.StepPlan(ops, [])
         dws = torch.empty(dplan.workspace_bytes(), dtype=torch.uint8, device=dev)
         w.dominant = ("gate|up 17920x1536 fp16",
@@ -172,9 +173,11 @@ def build_workload(name, dev, torch):
                                 % act[1:].upper(),
                     "weight_bytes_per_step": st.weight_bytes,
                     "l2": "inputs 4.22 GB > 126 MB L2 (no flush)"}
-        ops = [op for op in st.plan.array if op.N == 14336 and op.K == 4096 and not op.token]
-        for op in ops:
-            op.x = None  # codes already quantized by the step; time the GEMV alone
+        ops = [dg.Linear.from_buffer_copy(op) for op in st.plan.array
+               if op.N == 14336 and op.K == 4096 and not op.token]
+        if act == "a8":
+            for op in ops:
+                op.x = None  # codes already quantized by the step; time the GEMV alone
         dplan = plans.StepPlan(ops, [])
         dws = torch.empty(dplan.workspace_bytes(), dtype=torch.uint8, device=dev)
         w.dominant = ("gate|up 28672x4096 int4",
@@ -237,6 +240,64 @@ def build_workload(name, dev, torch):
                     "l2": "inputs 220 MB > 126 MB L2 (no flush)"}
         w.dominant = ("gate|up 17920x1536 fp16", w.run, 4, 2 * 8960 * 1536 * 2)
         w.cpu_sample = ("pairs", (pairs, x))
+    elif name == "decode_fp16_4l":
+        # small case of the fp16 decode step (4 layers, 374 MB > L2) for ncu captures
+        layers = synth.decode_fp16_workload(seed=0, layers=4)
+        st = plans.fp16_decode_step(layers, dev)
+        w.host = layers
+        w.in_arena, w.out_arena = st.in_arena, st.out_arena
+        w.unit_bytes = st.weight_bytes
+        w.launches = st.n_launches
+        w.run = lambda: dg.decode_step_weights(st.plan, st.ws, stream=s)
+        w.config = {"workload": "decode-step weight stream, 4 layers of the 1536-wide fp16 "
+                                "decoder, 28 matrices, M=1",
+                    "weight_bytes_per_step": st.weight_bytes,
+                    "l2": "inputs 374 MB > 126 MB L2 (no flush)"}
+        w.dominant = ("decode step (persistent kernel)", w.run, 1, st.weight_bytes)
+        w.cpu_sample = ("fp", layers)
+    elif name == "gemv_f16_2048" or name.startswith("w8a8_m"):
+        # one matrix called repeatedly; C rotating copies (> 2x L2 in total) keep
+        # every call cold.  A step is one call on each copy.
+        if name == "gemv_f16_2048":
+            W, x = synth.gemv_f16_workload(seed=0)
+            per = W.numel() * 2
+        else:
+            M = int(name[len("w8a8_m"):])
+            W, s_w, x = synth.w8a8_workload(M=M, seed=0)
+            per = W.numel() + s_w.numel() * 4
+        C = -(-2 * L2_BYTES // per)
+        ain, aout = plans.Arena(), plans.Arena()
+        ix = ain.reserve(x.shape, torch.float16)
+        iys = [aout.reserve((x.shape[0], W.shape[0]), torch.float16) for _ in range(C)]
+        xin, outs = ain.build(dev), aout.build(dev)
+        xd = xin[ix]
+        xd.copy_(x)
+        copies = [W.to(dev) for _ in range(C)]
+        if name == "gemv_f16_2048":
+            calls = [lambda Wd=Wd, y=outs[iy]: dg.gemv_f16(Wd, xd, y, stream=s)
+                     for Wd, iy in zip(copies, iys)]
+            w.dtype = "f16"
+            desc = "fp16 GEMV 2048x2048, M=1"
+            w.cpu_sample = ("pairs", ([(W, W)], x))
+        else:
+            swd = s_w.to(dev)
+            xq = torch.empty(x.shape, dtype=torch.int8, device=dev)
+            xs = torch.empty(x.shape[0], dtype=torch.float32, device=dev)
+            dg.quantize_act_i8(xd, xq, xs, stream=s)
+            calls = [lambda Wd=Wd, y=outs[iy]: dg.gemv_w8a8(Wd, swd, xq, xs, y=y, stream=s)
+                     for Wd, iy in zip(copies, iys)]
+            w.dtype = "i8"
+            desc = "W8A8 14336x4096 int8 GEMV, M=%d" % M
+            w.cpu_sample = ("w8", (W, s_w, x))
+        w.host = (W, x)
+        w.in_arena, w.out_arena = ain.buf, aout.buf
+        w.unit_bytes = C * per
+        w.launches = C
+        w.run = lambda: [c() for c in calls]
+        w.config = {"workload": desc, "bytes_per_call": per, "calls_per_step": C,
+                    "l2": "%d rotating weight copies, %.0f MB > 2x L2" % (C, C * per / 1e6)}
+        w.dominant = (desc, w.run, C, per)
+        w.keep = copies
     else:
         raise SystemExit("unknown workload %s" % name)
     return w
@@ -306,16 +367,28 @@ def oracle_sample(w, budget_s):
             if time.perf_counter() - t0 > budget_s:
                 break
         desc = "%d whole int4 matrices of the decoder in layer order" % mats
-    elif kind == "pairs":
-        pairs, x = data
-        for Wg, Wu in pairs:
-            for Wh in (Wg, Wu):
-                oracle.gemv_fp(bits(Wh), bits(x))
-                done += Wh.numel() * 2
-                mats += 1
+    elif kind == "w8":
+        import oracle as orc
+        W, s_w, x = data
+        q, sx = orc.quant_act(bits(x))
+        while True:
+            orc.gemv_w8a8(W.numpy(), s_w.numpy(), q, sx)
+            done += W.numel() + s_w.numel() * 4
+            mats += 1
             if time.perf_counter() - t0 > budget_s:
                 break
-        desc = "%d whole 8960x1536 fp16 matrices" % mats
+        desc = "%d whole W8A8 calls" % mats
+    elif kind == "pairs":
+        pairs, x = data
+        while True:
+            for Wg, Wu in pairs:
+                for Wh in (Wg, Wu):
+                    oracle.gemv_fp(bits(Wh), bits(x))
+                    done += Wh.numel() * 2
+                    mats += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        desc = "%d whole %dx%d fp16 matrices" % (mats, pairs[0][0].shape[0], pairs[0][0].shape[1])
     else:
         W, x = data
         rows = W.shape[0]
@@ -340,7 +413,8 @@ def main():
     ap.add_argument("--impl", default="dg", choices=["dg", "reference"])
     ap.add_argument("--workload", default="decode_fp16",
                     choices=["decode_fp16", "decode_int4_a16", "decode_int4_a8", "lm_head",
-                             "gateup_fp16"])
+                             "gateup_fp16", "decode_fp16_4l", "gemv_f16_2048", "w8a8_m1",
+                             "w8a8_m4", "w8a8_m16"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--quick", action="store_true",
                     help="time the step only (no dominant-kernel, e2e, probe or CPU legs); "

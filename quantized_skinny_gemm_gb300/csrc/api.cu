@@ -70,7 +70,7 @@ int* device_error_word() {
 // keeps the heuristic's choice.  STEP=0 runs decode steps as one launch per
 // fused group instead of the persistent step kernel.
 struct Tune {
-    int R = 0, KS = 0, CPS = 0, PF = -1, PDL = -1, STEP = -1, WIN = -1, SPIN = -1;
+    int R = 0, KS = 0, CPS = 0, PF = -1, PDL = -1, STEP = -1, WIN = -1, SPIN = -1, SNW = 0;
 };
 
 static Tune read_tune() {
@@ -90,6 +90,7 @@ static Tune read_tune() {
         else if (std::sscanf(tok, "STEP=%d", &v) == 1) t.STEP = v;
         else if (std::sscanf(tok, "WIN=%d", &v) == 1) t.WIN = v;
         else if (std::sscanf(tok, "SPIN=%d", &v) == 1) t.SPIN = v;
+        else if (std::sscanf(tok, "SNW=%d", &v) == 1) t.SNW = v;
     }
     return t;
 }
@@ -369,7 +370,7 @@ static int step_occupancy(Fmt f, int max_k, size_t smem) {
     }
     StepParams* none = nullptr;
     int occ = 0;
-    if (step_launch(f, none, 0, smem, nullptr, &occ) != cudaSuccess) occ = 0;
+    if (step_launch(f, none, 0, smem, nullptr, &occ, tune().SNW) != cudaSuccess) occ = 0;
     std::lock_guard<std::mutex> g(mu);
     cache[key] = occ;
     return occ;
@@ -433,7 +434,8 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
         const int grid = sm_count() * occ;
         if (grid > kMaxArgCtas) return DG_ERR_UNSUPPORTED;
         if (cudaMemsetAsync(ws, 0, 2 * sizeof(unsigned), s) != cudaSuccess) return DG_ERR_CUDA;
-        if (step_launch(f, &sp, grid, smem, s, nullptr) != cudaSuccess) return DG_ERR_CUDA;
+        if (step_launch(f, &sp, grid, smem, s, nullptr, tune().SNW) != cudaSuccess)
+            return DG_ERR_CUDA;
     }
     return DG_OK;
 }

@@ -247,9 +247,10 @@ dg_status launch_head(const dg_linear& op, void* parts, cudaStream_t s);
 int head_grid(const dg_linear& op);
 
 // Persistent decode-step kernel (step_kernel.cu): one cooperative launch over
-// sp.nphase phases of format f.  occ != nullptr: report CTAs per SM instead.
+// sp.nphase phases of format f, with nw warps per CTA (16, or 0 for the
+// format's default).  occ != nullptr: report CTAs per SM instead.
 cudaError_t step_launch(Fmt f, const StepParams* sp, int grid, size_t smem, cudaStream_t s,
-                        int* occ);
+                        int* occ, int nw);
 size_t step_smem(Fmt f, int max_k);
 cudaError_t launch_wait_selftest(unsigned limit, int* err, cudaStream_t s);
 

@@ -413,26 +413,23 @@ __device__ __forceinline__ void row_group(const RowRef (&rows)[R], bool active, 
         for (int m = 0; m < MT; ++m) acc[r][m] = Acc(0);
 
     if (active) {
+        // Batches of U chunks per row, all loads of a batch issued before any
+        // use (chunks past the row's end are skipped), so a short row costs one
+        // memory round trip; the sums still run in ascending chunk order.
         const int step = ks * 32;
-        int c = kw * 32 + lane;
-        for (; c + (U - 1) * step < g.nchunks; c += U * step) {
+        for (int c = kw * 32 + lane; c < g.nchunks; c += U * step) {
             typename P::Chunk ch[U][R];
 #pragma unroll
             for (int u = 0; u < U; ++u)
+                if (c + u * step < g.nchunks)
 #pragma unroll
-                for (int r = 0; r < R; ++r) P::load(ch[u][r], rows[r], c + u * step, g.gk, g.cpg);
+                    for (int r = 0; r < R; ++r) P::load(ch[u][r], rows[r], c + u * step, g.gk, g.cpg);
 #pragma unroll
             for (int u = 0; u < U; ++u)
+                if (c + u * step < g.nchunks)
 #pragma unroll
-                for (int r = 0; r < R; ++r)
-                    P::template mac<MT>(acc[r], ch[u][r], xs, c + u * step, g.K);
-        }
-        for (; c < g.nchunks; c += step) {
-            typename P::Chunk ch[R];
-#pragma unroll
-            for (int r = 0; r < R; ++r) P::load(ch[r], rows[r], c, g.gk, g.cpg);
-#pragma unroll
-            for (int r = 0; r < R; ++r) P::template mac<MT>(acc[r], ch[r], xs, c, g.K);
+                    for (int r = 0; r < R; ++r)
+                        P::template mac<MT>(acc[r], ch[u][r], xs, c + u * step, g.K);
         }
     }
 #pragma unroll

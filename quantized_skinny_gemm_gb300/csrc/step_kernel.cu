@@ -19,8 +19,9 @@
 
 namespace dg {
 
-constexpr int kStepR = 2;  // rows per slot (M = 1)
+constexpr int kStepR = 1;  // rows per slot (M = 1)
 
+// Warps per CTA (one CTA per SM): the default for each format, or 16.
 template <class P>
 struct StepCfg;
 template <bool B>
@@ -56,20 +57,23 @@ __device__ __forceinline__ int slice_begin(int N, int b, int G) {
 }
 
 // Grid barrier for a co-resident (cooperative) grid.  bar[0] counts arrivals
-// and returns to 0 at every barrier; bar[1] is the generation.
-__device__ __forceinline__ bool grid_barrier(unsigned* bar, unsigned nblocks, unsigned limit,
+// over the whole launch (zeroed before it); barrier number e (1, 2, ...)
+// completes when it reaches e * nblocks.  One release add per CTA, then
+// acquire polls: a single round trip after the last arrival.
+__device__ __forceinline__ bool grid_barrier(unsigned* bar, unsigned target, unsigned limit,
                                              int* err) {
     __syncthreads();
     int ok = 1;
     if (threadIdx.x == 0) {
-        const unsigned gen = ld_acquire_gpu(bar + 1);
         __threadfence();
-        if (atomicAdd(bar, 1u) == nblocks - 1) {
-            atomicExch(bar, 0u);
-            __threadfence();
-            atomicAdd(bar + 1, 1u);
-        } else {
-            ok = bounded_wait_change(bar + 1, gen, limit, err);
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(bar) : "memory");
+        for (unsigned n = 0; ld_acquire_gpu(bar) < target; ++n) {
+            if (n >= limit) {
+                atomicExch(err, kErrTimeout);
+                ok = 0;
+                break;
+            }
+            __nanosleep(32);
         }
         __threadfence();
     }
@@ -186,12 +190,11 @@ __host__ __device__ constexpr size_t step_smem_layout_x(int max_k) {
     return (P::x_bytes(1, max_k) + 15) & ~(size_t)15;
 }
 
-template <class P>
-__global__ void __launch_bounds__(StepCfg<P>::kWarps * 32, 1)
+template <class P, int NW>
+__global__ void __launch_bounds__(NW * 32, 1)
     k_step(const __grid_constant__ StepParams sp, int max_k) {
     extern __shared__ __align__(16) unsigned char smem[];
     using Acc = typename P::Acc;
-    constexpr int NW = StepCfg<P>::kWarps;
     constexpr int R = kStepR;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int G = gridDim.x, b = blockIdx.x;
@@ -209,7 +212,7 @@ __global__ void __launch_bounds__(StepCfg<P>::kWarps * 32, 1)
     for (int p = 0; p < sp.nphase; ++p) {
         const StepPhase& ph = sp.ph[p];
         if (p > 0) {
-            if (!grid_barrier(sp.bar, G, sp.spin_limit, sp.err)) return;
+            if (!grid_barrier(sp.bar, (unsigned)p * G, sp.spin_limit, sp.err)) return;
             if ((sp.ph[p - 1].flags & kPhaseHead) && b == 0 && threadIdx.x < 32) {
                 // greedy token of the previous (lm_head) phase from the CTAs' partials
                 float bv = NAN;
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(StepCfg<P>::kWarps * 32, 1)
     }
 
     if (sp.ph[sp.nphase - 1].flags & kPhaseHead) {
-        if (!grid_barrier(sp.bar, G, sp.spin_limit, sp.err)) return;
+        if (!grid_barrier(sp.bar, (unsigned)sp.nphase * G, sp.spin_limit, sp.err)) return;
         if (b == 0 && threadIdx.x < 32) {
             float bv = NAN;
             int bi = INT_MAX;
@@ -355,16 +358,16 @@ __global__ void __launch_bounds__(StepCfg<P>::kWarps * 32, 1)
 
 template <class P>
 size_t step_smem_for(int max_k) {
-    constexpr int NW = StepCfg<P>::kWarps;
+    constexpr int NW = 32;  // the largest CTA any format uses
     return step_smem_layout_x<P>(max_k) + (size_t)NW * kStepR * 4 + (size_t)NW * sizeof(ArgPart) +
            (size_t)NW * 4 + 16 + (size_t)max_k + 16;
 }
 
-template <class P>
-cudaError_t step_run(const StepParams* sp, int grid, size_t smem, cudaStream_t s, int* occ,
-                     int max_k) {
-    auto fn = k_step<P>;
-    constexpr int threads = StepCfg<P>::kWarps * 32;
+template <class P, int NW>
+cudaError_t step_run_nw(const StepParams* sp, int grid, size_t smem, cudaStream_t s, int* occ,
+                        int max_k) {
+    auto fn = k_step<P, NW>;
+    constexpr int threads = NW * 32;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
@@ -385,6 +388,13 @@ cudaError_t step_run(const StepParams* sp, int grid, size_t smem, cudaStream_t s
     return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(fn), args);
 }
 
+template <class P>
+cudaError_t step_run(const StepParams* sp, int grid, size_t smem, cudaStream_t s, int* occ,
+                     int max_k, int nw) {
+    if (nw == 16) return step_run_nw<P, 16>(sp, grid, smem, s, occ, max_k);
+    return step_run_nw<P, StepCfg<P>::kWarps>(sp, grid, smem, s, occ, max_k);
+}
+
 size_t step_smem(Fmt f, int max_k) {
     switch (f) {
         case F_F16:
@@ -397,17 +407,17 @@ size_t step_smem(Fmt f, int max_k) {
 }
 
 cudaError_t step_launch(Fmt f, const StepParams* sp, int grid, size_t smem, cudaStream_t s,
-                        int* occ) {
+                        int* occ, int nw) {
     int max_k = 0;
     if (sp)
         for (int p = 0; p < sp->nphase; ++p)
             if (sp->ph[p].K > max_k) max_k = sp->ph[p].K;
     switch (f) {
-        case F_F16: return step_run<PolicyFP<false>>(sp, grid, smem, s, occ, max_k);
-        case F_BF16: return step_run<PolicyFP<true>>(sp, grid, smem, s, occ, max_k);
-        case F_I8: return step_run<PolicyI8>(sp, grid, smem, s, occ, max_k);
-        case F_W4A16: return step_run<PolicyW4A16>(sp, grid, smem, s, occ, max_k);
-        case F_W4A8: return step_run<PolicyW4A8>(sp, grid, smem, s, occ, max_k);
+        case F_F16: return step_run<PolicyFP<false>>(sp, grid, smem, s, occ, max_k, nw);
+        case F_BF16: return step_run<PolicyFP<true>>(sp, grid, smem, s, occ, max_k, nw);
+        case F_I8: return step_run<PolicyI8>(sp, grid, smem, s, occ, max_k, nw);
+        case F_W4A16: return step_run<PolicyW4A16>(sp, grid, smem, s, occ, max_k, nw);
+        case F_W4A8: return step_run<PolicyW4A8>(sp, grid, smem, s, occ, max_k, nw);
     }
     return cudaErrorInvalidValue;
 }
