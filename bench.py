@@ -602,18 +602,34 @@ def run_reference(args, world):
         pass
 
     w = W()
-    if args.workload == "decode_fp16":
+    wl = args.workload
+    if wl in ("decode_fp16", "decode_fp16_4l"):
         w.cpu_sample = ("fp", synth.decode_fp16_workload(seed=0, layers=1))
-        cfg = "decode-step weight stream, 28-layer 1536-wide fp16 decoder (Qwen2.5-1.5B shape), 196 matrices, M=1"
-    elif args.workload.startswith("decode_int4"):
-        act = args.workload[-3:]
+        cfg = "decode-step weight stream, 1536-wide fp16 decoder (Qwen2.5-1.5B shape), M=1"
+    elif wl.startswith("decode_int4"):
+        act = wl[-3:]
         layers, head, xh = synth.decode_int4_workload(seed=0, layers=1, vocab=0)
         w.cpu_sample = ("w4" + act, (layers, head, xh))
-        cfg = "decode-step weight stream, 32-layer 4096-wide int4 g32 decoder (Llama-3.1-8B shape), W4%s, M=1" % act[1:].upper()
-    else:
-        W, x = synth.fp_case(15520, 2048, 1, seed=0)
-        w.cpu_sample = ("head", (W, x))
+        cfg = ("decode-step weight stream, 4096-wide int4 g32 decoder (Llama-3.1-8B shape), "
+               "W4%s, M=1" % act[1:].upper())
+    elif wl == "lm_head":
+        W_, x_ = synth.fp_case(15520, 2048, 1, seed=0)
+        w.cpu_sample = ("head", (W_, x_))
         cfg = "lm_head 248320x2048 fp16 with fused greedy argmax, M=1"
+    elif wl == "gateup_fp16":
+        g = synth.generator(0)
+        pair = (synth.normal((8960, 1536), synth.W_STD, g), synth.normal((8960, 1536), synth.W_STD, g))
+        w.cpu_sample = ("pairs", ([pair], synth.normal((1, 1536), 1.0, g)))
+        cfg = "fused gate|up 17920x1536 fp16, M=1"
+    elif wl == "gemv_f16_2048":
+        W_, x_ = synth.gemv_f16_workload(seed=0)
+        w.cpu_sample = ("pairs", ([(W_, W_)], x_))
+        cfg = "fp16 GEMV 2048x2048, M=1"
+    else:
+        M = int(wl[len("w8a8_m"):])
+        W_, s_w, x_ = synth.w8a8_workload(M=M, seed=0)
+        w.cpu_sample = ("w8", (W_, s_w, x_))
+        cfg = "W8A8 14336x4096 int8 GEMV, M=%d" % M
     # each step: one bounded sample (~1 s of oracle work)
     for _ in range(args.warmup):
         oracle_sample(w, 0.0)
@@ -628,7 +644,7 @@ def run_reference(args, world):
            "unit": "GB/s", "n_gpus": world, "steps": min(args.steps, 50), "warmup": args.warmup,
            "ms_per_step": round(secs / min(args.steps, 50) * 1e3, 3), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": cfg, "sample": "first layer's matrices per step"},
+           "config": {"workload": cfg, "sample": "about 1 s of whole-matrix oracle calls per step"},
            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": os.cpu_count(),
                             "kind": "oracle", "sample": desc},
            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

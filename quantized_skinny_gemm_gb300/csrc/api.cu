@@ -65,12 +65,13 @@ int* device_error_word() {
 }
 
 // ---- tuning knobs ------------------------------------------------------------------
-// DG_TUNE="R=2,KS=1,CPS=4,PF=32768,PDL=1,STEP=1,WIN=262144,SPIN=20000000"
+// DG_TUNE="R=2,KS=1,CPS=4,PF=32768,PDL=1,STEP=1,WIN=262144,SPIN=20000000,SNW=16,PFM=2"
 // overrides the launch heuristic (for configuration sweeps); an unset key
 // keeps the heuristic's choice.  STEP=0 runs decode steps as one launch per
 // fused group instead of the persistent step kernel.
 struct Tune {
-    int R = 0, KS = 0, CPS = 0, PF = -1, PDL = -1, STEP = -1, WIN = -1, SPIN = -1, SNW = 0;
+    int R = 0, KS = 0, CPS = 0, PF = -1, PDL = -1, STEP = -1, WIN = -1, SPIN = -1, SNW = 0,
+        PFM = -1;
 };
 
 static Tune read_tune() {
@@ -91,6 +92,7 @@ static Tune read_tune() {
         else if (std::sscanf(tok, "WIN=%d", &v) == 1) t.WIN = v;
         else if (std::sscanf(tok, "SPIN=%d", &v) == 1) t.SPIN = v;
         else if (std::sscanf(tok, "SNW=%d", &v) == 1) t.SNW = v;
+        else if (std::sscanf(tok, "PFM=%d", &v) == 1) t.PFM = v;
     }
     return t;
 }
@@ -142,6 +144,7 @@ static int pick_ks(Fmt f, int K) {
 static int pick_r(Fmt f, int MT) {
     const int t = tune().R;
     if (t == 1 || t == 2 || t == 4) return t;
+    if (MT == 1) return 1;
     if (MT <= 4) return 2;
     if (f == F_I8) return MT >= 16 ? 4 : 2;
     return 1;
@@ -185,7 +188,7 @@ static void configure(GemvLaunch& L, GemvParams& p) {
     const int need = (n_rg + slots - 1) / slots;
     int cps = occupancy(L);
     const int tc = tune().CPS;
-    cps = tc > 0 ? (tc < cps ? tc : cps) : (cps < 4 ? cps : 4);
+    cps = tc > 0 ? (tc < cps ? tc : cps) : (cps < 8 ? cps : 8);
     int maxg = sm_count() * cps;
     if (maxg < 1) maxg = 1;
     if (L.argmax && maxg > kMaxArgCtas) maxg = kMaxArgCtas;
@@ -422,6 +425,7 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
         }
         sp.group = ops[0].group_size >= 32 ? ops[0].group_size : 32;
         sp.window = tune().WIN >= 0 ? tune().WIN : 262144;
+        sp.pf_mode = tune().PFM >= 0 ? tune().PFM : 2;
         sp.spin_limit = tune().SPIN > 0 ? (unsigned)tune().SPIN : 20000000u;
         sp.bar = static_cast<unsigned*>(ws);
         sp.part = reinterpret_cast<ArgPart*>(static_cast<unsigned char*>(ws) + kStepHeader);

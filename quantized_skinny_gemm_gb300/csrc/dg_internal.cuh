@@ -92,7 +92,8 @@ struct StepParams {
     StepPhase ph[kMaxStepPhases];
     int nphase;
     int group;
-    int window;           // L2 prefetch lookahead per CTA, bytes
+    int window;           // L2 prefetch lookahead per CTA beyond the current phase, bytes
+    int pf_mode;          // 0 none, 1 bulk (TMA) prefetch, 2 per-lane line prefetch
     unsigned spin_limit;  // bound on every barrier wait
     unsigned* bar;        // 2 zeroed words: arrivals, generation
     ArgPart* part;        // one partial per CTA (lm_head phases)
@@ -110,6 +111,11 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;
+}
+
+// Hint L2 to fetch the 128-byte line holding p.
+__device__ __forceinline__ void prefetch_line_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 __device__ __forceinline__ uint16_t ld_stream_u16(const void* p) {

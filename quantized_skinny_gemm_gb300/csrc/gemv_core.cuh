@@ -197,11 +197,25 @@ __device__ __forceinline__ void unpack_int4x8_f16(uint32_t w, uint32_t (&q)[4]) 
     q[3] = h2_as_u32(__hfma2(u32_as_h2(and_xor(w8, 0x00F000F0u, 0x64806480u)), k16th, k72));
 }
 
+// Shared-memory layout of int4 activations: chunk c (32 codes) of a token is
+// cut into 16-byte pieces, and piece i of chunk c sits at
+//     ((c / 32) * pieces + i) * 512 + (c % 32) * 16
+// so the 32 lanes of a warp, which always hold chunks with c % 32 = lane,
+// read 32 consecutive 16-byte words: no bank conflicts.  A token's area is
+// padded to a multiple of 32 chunks.
+__host__ __device__ __forceinline__ size_t int4_x_token_bytes(int K, int piece_bytes_per_chunk) {
+    const size_t nch = (size_t)(K / 32);
+    return ((nch + 31) / 32) * 32 * (size_t)piece_bytes_per_chunk;
+}
+__device__ __forceinline__ size_t int4_x_piece(int c, int i, int pieces) {
+    return ((size_t)(c >> 5) * pieces + i) * 512 + (size_t)(c & 31) * 16;
+}
+
 // Groupwise int4 weights with fp16 activations; 32 codes per chunk.  Chunk c
 // covers codes [32c, 32c + 32) of the row and uses the scale of group c / cpg
-// (cpg = group / 32).  Activations are staged per 8-block in the order
-// x0 x4 x1 x5 x2 x6 x3 x7 so that a 16-byte shared load lines up with the
-// unpacked pairs.
+// (cpg = group / 32).  Within each 16-byte piece (8 activations) the order is
+// x0 x4 x1 x5 x2 x6 x3 x7, so that one shared load lines up with the unpacked
+// pairs.
 struct PolicyW4A16 {
     static constexpr int kElems = 32;
     static constexpr bool kIntAct = false;
@@ -209,14 +223,15 @@ struct PolicyW4A16 {
     struct Chunk { uint4 w; uint16_t s; };
 
     __host__ __device__ static size_t row_bytes(int K) { return (size_t)K / 2; }
-    __host__ __device__ static size_t x_bytes(int MT, int K) { return (size_t)MT * K * 2; }
+    __host__ __device__ static size_t token_bytes(int K) { return int4_x_token_bytes(K, 64); }
+    __host__ __device__ static size_t x_bytes(int MT, int K) { return (size_t)MT * token_bytes(K); }
 
     __device__ static void stage_x(const ActIn& a, unsigned char* xs, int MT) {
-        const int per_row = a.K / 8;
+        const int per_row = a.K / 8;  // 16-byte blocks of one token
         const uint4* src = static_cast<const uint4*>(a.x);
-        uint4* dst = reinterpret_cast<uint4*>(xs);
+        const size_t tb = token_bytes(a.K);
         for (int i = threadIdx.x; i < MT * per_row; i += blockDim.x) {
-            const int m = i / per_row;
+            const int m = i / per_row, blk = i - m * per_row;
             uint4 v = m < a.M ? src[i] : make_uint4(0, 0, 0, 0);
             // halves h0..h7 -> h0 h4 h1 h5 h2 h6 h3 h7
             uint4 o;
@@ -224,7 +239,7 @@ struct PolicyW4A16 {
             o.y = __byte_perm(v.x, v.z, 0x7632);  // h1, h5
             o.z = __byte_perm(v.y, v.w, 0x5410);  // h2, h6
             o.w = __byte_perm(v.y, v.w, 0x7632);  // h3, h7
-            dst[i] = o;
+            *reinterpret_cast<uint4*>(xs + m * tb + int4_x_piece(blk >> 2, blk & 3, 4)) = o;
         }
     }
     __device__ __forceinline__ static void load(Chunk& ch, const RowRef& r, int c, int gk, int cpg) {
@@ -240,13 +255,14 @@ struct PolicyW4A16 {
         unpack_int4x8_f16(ch.w.z, q[2]);
         unpack_int4x8_f16(ch.w.w, q[3]);
         const float s = __half2float(__ushort_as_half(ch.s));
+        const size_t tb = token_bytes(K);
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-            const unsigned char* xb = xs + ((size_t)m * K + (size_t)c * 32) * 2;
+            const unsigned char* xb = xs + m * tb;
             float P = 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const uint4 xv = *reinterpret_cast<const uint4*>(xb + i * 16);
+                const uint4 xv = *reinterpret_cast<const uint4*>(xb + int4_x_piece(c, i, 4));
                 P = fma_f16(lo16(q[i][0]), lo16(xv.x), P);
                 P = fma_f16(hi16(q[i][0]), hi16(xv.x), P);
                 P = fma_f16(lo16(q[i][1]), lo16(xv.y), P);
@@ -268,9 +284,10 @@ struct PolicyW4A16 {
 // Groupwise int4 weights with int8 activations.  Codes are biased to c + 8 in
 // [0, 15] (one LOP3 per four codes) and multiplied with dp4a (unsigned x
 // signed); the bias is removed exactly with the chunk's activation sum:
-// sum (c+8) x - 8 sum x = sum c x.  Activations are staged per 8-block as
-// x0 x2 x4 x6 | x1 x3 x5 x7 (even codes sit in low nibbles), followed by
-// the int32 sum of each 32-chunk.
+// sum (c+8) x - 8 sum x = sum c x.  Activations use the interleaved layout
+// above (two 16-byte pieces per chunk), each 8-byte block ordered
+// x0 x2 x4 x6 | x1 x3 x5 x7 (even codes sit in low nibbles), followed by the
+// int32 sum of each 32-chunk.
 struct PolicyW4A8 {
     static constexpr int kElems = 32;
     static constexpr bool kIntAct = true;
@@ -278,24 +295,27 @@ struct PolicyW4A8 {
     struct Chunk { uint4 w; uint16_t s; };
 
     __host__ __device__ static size_t row_bytes(int K) { return (size_t)K / 2; }
+    __host__ __device__ static size_t token_bytes(int K) { return int4_x_token_bytes(K, 32); }
     __host__ __device__ static size_t x_bytes(int MT, int K) {
-        return (size_t)MT * K + (size_t)MT * (K / 32) * 4;
+        return (size_t)MT * token_bytes(K) + (size_t)MT * (K / 32) * 4;
     }
 
     __device__ static void stage_x(const ActIn& a, unsigned char* xs, int MT) {
         const int K = a.K;
-        const int per_row = K / 8;
+        const int per_row = K / 8;  // 8-byte blocks of one token
         const uint2* src = reinterpret_cast<const uint2*>(a.xq);
-        uint2* dst = reinterpret_cast<uint2*>(xs);
+        const size_t tb = token_bytes(K);
         for (int i = threadIdx.x; i < MT * per_row; i += blockDim.x) {
-            const int m = i / per_row;
+            const int m = i / per_row, blk = i - m * per_row;
             uint2 v = m < a.M ? src[i] : make_uint2(0, 0);
             uint2 o;
             o.x = __byte_perm(v.x, v.y, 0x6420);  // x0 x2 x4 x6
             o.y = __byte_perm(v.x, v.y, 0x7531);  // x1 x3 x5 x7
-            dst[i] = o;
+            // block blk: chunk blk / 4, 16-byte piece (blk % 4) / 2, half blk % 2
+            *reinterpret_cast<uint2*>(xs + m * tb + int4_x_piece(blk >> 2, (blk >> 1) & 1, 2) +
+                                      (blk & 1) * 8) = o;
         }
-        int* xsum = reinterpret_cast<int*>(xs + (size_t)MT * K);
+        int* xsum = reinterpret_cast<int*>(xs + (size_t)MT * tb);
         const int nch = K / 32;
         const uint4* src16 = reinterpret_cast<const uint4*>(a.xq);
         for (int i = threadIdx.x; i < MT * nch; i += blockDim.x) {
@@ -330,13 +350,14 @@ struct PolicyW4A8 {
             hi[i] = and_xor(wv[i] >> 4, 0x0F0F0F0Fu, 0x08080808u);
         }
         const float s = __half2float(__ushort_as_half(ch.s));
-        const int* xsum = reinterpret_cast<const int*>(xs + (size_t)MT * K);
+        const size_t tb = token_bytes(K);
+        const int* xsum = reinterpret_cast<const int*>(xs + (size_t)MT * tb);
         const int nch = K / 32;
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-            const unsigned char* xb = xs + (size_t)m * K + (size_t)c * 32;
-            const uint4 x0 = *reinterpret_cast<const uint4*>(xb);
-            const uint4 x1 = *reinterpret_cast<const uint4*>(xb + 16);
+            const unsigned char* xb = xs + m * tb;
+            const uint4 x0 = *reinterpret_cast<const uint4*>(xb + int4_x_piece(c, 0, 2));
+            const uint4 x1 = *reinterpret_cast<const uint4*>(xb + int4_x_piece(c, 1, 2));
             int a = -8 * xsum[m * nch + c];
             a = dp4a_us(lo[0], x0.x, a);
             a = dp4a_us(hi[0], x0.y, a);

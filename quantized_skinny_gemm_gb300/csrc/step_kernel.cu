@@ -81,11 +81,12 @@ __device__ __forceinline__ bool grid_barrier(unsigned* bar, unsigned target, uns
 }
 
 // L2 prefetch cursor of one CTA: the next row (of its own slices, in phase
-// order) whose weights have not been prefetched yet.  Only thread 0 uses it.
+// order) whose weights have not been prefetched yet, and the bytes of its
+// stream before that row.  Kept identically by every lane of warp 0.
 struct Cursor {
     int phase;
-    int row;       // global row within `phase`
-    long long done;  // bytes prefetched so far (this CTA)
+    int row;         // global row within `phase`
+    long long done;  // bytes of this CTA's stream before (phase, row)
 };
 
 template <class P>
@@ -93,8 +94,22 @@ __device__ __forceinline__ size_t scale_row_bytes(int K, int group) {
     return P::kElems == 32 ? (size_t)(K / group) * 2 : 0;
 }
 
-// Advances the cursor until `target` bytes of this CTA's stream have been
-// requested, in pieces of at most 32 KB of consecutive rows of one matrix.
+__device__ __forceinline__ void prefetch_range(const unsigned char* p, size_t bytes, int mode) {
+    const int lane = threadIdx.x & 31;
+    if (mode == 1) {
+        if (lane == 0)
+            for (size_t off = 0; off < bytes; off += 32768) {
+                const size_t left = bytes - off;
+                prefetch_l2(p + off, (uint32_t)(left < 32768 ? left : 32768));
+            }
+    } else {
+        for (size_t off = (size_t)lane * 128; off < bytes; off += 32 * 128) prefetch_line_l2(p + off);
+    }
+}
+
+// Advances the cursor (all lanes of warp 0) until `target` bytes of this CTA's
+// stream have been requested, at most 32 KB of consecutive rows of one matrix
+// at a time.
 template <class P>
 __device__ void prefetch_until(const StepParams& sp, Cursor& cu, long long target) {
     const int G = gridDim.x, b = blockIdx.x;
@@ -119,16 +134,13 @@ __device__ void prefetch_until(const StepParams& sp, Cursor& cu, long long targe
         if (cap < 1) cap = 1;
         if (n > cap) n = cap;
         const size_t local = (size_t)(cu.row - sg.row_begin);
-        const unsigned char* w = static_cast<const unsigned char*>(sg.W) + local * rb;
-        for (size_t off = 0; off < (size_t)n * rb; off += 32768) {
-            const size_t left = (size_t)n * rb - off;
-            prefetch_l2(w + off, (uint32_t)(left < 32768 ? left : 32768));
-        }
+        prefetch_range(static_cast<const unsigned char*>(sg.W) + local * rb, (size_t)n * rb,
+                       sp.pf_mode);
         if (sb) {
             const unsigned char* sc = static_cast<const unsigned char*>(sg.scale) + local * sb;
             const size_t bytes = ((size_t)n * sb) & ~(size_t)15;
             // scale rows are 16-byte multiples when K / group is a multiple of 8
-            if (bytes && ((uintptr_t)sc & 15) == 0) prefetch_l2(sc, (uint32_t)bytes);
+            if (bytes && ((uintptr_t)sc & 15) == 0) prefetch_range(sc, bytes, sp.pf_mode);
         }
         cu.row += n;
         cu.done += (long long)n * (long long)(rb + sb);
@@ -235,7 +247,15 @@ __global__ void __launch_bounds__(NW * 32, 1)
             }
         }
         const long long here = slice_bytes<P>(sp, p, b, G);
-        if (threadIdx.x == 0) prefetch_until<P>(sp, cu, consumed + here + sp.window);
+        if (warp == 0 && sp.pf_mode != 0 && sp.window > 0) {
+            // the current phase is left to the demand loads: start at the next one
+            if (cu.phase <= p) {
+                cu.phase = p + 1;
+                cu.row = p + 1 < sp.nphase ? slice_begin(sp.ph[p + 1].N, b, G) : 0;
+                cu.done = consumed + here;
+            }
+            prefetch_until<P>(sp, cu, consumed + here + sp.window);
+        }
 
         // activations of this phase
         float sx = 1.f;
