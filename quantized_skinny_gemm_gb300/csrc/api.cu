@@ -8,6 +8,7 @@
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <vector>
 
 #include "dg_internal.cuh"
 
@@ -68,7 +69,8 @@ int* device_error_word() {
 // DG_TUNE="R=2,KS=1,CPS=4,PF=32768,PDL=1,STEP=1,WIN=262144,SPIN=20000000,SNW=16,PFM=2"
 // overrides the launch heuristic (for configuration sweeps); an unset key
 // keeps the heuristic's choice.  STEP=0 runs decode steps as one launch per
-// fused group instead of the persistent step kernel.
+// fused group instead of the persistent step kernel; STEP=2 puts a grid
+// barrier between every pair of phases of the persistent kernel.
 struct Tune {
     int R = 0, KS = 0, CPS = 0, PF = -1, PDL = -1, STEP = -1, WIN = -1, SPIN = -1, SNW = 0,
         PFM = -1;
@@ -379,20 +381,76 @@ static int step_occupancy(Fmt f, int max_k, size_t smem) {
     return occ;
 }
 
+// Byte ranges an op reads (activations) and writes (outputs); weights and
+// scales are read-only for the whole step and never conflict.
+struct Range {
+    uintptr_t lo, hi;
+};
+static bool overlaps(const Range& a, const Range& b) { return a.lo < b.hi && b.lo < a.hi; }
+static void add_range(std::vector<Range>& v, const void* p, size_t bytes) {
+    if (p && bytes) v.push_back({(uintptr_t)p, (uintptr_t)p + bytes});
+}
+static size_t act_elem_bytes(int kind) {
+    return (kind == DG_LINEAR_F16 || kind == DG_LINEAR_BF16 || kind == DG_LINEAR_W4A16) ? 2 : 1;
+}
+static void op_ranges(const dg_linear& op, std::vector<Range>& rd, std::vector<Range>& wr) {
+    const size_t M = (size_t)op.M, N = (size_t)op.N, K = (size_t)op.K;
+    if (quantized_act(op.kind)) {
+        if (op.x) {  // quantized here: reads fp16 x, writes the codes and scale
+            add_range(rd, op.x, M * K * 2);
+            add_range(wr, op.x_i8, M * K);
+            add_range(wr, op.x_scale, M * 4);
+        } else {
+            add_range(rd, op.x_i8, M * K);
+            add_range(rd, op.x_scale, M * 4);
+        }
+    } else {
+        add_range(rd, op.x, M * K * act_elem_bytes(op.kind));
+    }
+    add_range(wr, op.y, M * N * 2);
+    add_range(wr, op.logits, N * 4);
+    add_range(wr, op.token, 4);
+    add_range(wr, op.acc_out, M * N * 4);
+}
+static bool any_overlap(const std::vector<Range>& a, const std::vector<Range>& b) {
+    for (const Range& x : a)
+        for (const Range& y : b)
+            if (overlaps(x, y)) return true;
+    return false;
+}
+
 // Runs ops[0..n) (all of one kind, all step-eligible) with the persistent
-// kernel, in launches of at most kMaxStepPhases phases.
+// kernel, in launches of at most kMaxStepPhases phases.  A phase gets a grid
+// barrier when it conflicts with a phase since the previous barrier (RAW, WAR
+// or WAW on the activation / output ranges), or follows an lm_head (whose
+// token needs every CTA's partial).
 static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStream_t s) {
     static thread_local StepParams sp;
     const Fmt f = fmt_of(ops[0].kind);
+    const bool always_sync = tune().STEP == 2;  // barrier between every pair of phases
     int i = 0;
     while (i < n) {
         std::memset(&sp, 0, sizeof sp);
         int max_k = 0;
+        std::vector<Range> seen_rd, seen_wr;  // since the last barrier
+        bool after_head = false;
         while (i < n && sp.nphase < kMaxStepPhases) {
             const dg_linear& a = ops[i];
             int j = i + 1;
             if (!a.token)
                 while (j < n && j - i < kMaxSeg && same_group(a, ops[j])) ++j;
+            std::vector<Range> rd, wr;
+            for (int k = i; k < j; ++k) op_ranges(ops[k], rd, wr);
+            const bool conflict = any_overlap(seen_wr, rd) || any_overlap(seen_wr, wr) ||
+                                  any_overlap(seen_rd, wr);
+            if (sp.nphase > 0 && (conflict || after_head || always_sync)) {
+                seen_rd.clear();
+                seen_wr.clear();
+                sp.ph[sp.nphase].flags |= kPhaseBarrier;
+            }
+            seen_rd.insert(seen_rd.end(), rd.begin(), rd.end());
+            seen_wr.insert(seen_wr.end(), wr.begin(), wr.end());
+            after_head = a.token != nullptr;
             StepPhase& ph = sp.ph[sp.nphase++];
             int rows = 0;
             for (int k = i; k < j; ++k) {

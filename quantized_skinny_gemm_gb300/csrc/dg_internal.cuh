@@ -65,7 +65,7 @@ struct GemvParams {
 
 constexpr int kMaxStepPhases = 144;   // phases per launch (kernel parameter space)
 
-enum StepFlags : int { kPhaseHead = 1, kPhaseQuantize = 2 };
+enum StepFlags : int { kPhaseHead = 1, kPhaseQuantize = 2, kPhaseBarrier = 4 };
 
 struct StepSeg {
     const void* W;
@@ -75,8 +75,10 @@ struct StepSeg {
     int32_t row_begin;
 };
 
-// One phase = one fused group of ops; phases run in order, separated by a
-// grid-wide barrier (a phase may read what the previous one wrote).
+// One phase = one fused group of ops.  Phases run in order; a phase flagged
+// kPhaseBarrier starts only after every CTA finished every earlier phase (it
+// reads or overwrites memory an earlier phase wrote or read); other phases
+// only follow their own CTA's earlier work.
 struct StepPhase {
     StepSeg seg[kMaxSeg];
     const void* x;        // fp16 / bf16 activations (or the fp16 source to quantize)

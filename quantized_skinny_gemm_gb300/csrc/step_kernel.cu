@@ -3,14 +3,15 @@
 // taken one step further: one launch per step instead of one per op).
 //
 // One CTA per SM.  Each phase (a fused group of ops sharing their
-// activations) is split into contiguous row slices, one per CTA; phases run in
-// the ops' order and meet at a grid barrier, so a phase may read what the
-// previous one wrote.  Weights never depend on earlier phases, so each CTA
-// keeps an L2 prefetch cursor running ahead of its own consumption, across
-// phase boundaries, by a fixed window: HBM keeps streaming while the grid
-// meets at a barrier, and each phase starts from L2.  The per-row arithmetic
-// is the same device code as the per-launch kernel (gemv_core.cuh), so every
-// output is bitwise what the per-op entry points return.
+// activations) is split into contiguous row slices, one per CTA, and every CTA
+// walks the phases in the ops' order.  Where a phase depends on earlier ones
+// (it reads or overwrites memory they wrote, or overwrites what they read; the
+// host finds these from the ops' address ranges) the grid meets at a barrier
+// first; independent phases flow through without one, so the weight stream
+// never stops.  Optionally each CTA keeps an L2 prefetch cursor running ahead
+// of its own consumption across phases.  The per-row arithmetic is the same
+// device code as the per-launch kernel (gemv_core.cuh), so every output is
+// bitwise what the per-op entry points return.
 //
 // Every wait is bounded: a barrier that does not complete within the spin
 // limit records an error (reported by dg_check_device_status) and the CTA
@@ -219,12 +220,14 @@ __global__ void __launch_bounds__(NW * 32, 1)
     int8_t* qraw = reinterpret_cast<int8_t*>(sx_smem + 4);
 
     Cursor cu{0, slice_begin(sp.ph[0].N, b, G), 0};
+    unsigned nbar = 0;  // grid barriers passed
     long long consumed = 0;  // bytes of this CTA's slices before the current phase
 
     for (int p = 0; p < sp.nphase; ++p) {
         const StepPhase& ph = sp.ph[p];
-        if (p > 0) {
-            if (!grid_barrier(sp.bar, (unsigned)p * G, sp.spin_limit, sp.err)) return;
+        if (p > 0 && (ph.flags & kPhaseBarrier)) {
+            ++nbar;
+            if (!grid_barrier(sp.bar, nbar * G, sp.spin_limit, sp.err)) return;
             if ((sp.ph[p - 1].flags & kPhaseHead) && b == 0 && threadIdx.x < 32) {
                 // greedy token of the previous (lm_head) phase from the CTAs' partials
                 float bv = NAN;
@@ -353,7 +356,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
     }
 
     if (sp.ph[sp.nphase - 1].flags & kPhaseHead) {
-        if (!grid_barrier(sp.bar, (unsigned)sp.nphase * G, sp.spin_limit, sp.err)) return;
+        ++nbar;
+        if (!grid_barrier(sp.bar, nbar * G, sp.spin_limit, sp.err)) return;
         if (b == 0 && threadIdx.x < 32) {
             float bv = NAN;
             int bi = INT_MAX;

@@ -178,3 +178,49 @@ def test_bounded_wait_timeout_reaches_the_host_as_a_status():
     y = torch.empty(1, 64, dtype=torch.float16, device=DEV)
     dg.gemv_f16(W.to(DEV), x.to(DEV), y)
     sync()
+
+
+def test_dependent_ops_in_one_step_match_sequential_calls():
+    """An op that reads an earlier op's output (read after write) and an op
+    that overwrites an earlier op's input (write after read) force grid
+    barriers inside the persistent kernel; results equal sequential calls."""
+    need_gpu()
+    g = synth.generator(9)
+    K0, N1, N2, N3 = 1024, 2048, 1536, 3072
+    W1 = synth.normal((N1, K0), 0.02, g).to(DEV)
+    W2 = synth.normal((N2, N1), 0.02, g).to(DEV)
+    W3 = synth.normal((N3, N2), 0.02, g).to(DEV)
+    W4 = synth.normal((K0, N2), 0.02, g).to(DEV)
+    x0 = synth.normal((1, K0), 1.0, g).to(DEV)
+
+    def run_step():
+        buf = torch.zeros(1, 8192, dtype=torch.float16, device=DEV)
+        xa = buf[:, :K0]
+        xa.copy_(x0)
+        y1 = buf[:, 1024:1024 + N1]
+        y2 = buf[:, 3072:3072 + N2]
+        y3 = torch.empty(1, N3, dtype=torch.float16, device=DEV)
+        ops = [dg.linear(dg.LINEAR_F16, W1, 1, N1, K0, x=xa, y=y1),     # y1 = f(x)
+               dg.linear(dg.LINEAR_F16, W2, 1, N2, N1, x=y1, y=y2),     # reads y1 (RAW)
+               dg.linear(dg.LINEAR_F16, W3, 1, N3, N2, x=y2, y=y3),     # reads y2 (RAW)
+               dg.linear(dg.LINEAR_F16, W4, 1, K0, N2, x=y2, y=xa)]     # overwrites x (WAR)
+        plan = dg.StepPlan(ops, [buf, y3])
+        ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=DEV)
+        dg.decode_step_weights(plan, ws)
+        sync()
+        return y1.clone(), y2.clone(), y3.clone(), xa.clone()
+
+    def run_sequential():
+        y1 = torch.empty(1, N1, dtype=torch.float16, device=DEV)
+        y2 = torch.empty(1, N2, dtype=torch.float16, device=DEV)
+        y3 = torch.empty(1, N3, dtype=torch.float16, device=DEV)
+        y4 = torch.empty(1, K0, dtype=torch.float16, device=DEV)
+        dg.gemv_f16(W1, x0, y1)
+        dg.gemv_f16(W2, y1, y2)
+        dg.gemv_f16(W3, y2, y3)
+        dg.gemv_f16(W4, y2, y4)
+        sync()
+        return y1, y2, y3, y4
+
+    for got, ref in zip(run_step(), run_sequential()):
+        assert torch.equal(got, ref)
