@@ -240,6 +240,28 @@ def build_workload(name, dev, torch):
                     "l2": "inputs 220 MB > 126 MB L2 (no flush)"}
         w.dominant = ("gate|up 17920x1536 fp16", w.run, 4, 2 * 8960 * 1536 * 2)
         w.cpu_sample = ("pairs", (pairs, x))
+    elif name in ("gateup_w4a16", "gateup_w4a8"):
+        # the dominant launch of the int4 decoder alone: 2 layers' fused gate|up
+        # (2 x 66 MB, larger than L2)
+        act = name[-3:]
+        layers, _, _ = synth.decode_int4_workload(seed=0, layers=2, vocab=0)
+        sub = []
+        for L in layers:
+            L.linears = [l for l in L.linears if l.name in ("gate", "up")]
+            sub.append(L)
+        st = plans.int4_decode_step(sub, None, None, dev, act=act)
+        w.host = sub
+        w.in_arena, w.out_arena = st.in_arena, st.out_arena
+        w.unit_bytes = st.weight_bytes
+        w.launches = st.n_launches
+        w.run = lambda: dg.decode_step_weights(st.plan, st.ws, stream=s)
+        w.config = {"workload": "fused gate|up 28672x4096 int4 g32 (2 layers per step), W4%s, M=1"
+                                % act[1:].upper(),
+                    "weight_bytes_per_step": st.weight_bytes,
+                    "l2": "inputs 132 MB > 126 MB L2 (no flush)"}
+        w.dominant = ("gate|up 28672x4096 int4", w.run, 2, st.weight_bytes // 2)
+        w.cpu_sample = ("w4" + act, (sub, None, None))
+        w.dtype = "int4xf16" if act == "a16" else "int4xi8"
     elif name == "decode_fp16_4l":
         # small case of the fp16 decode step (4 layers, 374 MB > L2) for ncu captures
         layers = synth.decode_fp16_workload(seed=0, layers=4)
@@ -413,7 +435,8 @@ def main():
     ap.add_argument("--impl", default="dg", choices=["dg", "reference"])
     ap.add_argument("--workload", default="decode_fp16",
                     choices=["decode_fp16", "decode_int4_a16", "decode_int4_a8", "lm_head",
-                             "gateup_fp16", "decode_fp16_4l", "gemv_f16_2048", "w8a8_m1",
+                             "gateup_fp16", "gateup_w4a16", "gateup_w4a8", "decode_fp16_4l",
+                             "gemv_f16_2048", "w8a8_m1",
                              "w8a8_m4", "w8a8_m16"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--quick", action="store_true",
