@@ -66,14 +66,13 @@ int* device_error_word() {
 }
 
 // ---- tuning knobs ------------------------------------------------------------------
-// DG_TUNE="R=2,KS=1,CPS=4,PF=32768,PDL=1,STEP=1,WIN=262144,SPIN=20000000,SNW=16,PFM=2"
+// DG_TUNE="R=2,KS=1,CPS=4,PF=32768,PDL=1,STEP=1,SPIN=20000000,SNW=16"
 // overrides the launch heuristic (for configuration sweeps); an unset key
 // keeps the heuristic's choice.  STEP=0 runs decode steps as one launch per
 // fused group instead of the persistent step kernel; STEP=2 puts a grid
 // barrier between every pair of phases of the persistent kernel.
 struct Tune {
-    int R = 0, KS = 0, CPS = 0, PF = -1, PDL = -1, STEP = -1, WIN = -1, SPIN = -1, SNW = 0,
-        PFM = -1;
+    int R = 0, KS = 0, CPS = 0, PF = -1, PDL = -1, STEP = -1, SPIN = -1, SNW = 0;
 };
 
 static Tune read_tune() {
@@ -91,10 +90,8 @@ static Tune read_tune() {
         else if (std::sscanf(tok, "PF=%d", &v) == 1) t.PF = v;
         else if (std::sscanf(tok, "PDL=%d", &v) == 1) t.PDL = v;
         else if (std::sscanf(tok, "STEP=%d", &v) == 1) t.STEP = v;
-        else if (std::sscanf(tok, "WIN=%d", &v) == 1) t.WIN = v;
         else if (std::sscanf(tok, "SPIN=%d", &v) == 1) t.SPIN = v;
         else if (std::sscanf(tok, "SNW=%d", &v) == 1) t.SNW = v;
-        else if (std::sscanf(tok, "PFM=%d", &v) == 1) t.PFM = v;
     }
     return t;
 }
@@ -482,8 +479,6 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
             i = j;
         }
         sp.group = ops[0].group_size >= 32 ? ops[0].group_size : 32;
-        sp.window = tune().WIN >= 0 ? tune().WIN : 262144;
-        sp.pf_mode = tune().PFM >= 0 ? tune().PFM : 2;
         sp.spin_limit = tune().SPIN > 0 ? (unsigned)tune().SPIN : 20000000u;
         sp.bar = static_cast<unsigned*>(ws);
         sp.part = reinterpret_cast<ArgPart*>(static_cast<unsigned char*>(ws) + kStepHeader);

@@ -94,8 +94,6 @@ struct StepParams {
     StepPhase ph[kMaxStepPhases];
     int nphase;
     int group;
-    int window;           // L2 prefetch lookahead per CTA beyond the current phase, bytes
-    int pf_mode;          // 0 none, 1 bulk (TMA) prefetch, 2 per-lane line prefetch
     unsigned spin_limit;  // bound on every barrier wait
     unsigned* bar;        // 2 zeroed words: arrivals, generation
     ArgPart* part;        // one partial per CTA (lm_head phases)

@@ -8,8 +8,8 @@
 // (it reads or overwrites memory they wrote, or overwrites what they read; the
 // host finds these from the ops' address ranges) the grid meets at a barrier
 // first; independent phases flow through without one, so the weight stream
-// never stops.  Optionally each CTA keeps an L2 prefetch cursor running ahead
-// of its own consumption across phases.  The per-row arithmetic is the same
+// never stops; each CTA copies the next phase's activations into shared
+// memory while it streams the current one.  The per-row arithmetic is the same
 // device code as the per-launch kernel (gemv_core.cuh), so every output is
 // bitwise what the per-op entry points return.
 //
@@ -26,7 +26,7 @@ constexpr int kStepR = 1;  // rows per slot (M = 1)
 template <class P>
 struct StepCfg;
 template <bool B>
-struct StepCfg<PolicyFP<B>> { static constexpr int kWarps = 32; };
+struct StepCfg<PolicyFP<B>> { static constexpr int kWarps = 24; };
 template <>
 struct StepCfg<PolicyI8> { static constexpr int kWarps = 24; };
 template <>
@@ -81,81 +81,6 @@ __device__ __forceinline__ bool grid_barrier(unsigned* bar, unsigned target, uns
     return __syncthreads_and(ok) != 0;
 }
 
-// L2 prefetch cursor of one CTA: the next row (of its own slices, in phase
-// order) whose weights have not been prefetched yet, and the bytes of its
-// stream before that row.  Kept identically by every lane of warp 0.
-struct Cursor {
-    int phase;
-    int row;         // global row within `phase`
-    long long done;  // bytes of this CTA's stream before (phase, row)
-};
-
-template <class P>
-__device__ __forceinline__ size_t scale_row_bytes(int K, int group) {
-    return P::kElems == 32 ? (size_t)(K / group) * 2 : 0;
-}
-
-__device__ __forceinline__ void prefetch_range(const unsigned char* p, size_t bytes, int mode) {
-    const int lane = threadIdx.x & 31;
-    if (mode == 1) {
-        if (lane == 0)
-            for (size_t off = 0; off < bytes; off += 32768) {
-                const size_t left = bytes - off;
-                prefetch_l2(p + off, (uint32_t)(left < 32768 ? left : 32768));
-            }
-    } else {
-        for (size_t off = (size_t)lane * 128; off < bytes; off += 32 * 128) prefetch_line_l2(p + off);
-    }
-}
-
-// Advances the cursor (all lanes of warp 0) until `target` bytes of this CTA's
-// stream have been requested, at most 32 KB of consecutive rows of one matrix
-// at a time.
-template <class P>
-__device__ void prefetch_until(const StepParams& sp, Cursor& cu, long long target) {
-    const int G = gridDim.x, b = blockIdx.x;
-    while (cu.done < target && cu.phase < sp.nphase) {
-        const StepPhase& ph = sp.ph[cu.phase];
-        const int r1 = slice_begin(ph.N, b + 1, G);
-        if (cu.row >= r1) {
-            ++cu.phase;
-            if (cu.phase < sp.nphase) cu.row = slice_begin(sp.ph[cu.phase].N, b, G);
-            continue;
-        }
-        const size_t rb = P::row_bytes(ph.K);
-        const size_t sb = scale_row_bytes<P>(ph.K, sp.group);
-        int s = 0;
-#pragma unroll
-        for (int i = 1; i < kMaxSeg; ++i)
-            if (i < ph.nseg && cu.row >= ph.seg[i].row_begin) s = i;
-        const StepSeg& sg = ph.seg[s];
-        const int seg_end = sg.row_begin + sg.rows;
-        int n = (seg_end < r1 ? seg_end : r1) - cu.row;
-        int cap = (int)(32768 / rb);
-        if (cap < 1) cap = 1;
-        if (n > cap) n = cap;
-        const size_t local = (size_t)(cu.row - sg.row_begin);
-        prefetch_range(static_cast<const unsigned char*>(sg.W) + local * rb, (size_t)n * rb,
-                       sp.pf_mode);
-        if (sb) {
-            const unsigned char* sc = static_cast<const unsigned char*>(sg.scale) + local * sb;
-            const size_t bytes = ((size_t)n * sb) & ~(size_t)15;
-            // scale rows are 16-byte multiples when K / group is a multiple of 8
-            if (bytes && ((uintptr_t)sc & 15) == 0) prefetch_range(sc, bytes, sp.pf_mode);
-        }
-        cu.row += n;
-        cu.done += (long long)n * (long long)(rb + sb);
-    }
-}
-
-// Bytes of phase p's slice for CTA b.
-template <class P>
-__device__ __forceinline__ long long slice_bytes(const StepParams& sp, int p, int b, int G) {
-    const StepPhase& ph = sp.ph[p];
-    const long long rows = slice_begin(ph.N, b + 1, G) - slice_begin(ph.N, b, G);
-    return rows * (long long)(P::row_bytes(ph.K) + scale_row_bytes<P>(ph.K, sp.group));
-}
-
 // Per-token int8 quantization of the fp16 activations of one token into
 // shared memory, with the arithmetic of k_quant_act: amax = max |x|,
 // s = amax / 127 (IEEE), q = clamp(rne(x / s), -127, 127); s = 1, q = 0 if
@@ -203,6 +128,32 @@ __host__ __device__ constexpr size_t step_smem_layout_x(int max_k) {
     return (P::x_bytes(1, max_k) + 15) & ~(size_t)15;
 }
 
+// Raw activation bytes of a phase as they sit in global memory: fp16 / bf16 x,
+// or the given int8 codes.
+template <class P>
+__device__ __forceinline__ int raw_act_bytes(const StepPhase& ph) {
+    return (P::kIntAct && !(ph.flags & kPhaseQuantize)) ? ph.K : ph.K * 2;
+}
+template <class P>
+__device__ __forceinline__ const void* raw_act_src(const StepPhase& ph) {
+    return (P::kIntAct && !(ph.flags & kPhaseQuantize)) ? static_cast<const void*>(ph.xq) : ph.x;
+}
+
+// Copies `bytes` (a multiple of 16, 16-byte aligned ends) from global to
+// shared memory with cp.async, all threads of the CTA, one commit group.
+__device__ __forceinline__ void async_copy_block(void* dst, const void* src, int bytes) {
+    for (int off = threadIdx.x * 16; off < bytes; off += blockDim.x * 16) {
+        const unsigned s = (unsigned)__cvta_generic_to_shared(static_cast<char*>(dst) + off);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s),
+                     "l"(static_cast<const char*>(src) + off)
+                     : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void async_wait_all() {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
 template <class P, int NW>
 __global__ void __launch_bounds__(NW * 32, 1)
     k_step(const __grid_constant__ StepParams sp, int max_k) {
@@ -212,16 +163,19 @@ __global__ void __launch_bounds__(NW * 32, 1)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int G = gridDim.x, b = blockIdx.x;
 
-    unsigned char* xs = smem;
-    int* red = reinterpret_cast<int*>(smem + step_smem_layout_x<P>(max_k));
+    // shared memory: staged activations | two raw activation buffers | scratch
+    const size_t raw_bytes = ((size_t)max_k * 2 + 15) & ~(size_t)15;
+    unsigned char* xs_fmt = smem;
+    unsigned char* rawx[2] = {smem + step_smem_layout_x<P>(max_k),
+                              smem + step_smem_layout_x<P>(max_k) + raw_bytes};
+    int* red = reinterpret_cast<int*>(rawx[1] + raw_bytes);
     ArgPart* cta_best = reinterpret_cast<ArgPart*>(red + NW * R);
     float* fred = reinterpret_cast<float*>(cta_best + NW);
     float* sx_smem = fred + NW;
     int8_t* qraw = reinterpret_cast<int8_t*>(sx_smem + 4);
+    bool staged_ahead = false;  // this phase's raw activations are already in flight
 
-    Cursor cu{0, slice_begin(sp.ph[0].N, b, G), 0};
     unsigned nbar = 0;  // grid barriers passed
-    long long consumed = 0;  // bytes of this CTA's slices before the current phase
 
     for (int p = 0; p < sp.nphase; ++p) {
         const StepPhase& ph = sp.ph[p];
@@ -249,23 +203,23 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 if (lane == 0) *sp.ph[p - 1].token = bi == INT_MAX ? -1 : bi;
             }
         }
-        const long long here = slice_bytes<P>(sp, p, b, G);
-        if (warp == 0 && sp.pf_mode != 0 && sp.window > 0) {
-            // the current phase is left to the demand loads: start at the next one
-            if (cu.phase <= p) {
-                cu.phase = p + 1;
-                cu.row = p + 1 < sp.nphase ? slice_begin(sp.ph[p + 1].N, b, G) : 0;
-                cu.done = consumed + here;
-            }
-            prefetch_until<P>(sp, cu, consumed + here + sp.window);
+        // activations of this phase: raw bytes in rawx[p & 1] (copied ahead
+        // during the previous phase when no barrier separates them)
+        unsigned char* raw = rawx[p & 1];
+        if (!staged_ahead) async_copy_block(raw, raw_act_src<P>(ph), raw_act_bytes<P>(ph));
+        async_wait_all();
+        __syncthreads();
+        staged_ahead = false;
+        if (p + 1 < sp.nphase && !(sp.ph[p + 1].flags & kPhaseBarrier)) {
+            const StepPhase& nx = sp.ph[p + 1];
+            async_copy_block(rawx[(p + 1) & 1], raw_act_src<P>(nx), raw_act_bytes<P>(nx));
+            staged_ahead = true;
         }
-
-        // activations of this phase
         float sx = 1.f;
-        ActIn a{ph.x, ph.xq, ph.x_scale, ph.K, 1};
+        ActIn a{raw, reinterpret_cast<const int8_t*>(raw), ph.x_scale, ph.K, 1};
         if constexpr (P::kIntAct) {
             if (ph.flags & kPhaseQuantize) {
-                const float s = quantize_token_smem(static_cast<const __half*>(ph.x), ph.K, qraw, fred);
+                const float s = quantize_token_smem(reinterpret_cast<const __half*>(raw), ph.K, qraw, fred);
                 __syncthreads();
                 if (b == 0) {  // the documented side outputs of the fused quantization
                     if (ph.xq_out)
@@ -280,8 +234,13 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 sx = __ldg(ph.x_scale);
             }
         }
-        P::stage_x(a, xs, 1);
-        __syncthreads();
+        // fp16 / bf16 activations are used as copied; the int formats restage
+        unsigned char* xs = raw;
+        if constexpr (P::kIntAct || P::kElems == 32) {
+            xs = xs_fmt;
+            P::stage_x(a, xs, 1);
+            __syncthreads();
+        }
 
         const int ks = ph.ks;
         const int slots = NW / ks;
@@ -351,7 +310,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 sp.part[b].i = bi;
             }
         }
-        consumed += here;
         __syncthreads();  // shared activations are restaged by the next phase
     }
 
@@ -383,8 +341,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
 template <class P>
 size_t step_smem_for(int max_k) {
     constexpr int NW = 32;  // the largest CTA any format uses
-    return step_smem_layout_x<P>(max_k) + (size_t)NW * kStepR * 4 + (size_t)NW * sizeof(ArgPart) +
-           (size_t)NW * 4 + 16 + (size_t)max_k + 16;
+    const size_t raw_bytes = ((size_t)max_k * 2 + 15) & ~(size_t)15;
+    return step_smem_layout_x<P>(max_k) + 2 * raw_bytes + (size_t)NW * kStepR * 4 +
+           (size_t)NW * sizeof(ArgPart) + (size_t)NW * 4 + 16 + (size_t)max_k + 16;
 }
 
 template <class P, int NW>
