@@ -94,7 +94,8 @@ typedef struct {
 
 /* FP16 / BF16 weights (paragraph on the custom M=1 cube matmul of the Orange
  * Pi AIPro post; the vector-matrix product at M=1).
- * W [N][K], x [M][K], y [M][N], all of type t; 1 <= M <= 16.
+ * W [N][K], x [M][K], y [M][N], all of type t; 1 <= M <= 16 and M * K * 4
+ * bytes within the shared memory of one CTA (DG_ERR_UNSUPPORTED otherwise).
  * Products are exact in fp32 and summed in fp32; y = round-to-nearest-even of
  * the fp32 sum.  ws may be NULL (this call needs no workspace). */
 dg_status dg_gemv_f16(const void* W, const void* x, void* y, dg_ftype t, int M, int N, int K,
@@ -119,7 +120,9 @@ dg_status dg_gemv_w8a8(const int8_t* W, const float* w_scale, const int8_t* x,
  *                           P_g = sum_{k in g} q[n][k] * x[m][k]   (fp32)
  * W4A8 when x_i8 != NULL:   acc_g = sum_{k in g} q * x_i8 (exact int32),
  *                           y = fp16( x_scale[m] * sum_g s[n][g] * acc_g ).
- * x_f16 [M][K] is read for W4A16 and ignored for W4A8.  1 <= M <= 16. */
+ * x_f16 [M][K] is read for W4A16 and ignored for W4A8.  1 <= M <= 16, and the
+ * staged activations (4 bytes per element for W4A16, about 1 for W4A8) must
+ * fit one CTA's shared memory (DG_ERR_UNSUPPORTED otherwise). */
 dg_status dg_gemv_w4(const uint8_t* Wq, const void* scales, int group_size, const void* x_f16,
                      const int8_t* x_i8, const float* x_scale, void* y, int M, int N, int K,
                      void* ws, size_t ws_bytes, dg_stream stream);

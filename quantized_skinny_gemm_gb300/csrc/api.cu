@@ -143,7 +143,7 @@ static int pick_ks(Fmt f, int K) {
 static int pick_r(Fmt f, int MT) {
     const int t = tune().R;
     if (t == 1 || t == 2 || t == 4) return t;
-    if (MT == 1) return 1;
+    if (MT == 1) return (f == F_W4A16 || f == F_W4A8) ? 2 : 1;
     if (MT <= 4) return 2;
     if (f == F_I8) return MT >= 16 ? 4 : 2;
     return 1;

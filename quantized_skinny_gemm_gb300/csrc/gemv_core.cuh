@@ -77,7 +77,17 @@ __device__ __forceinline__ int from_bits<int>(int v) { return v; }
 // stage_x fills the CTA's activation area from `a`; the int8 policies read
 // their codes from `a.xq`, which may point to global or shared memory.
 
-// fp16 / bf16 weights and activations; 8 elements per chunk.
+// Two fp16 (or bf16) values of a packed word, converted exactly to fp32.
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2_f32(uint32_t w) {
+    if (BF16) return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    return __half22float2(u32_as_h2(w));
+}
+
+// fp16 / bf16 weights and activations; 8 elements per chunk.  Activations are
+// staged as fp32 (exact), so each weight pair costs one packed conversion and
+// two fp32 FMAs: the product of two 11-bit (8-bit) significands is exact in
+// fp32 and each FMA rounds once, in ascending k.
 template <bool BF16>
 struct PolicyFP {
     static constexpr int kElems = 8;
@@ -86,39 +96,41 @@ struct PolicyFP {
     struct Chunk { uint4 w; };
 
     __host__ __device__ static size_t row_bytes(int K) { return (size_t)K * 2; }
-    __host__ __device__ static size_t x_bytes(int MT, int K) { return (size_t)MT * K * 2; }
+    __host__ __device__ static size_t x_bytes(int MT, int K) { return (size_t)MT * K * 4; }
 
     __device__ static void stage_x(const ActIn& a, unsigned char* xs, int MT) {
         const int per_row = a.K / 8;
         const uint4* src = static_cast<const uint4*>(a.x);
-        uint4* dst = reinterpret_cast<uint4*>(xs);
+        float4* dst = reinterpret_cast<float4*>(xs);
         for (int i = threadIdx.x; i < MT * per_row; i += blockDim.x) {
             const int m = i / per_row;
-            dst[i] = m < a.M ? src[i] : make_uint4(0, 0, 0, 0);
+            const uint4 v = m < a.M ? src[i] : make_uint4(0, 0, 0, 0);
+            const float2 f0 = unpack2_f32<BF16>(v.x), f1 = unpack2_f32<BF16>(v.y);
+            const float2 f2 = unpack2_f32<BF16>(v.z), f3 = unpack2_f32<BF16>(v.w);
+            dst[2 * i] = make_float4(f0.x, f0.y, f1.x, f1.y);
+            dst[2 * i + 1] = make_float4(f2.x, f2.y, f3.x, f3.y);
         }
     }
     __device__ __forceinline__ static void load(Chunk& ch, const RowRef& r, int c, int, int) {
         ch.w = ld_stream16(r.w + (size_t)c * 16);
     }
-    __device__ __forceinline__ static float mac2(uint32_t w, uint32_t x, float a) {
-        if (BF16) {
-            a = fma_bf16(lo16(w), lo16(x), a);
-            return fma_bf16(hi16(w), hi16(x), a);
-        }
-        a = fma_f16(lo16(w), lo16(x), a);
-        return fma_f16(hi16(w), hi16(x), a);
+    __device__ __forceinline__ static float mac2(uint32_t w, float x0, float x1, float a) {
+        const float2 f = unpack2_f32<BF16>(w);
+        a = fmaf(f.x, x0, a);
+        return fmaf(f.y, x1, a);
     }
     template <int MT>
     __device__ __forceinline__ static void mac(Acc (&acc)[MT], const Chunk& ch,
                                                const unsigned char* xs, int c, int K) {
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-            const uint4 xv = *reinterpret_cast<const uint4*>(xs + ((size_t)m * K + (size_t)c * 8) * 2);
+            const float4* xv = reinterpret_cast<const float4*>(xs + ((size_t)m * K + (size_t)c * 8) * 4);
+            const float4 x0 = xv[0], x1 = xv[1];
             float a = acc[m];
-            a = mac2(ch.w.x, xv.x, a);
-            a = mac2(ch.w.y, xv.y, a);
-            a = mac2(ch.w.z, xv.z, a);
-            a = mac2(ch.w.w, xv.w, a);
+            a = mac2(ch.w.x, x0.x, x0.y, a);
+            a = mac2(ch.w.y, x0.z, x0.w, a);
+            a = mac2(ch.w.z, x1.x, x1.y, a);
+            a = mac2(ch.w.w, x1.z, x1.w, a);
             acc[m] = a;
         }
     }
@@ -207,15 +219,20 @@ __host__ __device__ __forceinline__ size_t int4_x_token_bytes(int K, int piece_b
     const size_t nch = (size_t)(K / 32);
     return ((nch + 31) / 32) * 32 * (size_t)piece_bytes_per_chunk;
 }
+// Scale group of chunk c when cpg chunks share a scale (no division in the
+// common case of one 32-code group per chunk).
+__device__ __forceinline__ int group_of_chunk(int c, int cpg) { return cpg == 1 ? c : c / cpg; }
+
 __device__ __forceinline__ size_t int4_x_piece(int c, int i, int pieces) {
     return ((size_t)(c >> 5) * pieces + i) * 512 + (size_t)(c & 31) * 16;
 }
 
 // Groupwise int4 weights with fp16 activations; 32 codes per chunk.  Chunk c
 // covers codes [32c, 32c + 32) of the row and uses the scale of group c / cpg
-// (cpg = group / 32).  Within each 16-byte piece (8 activations) the order is
-// x0 x4 x1 x5 x2 x6 x3 x7, so that one shared load lines up with the unpacked
-// pairs.
+// (cpg = group / 32).  Activations are staged as fp32 (exact) in the
+// interleaved layout, eight 16-byte pieces per chunk, each 8-block ordered
+// x0 x4 x1 x5 x2 x6 x3 x7 to line up with the unpacked pairs; q x is exact in
+// fp32 and each FMA rounds once.
 struct PolicyW4A16 {
     static constexpr int kElems = 32;
     static constexpr bool kIntAct = false;
@@ -223,28 +240,31 @@ struct PolicyW4A16 {
     struct Chunk { uint4 w; uint16_t s; };
 
     __host__ __device__ static size_t row_bytes(int K) { return (size_t)K / 2; }
-    __host__ __device__ static size_t token_bytes(int K) { return int4_x_token_bytes(K, 64); }
+    __host__ __device__ static size_t token_bytes(int K) { return int4_x_token_bytes(K, 128); }
     __host__ __device__ static size_t x_bytes(int MT, int K) { return (size_t)MT * token_bytes(K); }
 
     __device__ static void stage_x(const ActIn& a, unsigned char* xs, int MT) {
-        const int per_row = a.K / 8;  // 16-byte blocks of one token
+        const int per_row = a.K / 8;  // 16-byte blocks (8 halves) of one token
         const uint4* src = static_cast<const uint4*>(a.x);
         const size_t tb = token_bytes(a.K);
         for (int i = threadIdx.x; i < MT * per_row; i += blockDim.x) {
             const int m = i / per_row, blk = i - m * per_row;
-            uint4 v = m < a.M ? src[i] : make_uint4(0, 0, 0, 0);
-            // halves h0..h7 -> h0 h4 h1 h5 h2 h6 h3 h7
-            uint4 o;
-            o.x = __byte_perm(v.x, v.z, 0x5410);  // h0, h4
-            o.y = __byte_perm(v.x, v.z, 0x7632);  // h1, h5
-            o.z = __byte_perm(v.y, v.w, 0x5410);  // h2, h6
-            o.w = __byte_perm(v.y, v.w, 0x7632);  // h3, h7
-            *reinterpret_cast<uint4*>(xs + m * tb + int4_x_piece(blk >> 2, blk & 3, 4)) = o;
+            const uint4 v = m < a.M ? src[i] : make_uint4(0, 0, 0, 0);
+            const float2 h01 = unpack2_f32<false>(v.x), h23 = unpack2_f32<false>(v.y);
+            const float2 h45 = unpack2_f32<false>(v.z), h67 = unpack2_f32<false>(v.w);
+            // block blk = word blk % 4 of chunk blk / 4: pieces 2w and 2w + 1
+            unsigned char* base = xs + m * tb;
+            const int c = blk >> 2, wd = blk & 3;
+            *reinterpret_cast<float4*>(base + int4_x_piece(c, 2 * wd, 8)) =
+                make_float4(h01.x, h45.x, h01.y, h45.y);  // x0 x4 x1 x5
+            *reinterpret_cast<float4*>(base + int4_x_piece(c, 2 * wd + 1, 8)) =
+                make_float4(h23.x, h67.x, h23.y, h67.y);  // x2 x6 x3 x7
         }
     }
     __device__ __forceinline__ static void load(Chunk& ch, const RowRef& r, int c, int gk, int cpg) {
         ch.w = ld_stream16(r.w + (size_t)c * 16);
-        ch.s = ld_stream_u16(static_cast<const uint16_t*>(r.scale) + (size_t)r.local * gk + c / cpg);
+        ch.s = ld_stream_u16(static_cast<const uint16_t*>(r.scale) + (size_t)r.local * gk +
+                             group_of_chunk(c, cpg));
     }
     template <int MT>
     __device__ __forceinline__ static void mac(Acc (&acc)[MT], const Chunk& ch,
@@ -262,15 +282,18 @@ struct PolicyW4A16 {
             float P = 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const uint4 xv = *reinterpret_cast<const uint4*>(xb + int4_x_piece(c, i, 4));
-                P = fma_f16(lo16(q[i][0]), lo16(xv.x), P);
-                P = fma_f16(hi16(q[i][0]), hi16(xv.x), P);
-                P = fma_f16(lo16(q[i][1]), lo16(xv.y), P);
-                P = fma_f16(hi16(q[i][1]), hi16(xv.y), P);
-                P = fma_f16(lo16(q[i][2]), lo16(xv.z), P);
-                P = fma_f16(hi16(q[i][2]), hi16(xv.z), P);
-                P = fma_f16(lo16(q[i][3]), lo16(xv.w), P);
-                P = fma_f16(hi16(q[i][3]), hi16(xv.w), P);
+                const float4 xa = *reinterpret_cast<const float4*>(xb + int4_x_piece(c, 2 * i, 8));
+                const float4 xc = *reinterpret_cast<const float4*>(xb + int4_x_piece(c, 2 * i + 1, 8));
+                const float2 q04 = unpack2_f32<false>(q[i][0]), q15 = unpack2_f32<false>(q[i][1]);
+                const float2 q26 = unpack2_f32<false>(q[i][2]), q37 = unpack2_f32<false>(q[i][3]);
+                P = fmaf(q04.x, xa.x, P);
+                P = fmaf(q04.y, xa.y, P);
+                P = fmaf(q15.x, xa.z, P);
+                P = fmaf(q15.y, xa.w, P);
+                P = fmaf(q26.x, xc.x, P);
+                P = fmaf(q26.y, xc.y, P);
+                P = fmaf(q37.x, xc.z, P);
+                P = fmaf(q37.y, xc.w, P);
             }
             acc[m] = fmaf(P, s, acc[m]);
         }
@@ -337,7 +360,8 @@ struct PolicyW4A8 {
     }
     __device__ __forceinline__ static void load(Chunk& ch, const RowRef& r, int c, int gk, int cpg) {
         ch.w = ld_stream16(r.w + (size_t)c * 16);
-        ch.s = ld_stream_u16(static_cast<const uint16_t*>(r.scale) + (size_t)r.local * gk + c / cpg);
+        ch.s = ld_stream_u16(static_cast<const uint16_t*>(r.scale) + (size_t)r.local * gk +
+                             group_of_chunk(c, cpg));
     }
     template <int MT>
     __device__ __forceinline__ static void mac(Acc (&acc)[MT], const Chunk& ch,
@@ -378,10 +402,10 @@ struct PolicyW4A8 {
 
 // ---- the row-group computation shared by all kernels ------------------------------
 
-// Chunks in flight per lane and row, by the number of accumulators.
+// Chunks per row loaded ahead of use: about eight loads in flight per lane.
 template <int MT, int R>
 struct Unroll {
-    static constexpr int v = (MT * R <= 2) ? 8 : (MT * R <= 8 ? 4 : 2);
+    static constexpr int v = (MT * R <= 1) ? 8 : (MT * R <= 2 ? 4 : 2);
 };
 
 // Geometry of one launch or phase, uniform over the CTA.
@@ -417,8 +441,9 @@ __device__ __forceinline__ void rows_of(const SegTable& t, int rg, bool active, 
 }
 
 // Streams R rows for this lane and returns the per-row sums, complete in every
-// lane of the slot's first warp (kw == 0).  Every thread of the CTA must call
-// it (ks > 1 meets at CTA barriers); inactive slots pass active = false.
+// lane of the slot's first warp (kw == 0).  With ks > 1 the slot's warps meet
+// at named barrier 1 + slot, so all of them must call it; inactive slots pass
+// active = false.
 template <class P, int MT, int R>
 __device__ __forceinline__ void row_group(const RowRef (&rows)[R], bool active, const RowGeom& g,
                                           const unsigned char* xs, int* red,
@@ -465,7 +490,9 @@ __device__ __forceinline__ void row_group(const RowRef (&rows)[R], bool active, 
 #pragma unroll
                 for (int m = 0; m < MT; ++m) red[(warp * R + r) * MT + m] = to_bits(acc[r][m]);
         }
-        __syncthreads();
+        // only the slot's warps meet (named barrier 1 + slot, ks warps)
+        const int bar = 1 + warp / ks;
+        asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(ks * 32) : "memory");
         if (kw == 0) {
             for (int j = 1; j < ks; ++j) {
 #pragma unroll
@@ -475,7 +502,7 @@ __device__ __forceinline__ void row_group(const RowRef (&rows)[R], bool active, 
                         acc[r][m] += from_bits<Acc>(red[((warp + j) * R + r) * MT + m]);
             }
         }
-        __syncthreads();
+        asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(ks * 32) : "memory");
     }
 }
 

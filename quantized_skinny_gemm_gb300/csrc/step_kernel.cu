@@ -20,7 +20,11 @@
 
 namespace dg {
 
-constexpr int kStepR = 1;  // rows per slot (M = 1)
+// Rows per slot (M = 1): int4 rows are short, so two per warp keep enough
+// loads in flight.
+template <class P>
+struct StepRows { static constexpr int v = P::kElems == 32 ? 2 : 1; };
+constexpr int kStepRMax = 2;
 
 // Warps per CTA (one CTA per SM): the default for each format, or 16.
 template <class P>
@@ -30,9 +34,9 @@ struct StepCfg<PolicyFP<B>> { static constexpr int kWarps = 24; };
 template <>
 struct StepCfg<PolicyI8> { static constexpr int kWarps = 24; };
 template <>
-struct StepCfg<PolicyW4A16> { static constexpr int kWarps = 24; };
+struct StepCfg<PolicyW4A16> { static constexpr int kWarps = 16; };
 template <>
-struct StepCfg<PolicyW4A8> { static constexpr int kWarps = 24; };
+struct StepCfg<PolicyW4A8> { static constexpr int kWarps = 16; };
 
 // Row r (global over the phase's segments) of phase ph.
 __device__ __forceinline__ RowRef locate_step(const StepPhase& ph, int r, size_t rb) {
@@ -159,7 +163,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     k_step(const __grid_constant__ StepParams sp, int max_k) {
     extern __shared__ __align__(16) unsigned char smem[];
     using Acc = typename P::Acc;
-    constexpr int R = kStepR;
+    constexpr int R = StepRows<P>::v;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int G = gridDim.x, b = blockIdx.x;
 
@@ -169,7 +173,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     unsigned char* rawx[2] = {smem + step_smem_layout_x<P>(max_k),
                               smem + step_smem_layout_x<P>(max_k) + raw_bytes};
     int* red = reinterpret_cast<int*>(rawx[1] + raw_bytes);
-    ArgPart* cta_best = reinterpret_cast<ArgPart*>(red + NW * R);
+    ArgPart* cta_best = reinterpret_cast<ArgPart*>(red + NW * kStepRMax);
     float* fred = reinterpret_cast<float*>(cta_best + NW);
     float* sx_smem = fred + NW;
     int8_t* qraw = reinterpret_cast<int8_t*>(sx_smem + 4);
@@ -234,13 +238,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 sx = __ldg(ph.x_scale);
             }
         }
-        // fp16 / bf16 activations are used as copied; the int formats restage
-        unsigned char* xs = raw;
-        if constexpr (P::kIntAct || P::kElems == 32) {
-            xs = xs_fmt;
-            P::stage_x(a, xs, 1);
-            __syncthreads();
-        }
+        unsigned char* xs = xs_fmt;
+        P::stage_x(a, xs, 1);
+        __syncthreads();
 
         const int ks = ph.ks;
         const int slots = NW / ks;
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 sp.part[b].i = bi;
             }
         }
-        __syncthreads();  // shared activations are restaged by the next phase
+        // (the next phase's first barrier orders its restaging after this phase)
     }
 
     if (sp.ph[sp.nphase - 1].flags & kPhaseHead) {
@@ -342,7 +342,7 @@ template <class P>
 size_t step_smem_for(int max_k) {
     constexpr int NW = 32;  // the largest CTA any format uses
     const size_t raw_bytes = ((size_t)max_k * 2 + 15) & ~(size_t)15;
-    return step_smem_layout_x<P>(max_k) + 2 * raw_bytes + (size_t)NW * kStepR * 4 +
+    return step_smem_layout_x<P>(max_k) + 2 * raw_bytes + (size_t)NW * kStepRMax * 4 +
            (size_t)NW * sizeof(ArgPart) + (size_t)NW * 4 + 16 + (size_t)max_k + 16;
 }
 
@@ -374,7 +374,7 @@ cudaError_t step_run_nw(const StepParams* sp, int grid, size_t smem, cudaStream_
 template <class P>
 cudaError_t step_run(const StepParams* sp, int grid, size_t smem, cudaStream_t s, int* occ,
                      int max_k, int nw) {
-    if (nw == 16) return step_run_nw<P, 16>(sp, grid, smem, s, occ, max_k);
+    if (nw == 16 || StepCfg<P>::kWarps == 16) return step_run_nw<P, 16>(sp, grid, smem, s, occ, max_k);
     return step_run_nw<P, StepCfg<P>::kWarps>(sp, grid, smem, s, occ, max_k);
 }
 
