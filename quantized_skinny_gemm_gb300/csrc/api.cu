@@ -66,13 +66,13 @@ int* device_error_word() {
 }
 
 // ---- tuning knobs ------------------------------------------------------------------
-// DG_TUNE="R=2,KS=1,CPS=4,PF=32768,PDL=1,STEP=1,SPIN=20000000,SNW=16"
+// DG_TUNE="R=2,KS=1,CPS=4,PF=32768,PDL=1,STEP=1,SPIN=20000000,SNW=16,MMA=1"
 // overrides the launch heuristic (for configuration sweeps); an unset key
 // keeps the heuristic's choice.  STEP=0 runs decode steps as one launch per
 // fused group instead of the persistent step kernel; STEP=2 puts a grid
 // barrier between every pair of phases of the persistent kernel.
 struct Tune {
-    int R = 0, KS = 0, CPS = 0, PF = -1, PDL = -1, STEP = -1, SPIN = -1, SNW = 0;
+    int R = 0, KS = 0, CPS = 0, PF = -1, PDL = -1, STEP = -1, SPIN = -1, SNW = 0, MMA = -1;
 };
 
 static Tune read_tune() {
@@ -92,6 +92,7 @@ static Tune read_tune() {
         else if (std::sscanf(tok, "STEP=%d", &v) == 1) t.STEP = v;
         else if (std::sscanf(tok, "SPIN=%d", &v) == 1) t.SPIN = v;
         else if (std::sscanf(tok, "SNW=%d", &v) == 1) t.SNW = v;
+        else if (std::sscanf(tok, "MMA=%d", &v) == 1) t.MMA = v;
     }
     return t;
 }
@@ -288,6 +289,35 @@ static void fill_common(GemvParams& p, const dg_linear& op) {
     p.a.x_scale = op.x_scale;
 }
 
+// Whether W8A8 with this many tokens runs on the tensor-core kernel.
+static bool use_i8_mma(const dg_linear& op) {
+    if (op.kind != DG_LINEAR_W8A8 || op.M < 8 || op.K % 64 || tune().MMA == 0) return false;
+    return gemv_i8_mma_smem(op.K) <= smem_optin_limit();
+}
+
+static dg_status launch_i8_mma(GemvParams& p, cudaStream_t s) {
+    static std::mutex mu;
+    static std::map<std::pair<int, int>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int occ = 0;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = cache.find({dev, p.a.K});
+        if (it != cache.end()) occ = it->second;
+    }
+    if (!occ) {
+        if (gemv_i8_mma(nullptr, p.a.K, 0, nullptr, &occ) != cudaSuccess || occ < 1) occ = 1;
+        std::lock_guard<std::mutex> g(mu);
+        cache[{dev, p.a.K}] = occ;
+    }
+    const int tiles = (p.t.N + 15) / 16;
+    const int need = (tiles + kWarps - 1) / kWarps;
+    int maxg = sm_count() * occ;
+    if (maxg < 1) maxg = 1;
+    return to_status(gemv_i8_mma(&p, p.a.K, need < maxg ? need : maxg, s, nullptr));
+}
+
 // Launches ops[0..n) (same kind, same activations) as one kernel.
 static dg_status launch_group(const dg_linear* ops, int n, cudaStream_t s) {
     GemvParams p;
@@ -305,6 +335,7 @@ static dg_status launch_group(const dg_linear* ops, int n, cudaStream_t s) {
     }
     p.t.nseg = n;
     p.t.N = rows;
+    if (use_i8_mma(ops[0])) return launch_i8_mma(p, s);
     GemvLaunch L{fmt_of(ops[0].kind), pick_mt(ops[0].M), 0, false, ops[0].K, p.group, 0};
     L.R = pick_r(L.fmt, L.MT);
     configure(L, p);
@@ -430,6 +461,7 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
         std::memset(&sp, 0, sizeof sp);
         int max_k = 0;
         std::vector<Range> seen_rd, seen_wr;  // since the last barrier
+        std::vector<Range> all_wr;            // the whole launch so far
         bool after_head = false;
         while (i < n && sp.nphase < kMaxStepPhases) {
             const dg_linear& a = ops[i];
@@ -445,8 +477,10 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
                 seen_wr.clear();
                 sp.ph[sp.nphase].flags |= kPhaseBarrier;
             }
+            if (any_overlap(all_wr, rd)) sp.ph[sp.nphase].flags |= kPhaseXWritten;
             seen_rd.insert(seen_rd.end(), rd.begin(), rd.end());
             seen_wr.insert(seen_wr.end(), wr.begin(), wr.end());
+            all_wr.insert(all_wr.end(), wr.begin(), wr.end());
             after_head = a.token != nullptr;
             StepPhase& ph = sp.ph[sp.nphase++];
             int rows = 0;

@@ -65,7 +65,7 @@ struct GemvParams {
 
 constexpr int kMaxStepPhases = 144;   // phases per launch (kernel parameter space)
 
-enum StepFlags : int { kPhaseHead = 1, kPhaseQuantize = 2, kPhaseBarrier = 4 };
+enum StepFlags : int { kPhaseHead = 1, kPhaseQuantize = 2, kPhaseBarrier = 4, kPhaseXWritten = 8 };
 
 struct StepSeg {
     const void* W;
@@ -116,6 +116,23 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
 // Hint L2 to fetch the 128-byte line holding p.
 __device__ __forceinline__ void prefetch_line_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Activation loads: through the read-only path (L1-cached), or L2 only for
+// data written earlier in the same kernel (L1 is not kept coherent).
+__device__ __forceinline__ uint4 ld_nc16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint4 ld_cg16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
 }
 
 __device__ __forceinline__ uint16_t ld_stream_u16(const void* p) {
@@ -245,6 +262,9 @@ cudaError_t gemv_i8(const GemvLaunch& L, const GemvParams* p, cudaStream_t s, in
 cudaError_t gemv_w4a16(const GemvLaunch& L, const GemvParams* p, cudaStream_t s, int* occ);
 cudaError_t gemv_w4a8(const GemvLaunch& L, const GemvParams* p, cudaStream_t s, int* occ);
 size_t gemv_smem(Fmt f, int MT, int K, int group);
+// W8A8 for 8..16 tokens on the tensor cores (mma.sync s8, exact int32).
+cudaError_t gemv_i8_mma(const GemvParams* p, int K, int grid, cudaStream_t s, int* occ);
+size_t gemv_i8_mma_smem(int K);
 
 // Host helpers of api.cu shared with the static-scratch lm_head entry point.
 dg_status validate(const dg_linear& op, bool allow_quant_input);

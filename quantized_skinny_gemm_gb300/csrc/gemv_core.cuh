@@ -84,55 +84,64 @@ __device__ __forceinline__ float2 unpack2_f32(uint32_t w) {
     return __half22float2(u32_as_h2(w));
 }
 
-// fp16 / bf16 weights and activations; 8 elements per chunk.  Activations are
-// staged as fp32 (exact), so each weight pair costs one packed conversion and
-// two fp32 FMAs: the product of two 11-bit (8-bit) significands is exact in
-// fp32 and each FMA rounds once, in ascending k.
+// fp16 / bf16 weights and activations; 8 elements per chunk.  Each product
+// of two 11-bit (8-bit) significands is exact in fp32 and one FMA with fp32
+// accumulation rounds once, in ascending k.  With one token the activations
+// are read straight from global memory (16 bytes per chunk, L1-cached: every
+// warp of an SM reads the same vector); with more tokens they are staged in
+// shared memory.
 template <bool BF16>
 struct PolicyFP {
     static constexpr int kElems = 8;
     static constexpr bool kIntAct = false;
+    static constexpr bool kDirectX = true;  // M = 1 reads x from global memory
     using Acc = float;
     struct Chunk { uint4 w; };
 
     __host__ __device__ static size_t row_bytes(int K) { return (size_t)K * 2; }
-    __host__ __device__ static size_t x_bytes(int MT, int K) { return (size_t)MT * K * 4; }
+    __host__ __device__ static size_t x_bytes(int MT, int K) { return (size_t)MT * K * 2; }
 
     __device__ static void stage_x(const ActIn& a, unsigned char* xs, int MT) {
         const int per_row = a.K / 8;
         const uint4* src = static_cast<const uint4*>(a.x);
-        float4* dst = reinterpret_cast<float4*>(xs);
+        uint4* dst = reinterpret_cast<uint4*>(xs);
         for (int i = threadIdx.x; i < MT * per_row; i += blockDim.x) {
             const int m = i / per_row;
-            const uint4 v = m < a.M ? src[i] : make_uint4(0, 0, 0, 0);
-            const float2 f0 = unpack2_f32<BF16>(v.x), f1 = unpack2_f32<BF16>(v.y);
-            const float2 f2 = unpack2_f32<BF16>(v.z), f3 = unpack2_f32<BF16>(v.w);
-            dst[2 * i] = make_float4(f0.x, f0.y, f1.x, f1.y);
-            dst[2 * i + 1] = make_float4(f2.x, f2.y, f3.x, f3.y);
+            dst[i] = m < a.M ? src[i] : make_uint4(0, 0, 0, 0);
         }
     }
     __device__ __forceinline__ static void load(Chunk& ch, const RowRef& r, int c, int, int) {
         ch.w = ld_stream16(r.w + (size_t)c * 16);
     }
-    __device__ __forceinline__ static float mac2(uint32_t w, float x0, float x1, float a) {
-        const float2 f = unpack2_f32<BF16>(w);
-        a = fmaf(f.x, x0, a);
-        return fmaf(f.y, x1, a);
+    __device__ __forceinline__ static float mac2(uint32_t w, uint32_t x, float a) {
+        if (BF16) {
+            a = fma_bf16(lo16(w), lo16(x), a);
+            return fma_bf16(hi16(w), hi16(x), a);
+        }
+        a = fma_f16(lo16(w), lo16(x), a);
+        return fma_f16(hi16(w), hi16(x), a);
+    }
+    __device__ __forceinline__ static float mac8(const uint4& w, const uint4& xv, float a) {
+        a = mac2(w.x, xv.x, a);
+        a = mac2(w.y, xv.y, a);
+        a = mac2(w.z, xv.z, a);
+        return mac2(w.w, xv.w, a);
     }
     template <int MT>
     __device__ __forceinline__ static void mac(Acc (&acc)[MT], const Chunk& ch,
                                                const unsigned char* xs, int c, int K) {
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            const float4* xv = reinterpret_cast<const float4*>(xs + ((size_t)m * K + (size_t)c * 8) * 4);
-            const float4 x0 = xv[0], x1 = xv[1];
-            float a = acc[m];
-            a = mac2(ch.w.x, x0.x, x0.y, a);
-            a = mac2(ch.w.y, x0.z, x0.w, a);
-            a = mac2(ch.w.z, x1.x, x1.y, a);
-            a = mac2(ch.w.w, x1.z, x1.w, a);
-            acc[m] = a;
-        }
+        for (int m = 0; m < MT; ++m)
+            acc[m] = mac8(ch.w, *reinterpret_cast<const uint4*>(xs + ((size_t)m * K + (size_t)c * 8) * 2),
+                          acc[m]);
+    }
+    // One token, activations in global memory; `coherent` bypasses L1 (for an
+    // x written earlier in the same launch).
+    __device__ __forceinline__ static void mac_direct(Acc (&acc)[1], const Chunk& ch, const void* x,
+                                                      int c, bool coherent) {
+        const unsigned char* p = static_cast<const unsigned char*>(x) + (size_t)c * 16;
+        const uint4 xv = coherent ? ld_cg16(p) : ld_nc16(p);
+        acc[0] = mac8(ch.w, xv, acc[0]);
     }
     __device__ static float finish(const RowRef&, Acc a, float) { return a; }
     __device__ static void store(const RowRef& r, int m, Acc a, float) {
@@ -148,6 +157,7 @@ struct PolicyFP {
 struct PolicyI8 {
     static constexpr int kElems = 16;
     static constexpr bool kIntAct = true;
+    static constexpr bool kDirectX = false;
     using Acc = int;
     struct Chunk { uint4 w; };
 
@@ -236,6 +246,7 @@ __device__ __forceinline__ size_t int4_x_piece(int c, int i, int pieces) {
 struct PolicyW4A16 {
     static constexpr int kElems = 32;
     static constexpr bool kIntAct = false;
+    static constexpr bool kDirectX = false;
     using Acc = float;
     struct Chunk { uint4 w; uint16_t s; };
 
@@ -314,6 +325,7 @@ struct PolicyW4A16 {
 struct PolicyW4A8 {
     static constexpr int kElems = 32;
     static constexpr bool kIntAct = true;
+    static constexpr bool kDirectX = false;
     using Acc = float;
     struct Chunk { uint4 w; uint16_t s; };
 
@@ -444,10 +456,12 @@ __device__ __forceinline__ void rows_of(const SegTable& t, int rg, bool active, 
 // lane of the slot's first warp (kw == 0).  With ks > 1 the slot's warps meet
 // at named barrier 1 + slot, so all of them must call it; inactive slots pass
 // active = false.
-template <class P, int MT, int R>
+// DX: one token, activations read from global memory at `xs` (coherent:
+// bypassing L1); otherwise `xs` is the staged shared-memory copy.
+template <class P, int MT, int R, bool DX = false>
 __device__ __forceinline__ void row_group(const RowRef (&rows)[R], bool active, const RowGeom& g,
                                           const unsigned char* xs, int* red,
-                                          typename P::Acc (&acc)[R][MT]) {
+                                          typename P::Acc (&acc)[R][MT], bool coherent = false) {
     using Acc = typename P::Acc;
     constexpr int U = Unroll<MT, R>::v;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -474,8 +488,12 @@ __device__ __forceinline__ void row_group(const RowRef (&rows)[R], bool active, 
             for (int u = 0; u < U; ++u)
                 if (c + u * step < g.nchunks)
 #pragma unroll
-                    for (int r = 0; r < R; ++r)
-                        P::template mac<MT>(acc[r], ch[u][r], xs, c + u * step, g.K);
+                    for (int r = 0; r < R; ++r) {
+                        if constexpr (DX)
+                            P::mac_direct(acc[r], ch[u][r], xs, c + u * step, coherent);
+                        else
+                            P::template mac<MT>(acc[r], ch[u][r], xs, c + u * step, g.K);
+                    }
         }
     }
 #pragma unroll
@@ -536,9 +554,13 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvP
     griddep_launch_dependents();
     griddep_wait();
 
-    P::stage_x(p.a, smem, MT);
-    __syncthreads();
-    int* red = reinterpret_cast<int*>(smem + ((P::x_bytes(MT, g.K) + 15) & ~(size_t)15));
+    constexpr bool DX = P::kDirectX && MT == 1;
+    if constexpr (!DX) {
+        P::stage_x(p.a, smem, MT);
+        __syncthreads();
+    }
+    int* red = reinterpret_cast<int*>(smem + (DX ? 0 : ((P::x_bytes(MT, g.K) + 15) & ~(size_t)15)));
+    const unsigned char* xsrc = DX ? static_cast<const unsigned char*>(p.a.x) : smem;
 
     float best_v = NAN;
     int best_i = INT_MAX;
@@ -549,7 +571,7 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvP
         RowRef rows[R];
         rows_of<R>(p.t, rg, active, g.rb, rows);
         Acc acc[R][MT];
-        row_group<P, MT, R>(rows, active, g, smem, red, acc);
+        row_group<P, MT, R, DX>(rows, active, g, xsrc, red, acc);
 
         if (kw == 0 && active) {
 #pragma unroll
@@ -600,7 +622,8 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvP
 
 template <class P>
 size_t smem_bytes_for(int MT, int K) {
-    size_t x = (P::x_bytes(MT, K) + 15) & ~(size_t)15;
+    const bool direct = P::kDirectX && MT == 1;
+    size_t x = direct ? 0 : (P::x_bytes(MT, K) + 15) & ~(size_t)15;
     return x + (size_t)kWarps * 4 * MT * 4 + (size_t)kWarps * sizeof(ArgPart);
 }
 

@@ -207,40 +207,49 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 if (lane == 0) *sp.ph[p - 1].token = bi == INT_MAX ? -1 : bi;
             }
         }
-        // activations of this phase: raw bytes in rawx[p & 1] (copied ahead
-        // during the previous phase when no barrier separates them)
-        unsigned char* raw = rawx[p & 1];
-        if (!staged_ahead) async_copy_block(raw, raw_act_src<P>(ph), raw_act_bytes<P>(ph));
-        async_wait_all();
-        __syncthreads();
-        staged_ahead = false;
-        if (p + 1 < sp.nphase && !(sp.ph[p + 1].flags & kPhaseBarrier)) {
-            const StepPhase& nx = sp.ph[p + 1];
-            async_copy_block(rawx[(p + 1) & 1], raw_act_src<P>(nx), raw_act_bytes<P>(nx));
-            staged_ahead = true;
-        }
         float sx = 1.f;
-        ActIn a{raw, reinterpret_cast<const int8_t*>(raw), ph.x_scale, ph.K, 1};
-        if constexpr (P::kIntAct) {
-            if (ph.flags & kPhaseQuantize) {
-                const float s = quantize_token_smem(reinterpret_cast<const __half*>(raw), ph.K, qraw, fred);
-                __syncthreads();
-                if (b == 0) {  // the documented side outputs of the fused quantization
-                    if (ph.xq_out)
-                        for (int k = threadIdx.x * 16; k < ph.K; k += blockDim.x * 16)
-                            *reinterpret_cast<uint4*>(ph.xq_out + k) =
-                                *reinterpret_cast<const uint4*>(qraw + k);
-                    if (threadIdx.x == 0 && ph.x_scale) ph.x_scale[0] = s;
-                }
-                a.xq = qraw;
-                sx = s;
-            } else {
-                sx = __ldg(ph.x_scale);
-            }
-        }
         unsigned char* xs = xs_fmt;
-        P::stage_x(a, xs, 1);
-        __syncthreads();
+        if constexpr (!P::kDirectX) {
+            // activations of this phase: raw bytes in rawx[p & 1] (copied ahead
+            // during the previous phase when no barrier separates them), then
+            // restaged in the format's layout
+            unsigned char* raw = rawx[p & 1];
+            if (!staged_ahead) async_copy_block(raw, raw_act_src<P>(ph), raw_act_bytes<P>(ph));
+            async_wait_all();
+            __syncthreads();
+            staged_ahead = false;
+            if (p + 1 < sp.nphase && !(sp.ph[p + 1].flags & kPhaseBarrier)) {
+                const StepPhase& nx = sp.ph[p + 1];
+                async_copy_block(rawx[(p + 1) & 1], raw_act_src<P>(nx), raw_act_bytes<P>(nx));
+                staged_ahead = true;
+            }
+            ActIn a{raw, reinterpret_cast<const int8_t*>(raw), ph.x_scale, ph.K, 1};
+            if constexpr (P::kIntAct) {
+                if (ph.flags & kPhaseQuantize) {
+                    const float s = quantize_token_smem(reinterpret_cast<const __half*>(raw), ph.K,
+                                                        qraw, fred);
+                    __syncthreads();
+                    if (b == 0) {  // the documented side outputs of the fused quantization
+                        if (ph.xq_out)
+                            for (int k = threadIdx.x * 16; k < ph.K; k += blockDim.x * 16)
+                                *reinterpret_cast<uint4*>(ph.xq_out + k) =
+                                    *reinterpret_cast<const uint4*>(qraw + k);
+                        if (threadIdx.x == 0 && ph.x_scale) ph.x_scale[0] = s;
+                    }
+                    a.xq = qraw;
+                    sx = s;
+                } else {
+                    sx = __ldg(ph.x_scale);
+                }
+            }
+            P::stage_x(a, xs, 1);
+            __syncthreads();
+        } else {
+            // one token read from global memory in the MACs: no staging and no
+            // CTA-wide meeting between phases
+            xs = static_cast<unsigned char*>(const_cast<void*>(ph.x));
+        }
+        const bool coherent = (ph.flags & kPhaseXWritten) != 0;
 
         const int ks = ph.ks;
         const int slots = NW / ks;
@@ -272,7 +281,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 }
             }
             Acc acc[R][1];
-            row_group<P, 1, R>(rows, active, g, xs, red, acc);
+            row_group<P, 1, R, P::kDirectX>(rows, active, g, xs, red, acc, coherent);
             if (kw == 0 && active) {
 #pragma unroll
                 for (int r = 0; r < R; ++r) {

@@ -89,3 +89,31 @@ def test_quant_act_edge_tokens():
     assert np.array_equal(xq.cpu().numpy(), q_ref)
     assert np.array_equal(xs.cpu().numpy(), s_ref)
     assert float(xs[0]) == 1.0 and int(xq[0].abs().max()) == 0
+
+
+@pytest.mark.parametrize("N,K,M", [(37, 64, 9), (100, 128, 16), (16, 4096, 12), (4111, 4096, 16),
+                                   (257, 192, 8), (1, 4096, 16)])
+def test_tensor_core_tile_for_8_to_16_tokens(N, K, M):
+    """8..16 tokens with K a multiple of 64 run on the mma.sync s8 kernel:
+    int32 accumulators still bit-exact."""
+    need_gpu()
+    W, s_w, x = synth.w8_case(N, K, M, seed=N + K + 100 * M)
+    xq, xs = quant_gpu(x)
+    y, acc = run_w8(W, s_w, xq, xs)
+    q_ref, s_ref = oracle.quant_act(bits(x))
+    acc_ref, y_ref, A = oracle.gemv_w8a8(W.numpy(), s_w.numpy(), q_ref, s_ref)
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), acc_ref)
+    tol.assert_close(y.cpu().double().numpy(), y_ref, A, "f16", "w8a8 mma %dx%d M=%d" % (N, K, M))
+
+
+def test_tensor_core_tile_extreme_codes_exact():
+    need_gpu()
+    K = 4096
+    W = torch.full((32, K), 127, dtype=torch.int8)
+    W[1::2] = -127
+    xq = torch.full((16, K), -127, dtype=torch.int8, device=DEV)
+    xq[::3] = 127
+    xs = torch.full((16,), 1e-3, dtype=torch.float32, device=DEV)
+    y, acc = run_w8(W, torch.full((32,), 1e-3), xq, xs)
+    ref = xq.cpu().long() @ W.long().T
+    assert torch.equal(acc.cpu().long(), ref)
