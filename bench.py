@@ -74,6 +74,49 @@ def recorded_traffic(kernel):
     return e.get("bytes_per_launch")
 
 
+def floor_seconds(bytes_per_unit, gbs):
+    """Bandwidth floor: the time to move `bytes_per_unit` at `gbs` GB/s (the
+    weight-read roofline of the Orange Pi AIPro post's closing paragraph)."""
+    return bytes_per_unit / (gbs * 1e9)
+
+
+def job_throughput_gbs(unit_bytes, steps, world, secs):
+    """Whole-job weight bytes per second over all ranks, in GB/s."""
+    return unit_bytes * steps * world / secs / 1e9
+
+
+def max_over_ranks(secs, dist, device):
+    """The slowest rank's time (every rank gets it)."""
+    import torch
+    t = torch.tensor([float(secs)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+CLOCK_REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+def parse_clock_samples(text):
+    """nvidia-smi csv rows (sm, max sm, power, 4 throttle reasons) ->
+    {sm_mhz: median, sm_max_mhz, samples, reasons: [active ones]}."""
+    sm, smax, reasons = [], [], set()
+    for line in text.strip().splitlines():
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 7:
+            continue
+        try:
+            sm.append(float(f[0]))
+            smax.append(float(f[1]))
+        except ValueError:
+            continue
+        for n, v in zip(CLOCK_REASONS, f[3:7]):
+            if v.lower() == "active":
+                reasons.add(n)
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "samples": len(sm), "reasons": sorted(reasons)}
+
+
 class ClockSampler:
     """nvidia-smi samples every 200 ms while running."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
@@ -99,23 +142,7 @@ class ClockSampler:
         time.sleep(0.25)
         self.p.terminate()
         out, _ = self.p.communicate(timeout=10)
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 7:
-                continue
-            try:
-                sm.append(float(f[0]))
-                smax.append(float(f[1]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[3:7]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+        return parse_clock_samples(out)
 
 
 # ---- workloads ----------------------------------------------------------------
@@ -149,14 +176,9 @@ def build_workload(name, dev, torch):
                                 "(Qwen2.5-1.5B shape), 196 matrices, M=1",
                     "weight_bytes_per_step": st.weight_bytes,
                     "l2": "inputs 2.62 GB > 126 MB L2 (no flush)"}
-        # dominant kernel: the fused gate|up launch of every layer
-        ops = [dg.Linear.from_buffer_copy(op) for op in st.plan.array
-               if op.N == 8960 and op.K == 1536]
-        dplan = plans.StepPlan(ops, [])
-        dws = torch.empty(dplan.workspace_bytes(), dtype=torch.uint8, device=dev)
-        w.dominant = ("gate|up 17920x1536 fp16",
-                      lambda: dg.decode_step_weights(dplan, dws, stream=s), len(ops) // 2,
-                      2 * 8960 * 1536 * 2)
+        # the step runs as one persistent kernel launch: that launch dominates
+        w.dominant = ("k_step<fp16> (persistent decode-step kernel, 28 layers)", w.run, 1,
+                      st.weight_bytes)
         w.cpu_sample = ("fp", layers)
         w.dtype = "f16"
     elif name in ("decode_int4_a16", "decode_int4_a8"):
@@ -173,16 +195,8 @@ def build_workload(name, dev, torch):
                                 % act[1:].upper(),
                     "weight_bytes_per_step": st.weight_bytes,
                     "l2": "inputs 4.22 GB > 126 MB L2 (no flush)"}
-        ops = [dg.Linear.from_buffer_copy(op) for op in st.plan.array
-               if op.N == 14336 and op.K == 4096 and not op.token]
-        if act == "a8":
-            for op in ops:
-                op.x = None  # codes already quantized by the step; time the GEMV alone
-        dplan = plans.StepPlan(ops, [])
-        dws = torch.empty(dplan.workspace_bytes(), dtype=torch.uint8, device=dev)
-        w.dominant = ("gate|up 28672x4096 int4",
-                      lambda: dg.decode_step_weights(dplan, dws, stream=s), len(ops) // 2,
-                      2 * 14336 * 4096 // 2 + 2 * 14336 * (4096 // 32) * 2)
+        w.dominant = ("k_step<int4 %s> (persistent decode-step kernel, 32 layers + lm_head)"
+                      % act, w.run, 1, st.weight_bytes)
         w.cpu_sample = ("w4" + act, (layers, head, xh))
         w.dtype = "int4xf16" if act == "a16" else "int4xi8"
     elif name == "lm_head":
@@ -485,9 +499,7 @@ def main():
     secs = time_graph(g, s, args.steps, torch)
     torch.cuda.synchronize()
     if dist:
-        t = torch.tensor([secs], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        secs = float(t.item())
+        secs = max_over_ranks(secs, dist, dev)
         dist.barrier()
 
     if args.quick:
@@ -509,8 +521,7 @@ def main():
     # end to end through the public API with host buffers
     e2e = measure_e2e(w, args, torch, dg, g)
 
-    units = args.steps * world
-    value = w.unit_bytes * units / secs / 1e9
+    value = job_throughput_gbs(w.unit_bytes, args.steps, world, secs)
     out = {
         "metric": "decode weight-stream GB/s",
         "value": round(value, 1),

@@ -311,8 +311,17 @@ static dg_status launch_i8_mma(GemvParams& p, cudaStream_t s) {
         std::lock_guard<std::mutex> g(mu);
         cache[{dev, p.a.K}] = occ;
     }
+    // split K over ks warps per 16-row tile (ks | K / 64) until the GPU has
+    // about four warps per SM sub-partition to stream with
     const int tiles = (p.t.N + 15) / 16;
-    const int need = (tiles + kWarps - 1) / kWarps;
+    const int nblk = p.a.K / 64;
+    int ks = 1;
+    while (ks < 8 && nblk % (2 * ks) == 0 && nblk / (2 * ks) >= 4 &&
+           tiles * ks < sm_count() * 16)
+        ks *= 2;
+    p.ksplit = ks;
+    const int per_cta = kWarps / ks;
+    const int need = (tiles + per_cta - 1) / per_cta;
     int maxg = sm_count() * occ;
     if (maxg < 1) maxg = 1;
     return to_status(gemv_i8_mma(&p, p.a.K, need < maxg ? need : maxg, s, nullptr));

@@ -31,13 +31,18 @@ __device__ __forceinline__ void mma_s8_16816_32(int (&d)[4], uint32_t a0, uint32
 
 constexpr int kMmaUnroll = 4;  // 64-wide k blocks loaded ahead
 
-// p.a.xq: int8 [M][K], M <= 16; K a multiple of 64.  Grid-stride over 16-row
-// tiles, 8 warps per CTA.
+// p.a.xq: int8 [M][K], M <= 16; K a multiple of 64 * ks.  A CTA's 8 warps
+// take 8 / ks tiles, ks warps per tile, each warp a contiguous 1/ks of K; the
+// slices' int32 tiles are added in shared memory (exact in any order).
+// Grid-stride over tile groups.
 __global__ void __launch_bounds__(kThreads) k_w8a8_mma(const __grid_constant__ GemvParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int K = p.a.K, M = p.a.M;
+    const int ks = p.ksplit;
+    const int tiles_per_cta = kWarps / ks;
+    const int kw = warp % ks, slot = warp / ks;
 
     griddep_launch_dependents();
     griddep_wait();
@@ -54,23 +59,28 @@ __global__ void __launch_bounds__(kThreads) k_w8a8_mma(const __grid_constant__ G
                 m < M ? src[i] : make_uint4(0, 0, 0, 0);
         }
     }
+    int* part = reinterpret_cast<int*>(smem + (size_t)16 * xstride);  // [warp][8][32]
     __syncthreads();
 
     const int n_tiles = (p.t.N + 15) / 16;
-    const int nblk = K / 64;
-    for (int tile = blockIdx.x * kWarps + warp; tile < n_tiles; tile += gridDim.x * kWarps) {
-        const int r0 = tile * 16;
+    const int nblk = K / 64 / ks;  // 64-wide k blocks per warp
+    const int groups = (n_tiles + tiles_per_cta - 1) / tiles_per_cta;
+    for (int grp = blockIdx.x; grp < groups; grp += gridDim.x) {
+        const int tile = grp * tiles_per_cta + slot;
+        const bool active = tile < n_tiles;
+        const int r0 = (active ? tile : 0) * 16;
         RowRef z{};
         const RowRef first = locate(p.t, r0, (size_t)K, z);
         RowRef rlo = locate(p.t, r0 + g, (size_t)K, first);
         RowRef rhi = locate(p.t, r0 + g + 8, (size_t)K, first);
-        const unsigned char* wlo = (rlo.valid ? rlo.w : first.w) + 16 * t;
-        const unsigned char* whi = (rhi.valid ? rhi.w : first.w) + 16 * t;
-        const unsigned char* xlo = smem + (size_t)g * xstride + 16 * t;        // token g
-        const unsigned char* xhi = smem + (size_t)(g + 8) * xstride + 16 * t;  // token g + 8
+        const size_t k0 = (size_t)kw * nblk * 64 + 16 * t;
+        const unsigned char* wlo = (rlo.valid ? rlo.w : first.w) + k0;
+        const unsigned char* whi = (rhi.valid ? rhi.w : first.w) + k0;
+        const unsigned char* xlo = smem + (size_t)g * xstride + k0;        // token g
+        const unsigned char* xhi = smem + (size_t)(g + 8) * xstride + k0;  // token g + 8
         int d0[4] = {0, 0, 0, 0}, d1[4] = {0, 0, 0, 0};  // tokens 0..7, 8..15
 
-        for (int kb = 0; kb < nblk; kb += kMmaUnroll) {
+        for (int kb = 0; active && kb < nblk; kb += kMmaUnroll) {
             uint4 alo[kMmaUnroll], ahi[kMmaUnroll];
 #pragma unroll
             for (int u = 0; u < kMmaUnroll; ++u)
@@ -89,6 +99,28 @@ __global__ void __launch_bounds__(kThreads) k_w8a8_mma(const __grid_constant__ G
                     mma_s8_16816_32(d1, alo[u].z, ahi[u].z, alo[u].w, ahi[u].w, bh.z, bh.w);
                 }
         }
+        if (ks > 1) {  // slices 1..ks-1 hand their tiles to slice 0 of the slot
+            int* mine = part + (size_t)warp * 8 * 32;
+            if (kw != 0) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    mine[j * 32 + lane] = d0[j];
+                    mine[(4 + j) * 32 + lane] = d1[j];
+                }
+            }
+            asm volatile("bar.sync %0, %1;" ::"r"(1 + slot), "r"(ks * 32) : "memory");
+            if (kw == 0)
+                for (int w = 1; w < ks; ++w) {
+                    const int* o = part + (size_t)(warp + w) * 8 * 32;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        d0[j] += o[j * 32 + lane];
+                        d1[j] += o[(4 + j) * 32 + lane];
+                    }
+                }
+            asm volatile("bar.sync %0, %1;" ::"r"(1 + slot), "r"(ks * 32) : "memory");
+        }
+        if (kw != 0 || !active) continue;
         // d[0], d[1]: row g, tokens 2t, 2t+1 (+8 for d1); d[2], d[3]: row g + 8
         const int tok[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
         const int val_lo[4] = {d0[0], d0[1], d1[0], d1[1]};
@@ -104,7 +136,7 @@ __global__ void __launch_bounds__(kThreads) k_w8a8_mma(const __grid_constant__ G
     }
 }
 
-size_t gemv_i8_mma_smem(int K) { return (size_t)16 * (K + 64); }
+size_t gemv_i8_mma_smem(int K) { return (size_t)16 * (K + 64) + (size_t)kWarps * 8 * 32 * 4; }
 
 cudaError_t gemv_i8_mma(const GemvParams* p, int K, int grid, cudaStream_t s, int* occ) {
     const size_t smem = gemv_i8_mma_smem(K);
