@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     bool staged_ahead = false;  // this phase's raw activations are already in flight
 
     unsigned nbar = 0;  // grid barriers passed
+    unsigned deal = 0;  // row groups dealt to this CTA's slots so far
 
     for (int p = 0; p < sp.nphase; ++p) {
         const StepPhase& ph = sp.ph[p];
@@ -257,14 +258,19 @@ __global__ void __launch_bounds__(NW * 32, 1)
         const RowGeom g = row_geom<P>(ph.K, sp.group, ks);
         const int r0 = slice_begin(ph.N, b, G), r1 = slice_begin(ph.N, b + 1, G);
         const int n_rg = (r1 - r0 + R - 1) / R;
-        const int iters = (n_rg + slots - 1) / slots;
+        // row groups are dealt round-robin over the whole step (continuing
+        // where the previous phase stopped) so every warp streams a fair share
+        const int lead = (int)(deal % (unsigned)slots);
+        const int mine = (slot - lead + slots) % slots;  // first row group of this slot
+        const int iters = (n_rg - mine + slots - 1) / slots;  // the same in all of the slot's warps
+        deal += (unsigned)n_rg;
         const bool head = (ph.flags & kPhaseHead) != 0;
         float best_v = NAN;
         int best_i = INT_MAX;
 
         for (int it = 0; it < iters; ++it) {
-            const int rg = it * slots + slot;
-            const bool active = rg < n_rg;
+            const int rg = mine + it * slots;
+            const bool active = true;
             RowRef rows[R];
             {
                 const int first = r0 + rg * R;
