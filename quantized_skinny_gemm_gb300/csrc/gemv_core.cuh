@@ -135,13 +135,19 @@ struct PolicyFP {
             acc[m] = mac8(ch.w, *reinterpret_cast<const uint4*>(xs + ((size_t)m * K + (size_t)c * 8) * 2),
                           acc[m]);
     }
-    // One token, activations in global memory; `coherent` bypasses L1 (for an
-    // x written earlier in the same launch).
-    __device__ __forceinline__ static void mac_direct(Acc (&acc)[1], const Chunk& ch, const void* x,
-                                                      int c, bool coherent) {
+    // One token, activations from global memory (loaded with the weights,
+    // see row_group): the chunk's eight products go into two independent
+    // chains of four, merged into the row sum once per chunk.
+    __device__ __forceinline__ static uint4 load_x(const void* x, int c, bool coherent) {
         const unsigned char* p = static_cast<const unsigned char*>(x) + (size_t)c * 16;
-        const uint4 xv = coherent ? ld_cg16(p) : ld_nc16(p);
-        acc[0] = mac8(ch.w, xv, acc[0]);
+        return coherent ? ld_cg16(p) : ld_nc16(p);
+    }
+    __device__ __forceinline__ static void mac_direct(Acc (&acc)[1], const Chunk& ch, const uint4& xv) {
+        float s0 = mac2(ch.w.x, xv.x, 0.f);
+        float s1 = mac2(ch.w.z, xv.z, 0.f);
+        s0 = mac2(ch.w.y, xv.y, s0);
+        s1 = mac2(ch.w.w, xv.w, s1);
+        acc[0] += s0 + s1;
     }
     __device__ static float finish(const RowRef&, Acc a, float) { return a; }
     __device__ static void store(const RowRef& r, int m, Acc a, float) {
@@ -484,16 +490,26 @@ __device__ __forceinline__ void row_group(const RowRef (&rows)[R], bool active, 
                 if (c + u * step < g.nchunks)
 #pragma unroll
                     for (int r = 0; r < R; ++r) P::load(ch[u][r], rows[r], c + u * step, g.gk, g.cpg);
+            if constexpr (DX) {
+                // one activation chunk (an L1 hit, mostly) kept in flight ahead of the MACs
+                uint4 xn = P::load_x(xs, c, coherent);
 #pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (c + u * step < g.nchunks)
+                for (int u = 0; u < U; ++u)
+                    if (c + u * step < g.nchunks) {
+                        const uint4 xv = xn;
+                        if (u + 1 < U && c + (u + 1) * step < g.nchunks)
+                            xn = P::load_x(xs, c + (u + 1) * step, coherent);
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        if constexpr (DX)
-                            P::mac_direct(acc[r], ch[u][r], xs, c + u * step, coherent);
-                        else
-                            P::template mac<MT>(acc[r], ch[u][r], xs, c + u * step, g.K);
+                        for (int r = 0; r < R; ++r) P::mac_direct(acc[r], ch[u][r], xv);
                     }
+            } else {
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (c + u * step < g.nchunks)
+#pragma unroll
+                        for (int r = 0; r < R; ++r)
+                            P::template mac<MT>(acc[r], ch[u][r], xs, c + u * step, g.K);
+            }
         }
     }
 #pragma unroll
