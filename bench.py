@@ -181,20 +181,24 @@ def build_workload(name, dev, torch):
                       st.weight_bytes)
         w.cpu_sample = ("fp", layers)
         w.dtype = "f16"
-    elif name in ("decode_int4_a16", "decode_int4_a8"):
+    elif name in ("decode_int4_a16", "decode_int4_a8", "decode_int4_4l_a16", "decode_int4_4l_a8"):
         act = name[-3:]
-        layers, head, xh = synth.decode_int4_workload(seed=0)
+        small = "_4l_" in name
+        layers, head, xh = (synth.decode_int4_workload(seed=0, layers=4, vocab=0) if small
+                            else synth.decode_int4_workload(seed=0))
         st = plans.int4_decode_step(layers, head, xh, dev, act=act)
         w.host = (layers, head, xh)
         w.in_arena, w.out_arena = st.in_arena, st.out_arena
         w.unit_bytes = st.weight_bytes
         w.launches = st.n_launches
         w.run = lambda: dg.decode_step_weights(st.plan, st.ws, stream=s)
-        w.config = {"workload": "decode-step weight stream, 32-layer 4096-wide int4 g32 decoder "
-                                "(Llama-3.1-8B shape) + 128256-row lm_head with argmax, W4%s, M=1"
+        w.config = {"workload": ("decode-step weight stream, 4 layers of the 4096-wide int4 g32 "
+                                 "decoder, W4%s, M=1" if small else
+                                 "decode-step weight stream, 32-layer 4096-wide int4 g32 decoder "
+                                 "(Llama-3.1-8B shape) + 128256-row lm_head with argmax, W4%s, M=1")
                                 % act[1:].upper(),
                     "weight_bytes_per_step": st.weight_bytes,
-                    "l2": "inputs 4.22 GB > 126 MB L2 (no flush)"}
+                    "l2": "inputs %.2f GB > 126 MB L2 (no flush)" % (st.weight_bytes / 1e9)}
         w.dominant = ("k_step<int4 %s> (persistent decode-step kernel, 32 layers + lm_head)"
                       % act, w.run, 1, st.weight_bytes)
         w.cpu_sample = ("w4" + act, (layers, head, xh))
@@ -448,7 +452,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="dg", choices=["dg", "reference"])
     ap.add_argument("--workload", default="decode_fp16",
-                    choices=["decode_fp16", "decode_int4_a16", "decode_int4_a8", "lm_head",
+                    choices=["decode_fp16", "decode_int4_a16", "decode_int4_a8",
+                             "decode_int4_4l_a16", "decode_int4_4l_a8", "lm_head",
                              "gateup_fp16", "gateup_w4a16", "gateup_w4a8", "decode_fp16_4l",
                              "gemv_f16_2048", "w8a8_m1",
                              "w8a8_m4", "w8a8_m16"])

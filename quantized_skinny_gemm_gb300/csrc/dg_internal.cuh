@@ -5,6 +5,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "../../include/dg.h"
 
@@ -171,6 +172,19 @@ __device__ __forceinline__ float fma_bf16(uint16_t a, uint16_t b, float acc) {
 
 __device__ __forceinline__ uint16_t lo16(uint32_t v) { return (uint16_t)(v & 0xFFFFu); }
 __device__ __forceinline__ uint16_t hi16(uint32_t v) { return (uint16_t)(v >> 16); }
+
+// Two fp32 FMAs in one instruction: acc.{x,y} += a.{x,y} * b.{x,y}, each
+// rounded once.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 acc) {
+    unsigned long long ra, rb, rc;
+    memcpy(&ra, &a, 8);
+    memcpy(&rb, &b, 8);
+    memcpy(&rc, &acc, 8);
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(rc) : "l"(ra), "l"(rb));
+    float2 r;
+    memcpy(&r, &rc, 8);
+    return r;
+}
 
 // Dot products of four byte lanes.
 __device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {

@@ -296,23 +296,18 @@ struct PolicyW4A16 {
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             const unsigned char* xb = xs + m * tb;
-            float P = 0.f;
+            // codes (c_i, c_i+4) against (x_i, x_i+4): two chains, one per half
+            float2 P = make_float2(0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float4 xa = *reinterpret_cast<const float4*>(xb + int4_x_piece(c, 2 * i, 8));
                 const float4 xc = *reinterpret_cast<const float4*>(xb + int4_x_piece(c, 2 * i + 1, 8));
-                const float2 q04 = unpack2_f32<false>(q[i][0]), q15 = unpack2_f32<false>(q[i][1]);
-                const float2 q26 = unpack2_f32<false>(q[i][2]), q37 = unpack2_f32<false>(q[i][3]);
-                P = fmaf(q04.x, xa.x, P);
-                P = fmaf(q04.y, xa.y, P);
-                P = fmaf(q15.x, xa.z, P);
-                P = fmaf(q15.y, xa.w, P);
-                P = fmaf(q26.x, xc.x, P);
-                P = fmaf(q26.y, xc.y, P);
-                P = fmaf(q37.x, xc.z, P);
-                P = fmaf(q37.y, xc.w, P);
+                P = fma2(unpack2_f32<false>(q[i][0]), make_float2(xa.x, xa.y), P);
+                P = fma2(unpack2_f32<false>(q[i][1]), make_float2(xa.z, xa.w), P);
+                P = fma2(unpack2_f32<false>(q[i][2]), make_float2(xc.x, xc.y), P);
+                P = fma2(unpack2_f32<false>(q[i][3]), make_float2(xc.z, xc.w), P);
             }
-            acc[m] = fmaf(P, s, acc[m]);
+            acc[m] = fmaf(P.x + P.y, s, acc[m]);
         }
     }
     __device__ static float finish(const RowRef&, Acc a, float) { return a; }
