@@ -471,6 +471,7 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
         int max_k = 0;
         std::vector<Range> seen_rd, seen_wr;  // since the last barrier
         std::vector<Range> all_wr;            // the whole launch so far
+        std::vector<std::vector<Range>> phase_rd, phase_wr;
         bool after_head = false;
         while (i < n && sp.nphase < kMaxStepPhases) {
             const dg_linear& a = ops[i];
@@ -510,9 +511,11 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
             ph.xq = a.x_i8;
             ph.x_scale = const_cast<float*>(a.x_scale);
             if (quantized_act(a.kind) && a.x) {
-                ph.flags |= kPhaseQuantize;
                 ph.xq_out = const_cast<int8_t*>(a.x_i8);
+                ph.flags |= kPhaseQuantize;  // may become kPhasePreQuant below
             }
+            phase_rd.push_back(rd);
+            phase_wr.push_back(wr);
             if (a.token) {
                 ph.flags |= kPhaseHead;
                 ph.logits = a.logits;
@@ -520,6 +523,24 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
             }
             if (a.K > max_k) max_k = a.K;
             i = j;
+        }
+        // Quantize an input once in the launch's prologue instead of in every
+        // CTA when nothing else in the launch touches its codes / scale and the
+        // launch does not produce the input itself.
+        for (int q = 0; q < sp.nphase; ++q) {
+            StepPhase& ph = sp.ph[q];
+            if (!(ph.flags & kPhaseQuantize) || (ph.flags & kPhaseXWritten)) continue;
+            std::vector<Range> out;
+            add_range(out, ph.xq_out, (size_t)ph.K);
+            add_range(out, ph.x_scale, 4);
+            bool private_out = true;
+            for (int o = 0; o < sp.nphase && private_out; ++o)
+                if (o != q && (any_overlap(out, phase_rd[o]) || any_overlap(out, phase_wr[o])))
+                    private_out = false;
+            if (private_out) {
+                ph.flags = (ph.flags & ~kPhaseQuantize) | kPhasePreQuant;
+                sp.prequant = 1;
+            }
         }
         sp.group = ops[0].group_size >= 32 ? ops[0].group_size : 32;
         sp.spin_limit = tune().SPIN > 0 ? (unsigned)tune().SPIN : 20000000u;

@@ -66,7 +66,13 @@ struct GemvParams {
 
 constexpr int kMaxStepPhases = 144;   // phases per launch (kernel parameter space)
 
-enum StepFlags : int { kPhaseHead = 1, kPhaseQuantize = 2, kPhaseBarrier = 4, kPhaseXWritten = 8 };
+enum StepFlags : int {
+    kPhaseHead = 1,       // lm_head: logits + greedy token
+    kPhaseQuantize = 2,   // quantize the fp16 activations inside the phase
+    kPhaseBarrier = 4,    // grid barrier before the phase
+    kPhaseXWritten = 8,   // activations written earlier in this launch
+    kPhasePreQuant = 16   // activations quantized in the launch's prologue
+};
 
 struct StepSeg {
     const void* W;
@@ -94,6 +100,7 @@ struct StepPhase {
 struct StepParams {
     StepPhase ph[kMaxStepPhases];
     int nphase;
+    int prequant;         // some phase has kPhasePreQuant (the prologue runs)
     int group;
     unsigned spin_limit;  // bound on every barrier wait
     unsigned* bar;        // 2 zeroed words: arrivals, generation

@@ -32,7 +32,7 @@ struct StepCfg;
 template <bool B>
 struct StepCfg<PolicyFP<B>> { static constexpr int kWarps = 24; };
 template <>
-struct StepCfg<PolicyI8> { static constexpr int kWarps = 24; };
+struct StepCfg<PolicyI8> { static constexpr int kWarps = 16; };
 template <>
 struct StepCfg<PolicyW4A16> { static constexpr int kWarps = 16; };
 template <>
@@ -127,6 +127,24 @@ __device__ float quantize_token_smem(const __half* x, int K, int8_t* q, float* r
     return s;
 }
 
+// The launch's prologue: CTA b quantizes the activations of the b-th, (b+G)-th,
+// ... phase flagged kPhasePreQuant (each distinct input once, not once per
+// CTA), with the arithmetic of k_quant_act, into the phase's x_i8 / x_scale.
+__device__ void prequantize(const StepParams& sp, int8_t* qbuf, float* red) {
+    int j = 0;
+    for (int p = 0; p < sp.nphase; ++p) {
+        const StepPhase& ph = sp.ph[p];
+        if (!(ph.flags & kPhasePreQuant)) continue;
+        if (j++ % (int)gridDim.x != (int)blockIdx.x) continue;
+        const float s = quantize_token_smem(static_cast<const __half*>(ph.x), ph.K, qbuf, red);
+        __syncthreads();
+        for (int k = threadIdx.x * 16; k < ph.K; k += blockDim.x * 16)
+            *reinterpret_cast<uint4*>(ph.xq_out + k) = *reinterpret_cast<const uint4*>(qbuf + k);
+        if (threadIdx.x == 0) ph.x_scale[0] = s;
+        __syncthreads();
+    }
+}
+
 template <class P>
 __host__ __device__ constexpr size_t step_smem_layout_x(int max_k) {
     return (P::x_bytes(1, max_k) + 15) & ~(size_t)15;
@@ -140,6 +158,7 @@ __device__ __forceinline__ int raw_act_bytes(const StepPhase& ph) {
 }
 template <class P>
 __device__ __forceinline__ const void* raw_act_src(const StepPhase& ph) {
+    if (P::kIntAct && (ph.flags & kPhasePreQuant)) return ph.xq_out;
     return (P::kIntAct && !(ph.flags & kPhaseQuantize)) ? static_cast<const void*>(ph.xq) : ph.x;
 }
 
@@ -181,6 +200,14 @@ __global__ void __launch_bounds__(NW * 32, 1)
 
     unsigned nbar = 0;  // grid barriers passed
     unsigned deal = 0;  // row groups dealt to this CTA's slots so far
+
+    if constexpr (P::kIntAct) {
+        if (sp.prequant) {
+            prequantize(sp, qraw, fred);
+            ++nbar;
+            if (!grid_barrier(sp.bar, nbar * G, sp.spin_limit, sp.err)) return;
+        }
+    }
 
     for (int p = 0; p < sp.nphase; ++p) {
         const StepPhase& ph = sp.ph[p];
@@ -240,7 +267,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
                     a.xq = qraw;
                     sx = s;
                 } else {
-                    sx = __ldg(ph.x_scale);
+                    // given codes, or codes the prologue wrote in this launch
+                    // (read through L2: the prologue's writes are not in L1)
+                    sx = (ph.flags & kPhasePreQuant) ? __ldcg(ph.x_scale) : __ldg(ph.x_scale);
                 }
             }
             P::stage_x(a, xs, 1);

@@ -224,3 +224,33 @@ def test_dependent_ops_in_one_step_match_sequential_calls():
 
     for got, ref in zip(run_step(), run_sequential()):
         assert torch.equal(got, ref)
+
+
+def test_w4a8_step_with_one_shared_code_buffer_for_every_layer():
+    """Callers often reuse one int8 scratch buffer for every layer's codes.
+    Then no input may be quantized ahead of its phase: each phase quantizes
+    its own input in place; results still match the oracle."""
+    need_gpu()
+    layers, _, _ = synth.decode_int4_workload(seed=6, layers=2, hidden=1024, kv=256, inter=2048,
+                                              vocab=0)
+    xq = torch.empty(1, 2048, dtype=torch.int8, device=DEV)     # shared scratch (max K)
+    xs = torch.empty(1, dtype=torch.float32, device=DEV)
+    ops, keep, outs = [], [], []
+    for L in layers:
+        xin = {k: v.to(DEV) for k, v in L.inputs.items()}
+        keep += list(xin.values())
+        for lin in L.linears:
+            W, S = lin.W.to(DEV), lin.scales.to(DEV)
+            y = torch.empty(1, lin.N, dtype=torch.float16, device=DEV)
+            keep += [W, S, y]
+            outs.append((L, lin, y))
+            ops.append(dg.linear(dg.LINEAR_W4A8, W, 1, lin.N, lin.K, w_scale=S, x=xin[lin.x_name],
+                                 x_i8=xq[:, :lin.K], x_scale=xs, y=y))
+    plan = dg.StepPlan(ops, keep)
+    ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=DEV)
+    dg.decode_step_weights(plan, ws)
+    sync()
+    for L, lin, y in outs:
+        q, s = oracle.quant_act(bits(L.inputs[lin.x_name]))
+        yr, A, _ = oracle.gemv_w4a8(lin.W.numpy(), bits(lin.scales), q, s)
+        tol.assert_close(y.cpu().double().numpy(), yr, A, "f16", "shared-scratch %s" % lin.name)
