@@ -73,6 +73,7 @@ int* device_error_word() {
 // barrier between every pair of phases of the persistent kernel.
 struct Tune {
     int R = 0, KS = 0, CPS = 0, PF = -1, PDL = -1, STEP = -1, SPIN = -1, SNW = 0, MMA = -1;
+    int RING = -1, TSB = 0, TNS = 0, TNC = 0;  // weight ring: on/off, KB per stage, stages, consumers
 };
 
 static Tune read_tune() {
@@ -93,6 +94,10 @@ static Tune read_tune() {
         else if (std::sscanf(tok, "SPIN=%d", &v) == 1) t.SPIN = v;
         else if (std::sscanf(tok, "SNW=%d", &v) == 1) t.SNW = v;
         else if (std::sscanf(tok, "MMA=%d", &v) == 1) t.MMA = v;
+        else if (std::sscanf(tok, "RING=%d", &v) == 1) t.RING = v;
+        else if (std::sscanf(tok, "TSB=%d", &v) == 1) t.TSB = v;
+        else if (std::sscanf(tok, "TNS=%d", &v) == 1) t.TNS = v;
+        else if (std::sscanf(tok, "TNC=%d", &v) == 1) t.TNC = v;
     }
     return t;
 }
@@ -388,6 +393,12 @@ static size_t head_ws_bytes() { return (size_t)kMaxArgCtas * sizeof(ArgPart); }
 // Decode-step workspace: [0, 256) the persistent kernel's barrier words,
 // then the argmax partials when the step has an lm_head.
 constexpr size_t kStepHeader = 256;
+// Weight ring of the fp16 / bf16 step kernel: 6 stages of 36 KB in flight per
+// SM (a copy's worth of bytes for the HBM latency several times over); a
+// stage grows to the longest row when one row does not fit.
+constexpr size_t kRingStageBytes = 36864;
+constexpr int kRingStages = 6;
+constexpr int kRingMaxStages = 16;
 
 // ---- the persistent decode-step path -----------------------------------------------
 
@@ -399,12 +410,14 @@ static bool same_group(const dg_linear& a, const dg_linear& b) {
 // Ops the persistent kernel runs: one token, no int32 accumulator output.
 static bool step_eligible(const dg_linear& op) { return op.M == 1 && !op.acc_out; }
 
-static int step_occupancy(Fmt f, int max_k, size_t smem) {
+// CTAs of the step kernel per SM (ring_nc = 0: k_step; else k_step_ring
+// with that many consumer warps).
+static int step_occupancy(Fmt f, int max_k, size_t smem, int ring_nc, int nw) {
     static std::mutex mu;
-    static std::map<std::tuple<int, int, int>, int> cache;
+    static std::map<std::tuple<int, int, int, size_t, int, int>, int> cache;
     int dev = 0;
     cudaGetDevice(&dev);
-    const auto key = std::make_tuple(dev, (int)f, max_k);
+    const auto key = std::make_tuple(dev, (int)f, max_k, smem, ring_nc, nw);
     {
         std::lock_guard<std::mutex> g(mu);
         auto it = cache.find(key);
@@ -412,7 +425,9 @@ static int step_occupancy(Fmt f, int max_k, size_t smem) {
     }
     StepParams* none = nullptr;
     int occ = 0;
-    if (step_launch(f, none, 0, smem, nullptr, &occ, tune().SNW) != cudaSuccess) occ = 0;
+    const cudaError_t e = ring_nc ? step_ring_launch(f, none, 0, smem, nullptr, &occ, ring_nc)
+                                  : step_launch(f, none, 0, smem, nullptr, &occ, nw);
+    if (e != cudaSuccess) occ = 0;
     std::lock_guard<std::mutex> g(mu);
     cache[key] = occ;
     return occ;
@@ -454,6 +469,36 @@ static bool any_overlap(const std::vector<Range>& a, const std::vector<Range>& b
         for (const Range& y : b)
             if (overlaps(x, y)) return true;
     return false;
+}
+
+// Weight and scale bytes of an op.
+static void weight_ranges(const dg_linear& op, std::vector<Range>& v) {
+    const size_t N = (size_t)op.N, K = (size_t)op.K;
+    switch (op.kind) {
+        case DG_LINEAR_F16:
+        case DG_LINEAR_BF16: add_range(v, op.W, N * K * 2); break;
+        case DG_LINEAR_W8A8:
+            add_range(v, op.W, N * K);
+            add_range(v, op.w_scale, N * 4);
+            break;
+        default:  // int4
+            add_range(v, op.W, N * K / 2);
+            if (op.group_size > 0) add_range(v, op.w_scale, N * (K / (size_t)op.group_size) * 2);
+            break;
+    }
+}
+
+// True when an op of ops[0..n) writes into the weights or scales of an op of
+// the same run.  The persistent kernels read weights without coherence (and
+// the weight ring copies them ahead of any barrier), so such a run goes to the
+// per-launch path, which keeps the ops' order.
+static bool run_writes_weights(const dg_linear* ops, int n) {
+    std::vector<Range> w, out, rd;
+    for (int i = 0; i < n; ++i) {
+        weight_ranges(ops[i], w);
+        op_ranges(ops[i], rd, out);
+    }
+    return any_overlap(out, w);
 }
 
 // Runs ops[0..n) (all of one kind, all step-eligible) with the persistent
@@ -548,15 +593,54 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
         sp.part = reinterpret_cast<ArgPart*>(static_cast<unsigned char*>(ws) + kStepHeader);
         sp.err = device_error_word();
         if (!sp.err) return DG_ERR_CUDA;
-        const size_t smem = step_smem(f, max_k);
+        // fp16 / bf16 with the weight ring selected (DG_TUNE=RING=1; measured
+        // slower than k_step on the decoder shapes, so not the default): when
+        // whole rows fit a stage and at least two stages fit shared memory
+        int ring_nc = 0;
+        size_t smem = 0;
+        if ((f == F_F16 || f == F_BF16) && tune().RING == 1) {
+            const int nc = tune().TNC == 8 ? 8 : 12;
+            const size_t rb_max = (size_t)max_k * 2;
+            size_t sb = tune().TSB > 0 ? (size_t)tune().TSB * 1024 : kRingStageBytes;
+            if (sb < rb_max) sb = (rb_max + 127) & ~(size_t)127;
+            const size_t over = step_ring_overhead(nc), lim = smem_optin_limit();
+            int ns = lim > over ? (int)((lim - over) / sb) : 0;
+            ns = std::min(ns, tune().TNS > 0 ? tune().TNS : kRingStages);
+            ns = std::min(ns, kRingMaxStages);
+            if (ns >= 2) {
+                ring_nc = nc;
+                sp.nstage = ns;
+                sp.stage_bytes = (int)sb;
+                smem = (size_t)ns * sb + over;
+                // activations that no op of the launch writes, of phases whose
+                // lanes keep them in registers, travel in the ring ahead of
+                // their rows (the producer copies them before any barrier)
+                for (int q = 0; q < sp.nphase; ++q) {
+                    StepPhase& ph = sp.ph[q];
+                    const int nch = ph.K / 8, stp = ph.ks * 32;
+                    if (!(ph.flags & kPhaseXWritten) && (nch + stp - 1) / stp <= kRingXR)
+                        ph.flags |= kPhaseXRing;
+                }
+            }
+        }
+        if (!ring_nc) smem = step_smem(f, max_k);
         if (smem > smem_optin_limit()) return DG_ERR_UNSUPPORTED;
-        const int occ = step_occupancy(f, max_k, smem);
+        // k_step's slot barriers are disjoint for ks = 2 and ks = 4 only up to
+        // 16 warps: a launch with both splits runs 16 warps
+        bool ks2 = false, ks4 = false;
+        for (int q = 0; q < sp.nphase; ++q) {
+            ks2 = ks2 || sp.ph[q].ks == 2;
+            ks4 = ks4 || sp.ph[q].ks == 4;
+        }
+        const int nw = (ks2 && ks4) ? 16 : tune().SNW;
+        const int occ = step_occupancy(f, max_k, smem, ring_nc, nw);
         if (occ < 1) return DG_ERR_UNSUPPORTED;
         const int grid = sm_count() * occ;
         if (grid > kMaxArgCtas) return DG_ERR_UNSUPPORTED;
         if (cudaMemsetAsync(ws, 0, 2 * sizeof(unsigned), s) != cudaSuccess) return DG_ERR_CUDA;
-        if (step_launch(f, &sp, grid, smem, s, nullptr, tune().SNW) != cudaSuccess)
-            return DG_ERR_CUDA;
+        const cudaError_t e = ring_nc ? step_ring_launch(f, &sp, grid, smem, s, nullptr, ring_nc)
+                                      : step_launch(f, &sp, grid, smem, s, nullptr, nw);
+        if (e != cudaSuccess) return DG_ERR_CUDA;
     }
     return DG_OK;
 }
@@ -694,7 +778,7 @@ dg_status dg_decode_step_weights(const dg_linear* ops, int n_ops, void* ws, size
         // a maximal run of step-eligible ops of one kind goes to the persistent kernel
         int j = i;
         while (persistent && j < n_ops && ops[j].kind == ops[i].kind && step_eligible(ops[j])) ++j;
-        if (j > i) {
+        if (j > i && !run_writes_weights(ops + i, j - i)) {
             dg_status st = launch_step_run(ops + i, j - i, ws, stream);
             if (st != DG_OK) return st;
             i = j;

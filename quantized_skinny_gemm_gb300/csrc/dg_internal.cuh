@@ -71,8 +71,13 @@ enum StepFlags : int {
     kPhaseQuantize = 2,   // quantize the fp16 activations inside the phase
     kPhaseBarrier = 4,    // grid barrier before the phase
     kPhaseXWritten = 8,   // activations written earlier in this launch
-    kPhasePreQuant = 16   // activations quantized in the launch's prologue
+    kPhasePreQuant = 16,  // activations quantized in the launch's prologue
+    kPhaseXRing = 32      // k_step_ring: x travels in the weight ring ahead of the rows
 };
+
+// k_step_ring keeps a lane's activation chunks of a phase in registers when
+// they number at most this (rows of up to 9 * 32 * ks chunks).
+constexpr int kRingXR = 9;
 
 struct StepSeg {
     const void* W;
@@ -106,6 +111,8 @@ struct StepParams {
     unsigned* bar;        // 2 zeroed words: arrivals, generation
     ArgPart* part;        // one partial per CTA (lm_head phases)
     int* err;             // device error word
+    int nstage;           // weight ring (k_step_ring): stages
+    int stage_bytes;      //   and bytes per stage (a multiple of 128)
 };
 
 constexpr int kErrTimeout = 1;
@@ -298,6 +305,11 @@ int head_grid(const dg_linear& op);
 // format's default).  occ != nullptr: report CTAs per SM instead.
 cudaError_t step_launch(Fmt f, const StepParams* sp, int grid, size_t smem, cudaStream_t s,
                         int* occ, int nw);
+// The weight-ring variant of the persistent step (fp16 / bf16 weights, one
+// token): `nc` consumer warps (8 or 12) plus one producer warp per CTA.
+size_t step_ring_overhead(int nc);
+cudaError_t step_ring_launch(Fmt f, const StepParams* sp, int grid, size_t smem, cudaStream_t s,
+                             int* occ, int nc);
 size_t step_smem(Fmt f, int max_k);
 cudaError_t launch_wait_selftest(unsigned limit, int* err, cudaStream_t s);
 

@@ -413,6 +413,16 @@ struct PolicyW4A8 {
     }
 };
 
+// Named barrier of warp `warp`'s slot when ks = 2 or 4 warps share a row.
+// In a persistent kernel warps move through phases independently, so phases
+// with different ks can be live at once, and a named barrier must never be
+// used with two thread counts at the same time: the two splits take disjoint
+// ids, ks = 2 from 1 upward and ks = 4 from 14 downward (disjoint for up to
+// 16 warps; 0 is __syncthreads, 15 the weight ring's consumer barrier).
+__device__ __forceinline__ int slot_barrier(int warp, int ks) {
+    return ks == 4 ? 14 - warp / 4 : 1 + warp / ks;
+}
+
 // ---- the row-group computation shared by all kernels ------------------------------
 
 // Chunks per row loaded ahead of use: about eight loads in flight per lane.
@@ -426,6 +436,18 @@ struct RowGeom {
     int K, nchunks, gk, cpg, ks;
     size_t rb;
 };
+
+template <class P>
+__device__ __forceinline__ RowGeom row_geom_gk(int K, int group, int ks, int gk) {
+    RowGeom g;
+    g.K = K;
+    g.nchunks = K / P::kElems;
+    g.gk = gk;
+    g.cpg = group / 32;
+    g.ks = ks;
+    g.rb = P::row_bytes(K);
+    return g;
+}
 
 template <class P>
 __device__ __forceinline__ RowGeom row_geom(int K, int group, int ks) {
@@ -455,7 +477,7 @@ __device__ __forceinline__ void rows_of(const SegTable& t, int rg, bool active, 
 
 // Streams R rows for this lane and returns the per-row sums, complete in every
 // lane of the slot's first warp (kw == 0).  With ks > 1 the slot's warps meet
-// at named barrier 1 + slot, so all of them must call it; inactive slots pass
+// at the slot's named barrier, so all of them must call it; inactive slots pass
 // active = false.
 // DX: one token, activations read from global memory at `xs` (coherent:
 // bypassing L1); otherwise `xs` is the staged shared-memory copy.
@@ -519,8 +541,8 @@ __device__ __forceinline__ void row_group(const RowRef (&rows)[R], bool active, 
 #pragma unroll
                 for (int m = 0; m < MT; ++m) red[(warp * R + r) * MT + m] = to_bits(acc[r][m]);
         }
-        // only the slot's warps meet (named barrier 1 + slot, ks warps)
-        const int bar = 1 + warp / ks;
+        // only the slot's warps meet (its named barrier, ks warps)
+        const int bar = slot_barrier(warp, ks);
         asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(ks * 32) : "memory");
         if (kw == 0) {
             for (int j = 1; j < ks; ++j) {

@@ -16,7 +16,7 @@
 // Every wait is bounded: a barrier that does not complete within the spin
 // limit records an error (reported by dg_check_device_status) and the CTA
 // leaves; the other CTAs then time out at their next barrier as well.
-#include "gemv_core.cuh"
+#include "step_common.cuh"
 
 namespace dg {
 
@@ -37,29 +37,6 @@ template <>
 struct StepCfg<PolicyW4A16> { static constexpr int kWarps = 16; };
 template <>
 struct StepCfg<PolicyW4A8> { static constexpr int kWarps = 16; };
-
-// Row r (global over the phase's segments) of phase ph.
-__device__ __forceinline__ RowRef locate_step(const StepPhase& ph, int r, size_t rb) {
-    RowRef rr{};
-    int s = 0;
-#pragma unroll
-    for (int i = 1; i < kMaxSeg; ++i)
-        if (i < ph.nseg && r >= ph.seg[i].row_begin) s = i;
-    const StepSeg& sg = ph.seg[s];
-    rr.local = r - sg.row_begin;
-    rr.w = static_cast<const unsigned char*>(sg.W) + (size_t)rr.local * rb;
-    rr.scale = sg.scale;
-    rr.y = sg.y;
-    rr.acc_out = nullptr;
-    rr.seg_rows = sg.rows;
-    rr.global = r;
-    rr.valid = true;
-    return rr;
-}
-
-__device__ __forceinline__ int slice_begin(int N, int b, int G) {
-    return (int)(((long long)N * b) / G);
-}
 
 // Grid barrier for a co-resident (cooperative) grid.  bar[0] counts arrivals
 // over the whole launch (zeroed before it); barrier number e (1, 2, ...)
@@ -145,9 +122,15 @@ __device__ void prequantize(const StepParams& sp, int8_t* qbuf, float* red) {
     }
 }
 
+// Staged activations (formats that read x from shared memory).
 template <class P>
 __host__ __device__ constexpr size_t step_smem_layout_x(int max_k) {
-    return (P::x_bytes(1, max_k) + 15) & ~(size_t)15;
+    return P::kDirectX ? 0 : (P::x_bytes(1, max_k) + 15) & ~(size_t)15;
+}
+// Each of the two raw activation buffers (none when x is read from global).
+template <class P>
+__host__ __device__ constexpr size_t step_raw_bytes(int max_k) {
+    return P::kDirectX ? 0 : ((size_t)max_k * 2 + 15) & ~(size_t)15;
 }
 
 // Raw activation bytes of a phase as they sit in global memory: fp16 / bf16 x,
@@ -186,11 +169,13 @@ __global__ void __launch_bounds__(NW * 32, 1)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int G = gridDim.x, b = blockIdx.x;
 
-    // shared memory: staged activations | two raw activation buffers | scratch
-    const size_t raw_bytes = ((size_t)max_k * 2 + 15) & ~(size_t)15;
-    unsigned char* xs_fmt = smem;
-    unsigned char* rawx[2] = {smem + step_smem_layout_x<P>(max_k),
-                              smem + step_smem_layout_x<P>(max_k) + raw_bytes};
+    // shared memory: phase table | staged activations | two raw activation
+    // buffers | scratch
+    PhaseSlice* table = reinterpret_cast<PhaseSlice*>(smem);
+    const size_t raw_bytes = step_raw_bytes<P>(max_k);
+    unsigned char* xs_fmt = smem + kPhaseTableBytes;
+    unsigned char* rawx[2] = {xs_fmt + step_smem_layout_x<P>(max_k),
+                              xs_fmt + step_smem_layout_x<P>(max_k) + raw_bytes};
     int* red = reinterpret_cast<int*>(rawx[1] + raw_bytes);
     ArgPart* cta_best = reinterpret_cast<ArgPart*>(red + NW * kStepRMax);
     float* fred = reinterpret_cast<float*>(cta_best + NW);
@@ -199,7 +184,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     bool staged_ahead = false;  // this phase's raw activations are already in flight
 
     unsigned nbar = 0;  // grid barriers passed
-    unsigned deal = 0;  // row groups dealt to this CTA's slots so far
+    plan_phases(sp, table, b, G, [](const StepPhase&, int n) { return (n + R - 1) / R; });
 
     if constexpr (P::kIntAct) {
         if (sp.prequant) {
@@ -209,31 +194,21 @@ __global__ void __launch_bounds__(NW * 32, 1)
         }
     }
 
+    // The first read of a phase's parameters on an SM misses the constant
+    // cache; thread 0 touches the lines of phase p + 2 while phase p runs (the
+    // values only feed a comparison at the end, so the loads never stall it).
+    int touch = 0;
     for (int p = 0; p < sp.nphase; ++p) {
         const StepPhase& ph = sp.ph[p];
+        if (threadIdx.x == 0 && p + 2 < sp.nphase) {
+            const int* w = reinterpret_cast<const int*>(&sp.ph[p + 2]);
+            touch ^= w[0] ^ w[16] ^ w[32] ^ w[48];
+        }
         if (p > 0 && (ph.flags & kPhaseBarrier)) {
             ++nbar;
             if (!grid_barrier(sp.bar, nbar * G, sp.spin_limit, sp.err)) return;
-            if ((sp.ph[p - 1].flags & kPhaseHead) && b == 0 && threadIdx.x < 32) {
-                // greedy token of the previous (lm_head) phase from the CTAs' partials
-                float bv = NAN;
-                int bi = INT_MAX;
-                for (int i = lane; i < G; i += 32)
-                    if (arg_better(sp.part[i].v, sp.part[i].i, bv, bi)) {
-                        bv = sp.part[i].v;
-                        bi = sp.part[i].i;
-                    }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                    if (arg_better(ov, oi, bv, bi)) {
-                        bv = ov;
-                        bi = oi;
-                    }
-                }
-                if (lane == 0) *sp.ph[p - 1].token = bi == INT_MAX ? -1 : bi;
-            }
+            if ((sp.ph[p - 1].flags & kPhaseHead) && b == 0 && threadIdx.x < 32)
+                reduce_token(sp.part, G, sp.ph[p - 1].token);
         }
         float sx = 1.f;
         unsigned char* xs = xs_fmt;
@@ -284,15 +259,16 @@ __global__ void __launch_bounds__(NW * 32, 1)
         const int ks = ph.ks;
         const int slots = NW / ks;
         const int slot = warp / ks, kw = warp - slot * ks;
-        const RowGeom g = row_geom<P>(ph.K, sp.group, ks);
-        const int r0 = slice_begin(ph.N, b, G), r1 = slice_begin(ph.N, b + 1, G);
-        const int n_rg = (r1 - r0 + R - 1) / R;
+        const PhaseSlice sl = table[p];
+        const RowGeom g = row_geom_gk<P>(ph.K, sp.group, ks, sl.gk);
+        const int r0 = sl.r0, r1 = sl.r0 + sl.n;
+        const int n_rg = (sl.n + R - 1) / R;
         // row groups are dealt round-robin over the whole step (continuing
         // where the previous phase stopped) so every warp streams a fair share
-        const int lead = (int)(deal % (unsigned)slots);
-        const int mine = (slot - lead + slots) % slots;  // first row group of this slot
-        const int iters = (n_rg - mine + slots - 1) / slots;  // the same in all of the slot's warps
-        deal += (unsigned)n_rg;
+        const int lead = mod_slots<NW>(sl.deal0, ks);
+        const int mine = slot >= lead ? slot - lead : slot - lead + slots;  // first row group
+        // the same in all of the slot's warps
+        const int iters = n_rg > mine ? div_slots<NW>(n_rg - mine + slots - 1, ks) : 0;
         const bool head = (ph.flags & kPhaseHead) != 0;
         float best_v = NAN;
         int best_i = INT_MAX;
@@ -357,37 +333,21 @@ __global__ void __launch_bounds__(NW * 32, 1)
         // (the next phase's first barrier orders its restaging after this phase)
     }
 
+    if (touch == 0x5eed && b == G) sp.err[1] = touch;  // never true (b < G): keeps the loads
+
     if (sp.ph[sp.nphase - 1].flags & kPhaseHead) {
         ++nbar;
         if (!grid_barrier(sp.bar, nbar * G, sp.spin_limit, sp.err)) return;
-        if (b == 0 && threadIdx.x < 32) {
-            float bv = NAN;
-            int bi = INT_MAX;
-            for (int i = lane; i < G; i += 32)
-                if (arg_better(sp.part[i].v, sp.part[i].i, bv, bi)) {
-                    bv = sp.part[i].v;
-                    bi = sp.part[i].i;
-                }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                if (arg_better(ov, oi, bv, bi)) {
-                    bv = ov;
-                    bi = oi;
-                }
-            }
-            if (lane == 0) *sp.ph[sp.nphase - 1].token = bi == INT_MAX ? -1 : bi;
-        }
+        if (b == 0 && threadIdx.x < 32) reduce_token(sp.part, G, sp.ph[sp.nphase - 1].token);
     }
 }
 
 template <class P>
 size_t step_smem_for(int max_k) {
     constexpr int NW = 32;  // the largest CTA any format uses
-    const size_t raw_bytes = ((size_t)max_k * 2 + 15) & ~(size_t)15;
-    return step_smem_layout_x<P>(max_k) + 2 * raw_bytes + (size_t)NW * kStepRMax * 4 +
-           (size_t)NW * sizeof(ArgPart) + (size_t)NW * 4 + 16 + (size_t)max_k + 16;
+    return kPhaseTableBytes + step_smem_layout_x<P>(max_k) + 2 * step_raw_bytes<P>(max_k) +
+           (size_t)NW * kStepRMax * 4 + (size_t)NW * sizeof(ArgPart) + (size_t)NW * 4 + 16 +
+           (P::kDirectX ? 0 : (size_t)max_k + 16);
 }
 
 template <class P, int NW>
