@@ -501,6 +501,27 @@ static bool run_writes_weights(const dg_linear* ops, int n) {
     return any_overlap(out, w);
 }
 
+// W4A8 step phases whose activations are ready before the launch (given
+// codes, or quantized once in its prologue) get a copy in the kernel's
+// interleaved layout plus the chunk sums, written by the prologue into the
+// workspace after the barrier words and argmax partials.
+static size_t w4a8_layout_bytes(int K) {
+    const size_t nch = (size_t)(K / 32);
+    const size_t bytes = ((nch + 31) / 32) * 32 * 32 + nch * 4;
+    return (bytes + 255) & ~(size_t)255;
+}
+static size_t step_scratch_offset(const dg_linear* ops, int n) {
+    for (int i = 0; i < n; ++i)
+        if (ops[i].token) return kStepHeader + head_ws_bytes();
+    return kStepHeader;
+}
+static size_t step_scratch_bytes(const dg_linear* ops, int n) {
+    size_t b = 0;
+    for (int i = 0; i < n; ++i)
+        if (ops[i].kind == DG_LINEAR_W4A8 && ops[i].M == 1) b += w4a8_layout_bytes(ops[i].K);
+    return b;
+}
+
 // Runs ops[0..n) (all of one kind, all step-eligible) with the persistent
 // kernel, in launches of at most kMaxStepPhases phases.  A phase gets a grid
 // barrier when it conflicts with a phase since the previous barrier (RAW, WAR
@@ -551,6 +572,7 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
             ph.nseg = j - i;
             ph.N = rows;
             ph.K = a.K;
+            ph.group = a.group_size >= 32 ? a.group_size : 32;
             ph.ks = pick_ks(f, a.K);
             ph.x = a.x;
             ph.xq = a.x_i8;
@@ -587,7 +609,21 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
                 sp.prequant = 1;
             }
         }
-        sp.group = ops[0].group_size >= 32 ? ops[0].group_size : 32;
+        // W4A8: activations ready before the launch are laid out once by the
+        // prologue and read from the workspace (no per-phase staging)
+        if (f == F_W4A8) {
+            unsigned char* scratch = static_cast<unsigned char*>(ws) + step_scratch_offset(ops, n);
+            size_t off = 0;
+            for (int q = 0; q < sp.nphase; ++q) {
+                StepPhase& ph = sp.ph[q];
+                const bool given = !(ph.flags & (kPhaseQuantize | kPhasePreQuant | kPhaseXWritten));
+                if (!(ph.flags & kPhasePreQuant) && !given) continue;
+                ph.flags |= kPhaseXLaid;
+                ph.xlay = scratch + off;
+                off += w4a8_layout_bytes(ph.K);
+                sp.prequant = 1;
+            }
+        }
         sp.spin_limit = tune().SPIN > 0 ? (unsigned)tune().SPIN : 20000000u;
         sp.bar = static_cast<unsigned*>(ws);
         sp.part = reinterpret_cast<ArgPart*>(static_cast<unsigned char*>(ws) + kStepHeader);
@@ -668,9 +704,7 @@ const char* dg_version(void) { return "dg 0.1 (sm_103a)"; }
 
 size_t dg_workspace_bytes(const dg_linear* ops, int n_ops) {
     if (!ops || n_ops <= 0) return 0;
-    for (int i = 0; i < n_ops; ++i)
-        if (ops[i].token) return kStepHeader + head_ws_bytes();
-    return kStepHeader;
+    return step_scratch_offset(ops, n_ops) + step_scratch_bytes(ops, n_ops);
 }
 
 dg_status dg_gemv_f16(const void* W, const void* x, void* y, dg_ftype t, int M, int N, int K,

@@ -72,7 +72,9 @@ enum StepFlags : int {
     kPhaseBarrier = 4,    // grid barrier before the phase
     kPhaseXWritten = 8,   // activations written earlier in this launch
     kPhasePreQuant = 16,  // activations quantized in the launch's prologue
-    kPhaseXRing = 32      // k_step_ring: x travels in the weight ring ahead of the rows
+    kPhaseXRing = 32,     // k_step_ring: x travels in the weight ring ahead of the rows
+    kPhaseXLaid = 64      // the prologue wrote x in the format's layout at xlay: the
+                          // MACs read it from global memory (no staging, no meeting)
 };
 
 // k_step_ring keeps a lane's activation chunks of a phase in registers when
@@ -99,14 +101,15 @@ struct StepPhase {
     int8_t* xq_out;       // where the quantization writes its codes (may be null)
     float* logits;        // lm_head
     int32_t* token;       // lm_head
-    int32_t K, N, nseg, flags, ks, pad;
+    unsigned char* xlay;  // kPhaseXLaid: the activations in the format's layout (workspace)
+    int32_t K, N, nseg, flags, ks;
+    int32_t group;        // int4 scale group along K (the ops of a phase share it)
 };
 
 struct StepParams {
     StepPhase ph[kMaxStepPhases];
     int nphase;
-    int prequant;         // some phase has kPhasePreQuant (the prologue runs)
-    int group;
+    int prequant;         // the launch's prologue runs (kPhasePreQuant / kPhaseXLaid phases)
     unsigned spin_limit;  // bound on every barrier wait
     unsigned* bar;        // 2 zeroed words: arrivals, generation
     ArgPart* part;        // one partial per CTA (lm_head phases)
@@ -114,6 +117,9 @@ struct StepParams {
     int nstage;           // weight ring (k_step_ring): stages
     int stage_bytes;      //   and bytes per stage (a multiple of 128)
 };
+
+// StepParams travels as a kernel parameter (at most 32,764 bytes).
+static_assert(sizeof(StepParams) <= 32764, "step parameters exceed the kernel parameter space");
 
 constexpr int kErrTimeout = 1;
 

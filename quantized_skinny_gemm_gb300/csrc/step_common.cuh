@@ -79,7 +79,7 @@ __device__ void plan_phases(const StepParams& sp, PhaseSlice* table, int b, int 
         if (lane == 0) {
             table[p].r0 = r0;
             table[p].n = r1 - r0;
-            table[p].gk = sp.group > 0 ? ph.K / sp.group : 0;
+            table[p].gk = ph.group > 0 ? ph.K / ph.group : 0;
             table[p].deal0 = (unsigned)units(ph, r1 - r0);  // scanned below
         }
     }

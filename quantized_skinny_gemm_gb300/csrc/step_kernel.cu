@@ -104,20 +104,32 @@ __device__ float quantize_token_smem(const __half* x, int K, int8_t* q, float* r
     return s;
 }
 
-// The launch's prologue: CTA b quantizes the activations of the b-th, (b+G)-th,
-// ... phase flagged kPhasePreQuant (each distinct input once, not once per
-// CTA), with the arithmetic of k_quant_act, into the phase's x_i8 / x_scale.
-__device__ void prequantize(const StepParams& sp, int8_t* qbuf, float* red) {
+// The launch's prologue.  CTA b takes the b-th, (b+G)-th, ... phase flagged
+// kPhasePreQuant or kPhaseXLaid (each distinct input once, not once per CTA):
+// a kPhasePreQuant input is quantized with the arithmetic of k_quant_act into
+// the phase's x_i8 / x_scale; a kPhaseXLaid phase's codes (just quantized, or
+// given) are then written in the format's layout to its xlay, from where every
+// CTA's MACs read them.
+template <class P>
+__device__ void prologue(const StepParams& sp, int8_t* qbuf, float* red) {
     int j = 0;
     for (int p = 0; p < sp.nphase; ++p) {
         const StepPhase& ph = sp.ph[p];
-        if (!(ph.flags & kPhasePreQuant)) continue;
+        if (!(ph.flags & (kPhasePreQuant | kPhaseXLaid))) continue;
         if (j++ % (int)gridDim.x != (int)blockIdx.x) continue;
-        const float s = quantize_token_smem(static_cast<const __half*>(ph.x), ph.K, qbuf, red);
-        __syncthreads();
-        for (int k = threadIdx.x * 16; k < ph.K; k += blockDim.x * 16)
-            *reinterpret_cast<uint4*>(ph.xq_out + k) = *reinterpret_cast<const uint4*>(qbuf + k);
-        if (threadIdx.x == 0) ph.x_scale[0] = s;
+        const int8_t* codes = ph.xq;
+        if (ph.flags & kPhasePreQuant) {
+            const float s = quantize_token_smem(static_cast<const __half*>(ph.x), ph.K, qbuf, red);
+            __syncthreads();
+            for (int k = threadIdx.x * 16; k < ph.K; k += blockDim.x * 16)
+                *reinterpret_cast<uint4*>(ph.xq_out + k) = *reinterpret_cast<const uint4*>(qbuf + k);
+            if (threadIdx.x == 0) ph.x_scale[0] = s;
+            codes = qbuf;
+        }
+        if (ph.flags & kPhaseXLaid) {
+            ActIn a{nullptr, codes, ph.x_scale, ph.K, 1};
+            P::stage_x(a, ph.xlay, 1);
+        }
         __syncthreads();
     }
 }
@@ -188,7 +200,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
 
     if constexpr (P::kIntAct) {
         if (sp.prequant) {
-            prequantize(sp, qraw, fred);
+            prologue<P>(sp, qraw, fred);
             ++nbar;
             if (!grid_barrier(sp.bar, nbar * G, sp.spin_limit, sp.err)) return;
         }
@@ -212,7 +224,15 @@ __global__ void __launch_bounds__(NW * 32, 1)
         }
         float sx = 1.f;
         unsigned char* xs = xs_fmt;
-        if constexpr (!P::kDirectX) {
+        bool laid = false;
+        if constexpr (P::kIntAct) laid = (ph.flags & kPhaseXLaid) != 0;
+        if (laid) {
+            // laid out by the prologue: read from global memory in the MACs (the
+            // prologue's writes are not in this SM's L1), no staging and no
+            // CTA-wide meeting between phases
+            xs = ph.xlay;
+            sx = __ldcg(ph.x_scale);
+        } else if constexpr (!P::kDirectX) {
             // activations of this phase: raw bytes in rawx[p & 1] (copied ahead
             // during the previous phase when no barrier separates them), then
             // restaged in the format's layout
@@ -221,7 +241,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
             async_wait_all();
             __syncthreads();
             staged_ahead = false;
-            if (p + 1 < sp.nphase && !(sp.ph[p + 1].flags & kPhaseBarrier)) {
+            if (p + 1 < sp.nphase && !(sp.ph[p + 1].flags & (kPhaseBarrier | kPhaseXLaid))) {
                 const StepPhase& nx = sp.ph[p + 1];
                 async_copy_block(rawx[(p + 1) & 1], raw_act_src<P>(nx), raw_act_bytes<P>(nx));
                 staged_ahead = true;
@@ -260,7 +280,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
         const int slots = NW / ks;
         const int slot = warp / ks, kw = warp - slot * ks;
         const PhaseSlice sl = table[p];
-        const RowGeom g = row_geom_gk<P>(ph.K, sp.group, ks, sl.gk);
+        const RowGeom g = row_geom_gk<P>(ph.K, ph.group, ks, sl.gk);
         const int r0 = sl.r0, r1 = sl.r0 + sl.n;
         const int n_rg = (sl.n + R - 1) / R;
         // row groups are dealt round-robin over the whole step (continuing

@@ -111,6 +111,23 @@ def test_lm_head_validation_and_workspace(lib):
     assert dg.workspace_bytes([plain]) == 256  # the persistent step's barrier words
 
 
+def test_workspace_holds_the_w4a8_activation_layouts():
+    # per W4A8 op at M = 1: ceil(K/32/32)*32 chunks x 32 bytes of interleaved
+    # codes + K/32 int32 chunk sums, rounded up to 256 bytes, after the
+    # barrier words (and the argmax partials when an op is an lm_head)
+    def w4a8(K, **kw):
+        d = dict(kind=dg.LINEAR_W4A8, M=1, N=8, K=K, W=A, w_scale=A, x_i8=A, x_scale=A, y=B,
+                 group_size=32)
+        d.update(kw)
+        return dg.Linear(**d)
+    assert dg.workspace_bytes([w4a8(4096)]) == 256 + 4096 + 512
+    assert dg.workspace_bytes([w4a8(1024)]) == 256 + 1024 + 128 + 128  # 1152 -> 1280
+    assert dg.workspace_bytes([w4a8(14336), w4a8(4096)]) == 256 + (14336 + 1792) + 4608
+    head_ws = dg.workspace_bytes([_head()])
+    assert dg.workspace_bytes([w4a8(4096), _head()]) == head_ws + 4608
+    assert dg.workspace_bytes([w4a8(4096, M=2)]) == 256  # M > 1 runs per group
+
+
 def test_decode_step_validates_every_op_first(lib):
     good = [dg.Linear(kind=dg.LINEAR_F16, M=1, N=8, K=8, W=A, x=A, y=B) for _ in range(6)]
     bad = list(good)

@@ -254,3 +254,43 @@ def test_w4a8_step_with_one_shared_code_buffer_for_every_layer():
         q, s = oracle.quant_act(bits(L.inputs[lin.x_name]))
         yr, A, _ = oracle.gemv_w4a8(lin.W.numpy(), bits(lin.scales), q, s)
         tol.assert_close(y.cpu().double().numpy(), yr, A, "f16", "shared-scratch %s" % lin.name)
+
+
+def test_w4a8_step_with_given_codes_reads_the_prologue_layout():
+    """W4A8 ops whose int8 codes are given (no fp16 x): the launch's prologue
+    lays them out once in the workspace and every CTA reads them from there.
+    Two fused ops share one code vector, a third has its own; ragged N, groups
+    of 32 and 128; results equal the per-op calls bitwise and the oracle."""
+    need_gpu()
+    g = synth.generator(17)
+    shapes = [(777, 4096, 32), (1025, 4096, 32), (333, 1024, 128)]
+    xs = {}
+    keep, ops, cases = [], [], []
+    for i, (N, K, grp) in enumerate(shapes):
+        Wq = synth.int4_packed(N, K, g).to(DEV)
+        sc = synth.uniform((N, K // grp), 1e-3, 1e-2, g, torch.float16).to(DEV)
+        key = 0 if i < 2 else i  # ops 0 and 1 share their codes (one fused phase)
+        if key not in xs:
+            xq = synth.int8_codes((1, K), g).to(DEV)
+            s = synth.uniform((1,), 1e-3, 1e-1, g).to(DEV)
+            xs[key] = (xq, s)
+        xq, s = xs[key]
+        y = torch.empty(1, N, dtype=torch.float16, device=DEV)
+        keep += [Wq, sc, xq, s, y]
+        ops.append(dg.linear(dg.LINEAR_W4A8, Wq, 1, N, K, w_scale=sc, x_i8=xq, x_scale=s, y=y,
+                             group_size=grp))
+        cases.append((Wq, sc, xq, s, y, grp))
+    plan = dg.StepPlan(ops, keep)
+    ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=DEV)
+    for _ in range(2):  # the workspace is reused
+        dg.decode_step_weights(plan, ws)
+    sync()
+    dg.check_device_status()
+    for Wq, sc, xq, s, y, grp in cases:
+        ref = torch.empty_like(y)
+        dg.gemv_w4(Wq, sc, ref, x_i8=xq, x_scale=s, group_size=grp)
+        sync()
+        assert torch.equal(y, ref), tuple(Wq.shape)
+        yr, A, _ = oracle.gemv_w4a8(Wq.cpu().numpy(), bits(sc.cpu()), xq.cpu().numpy(),
+                                    s.cpu().numpy(), group=grp)
+        tol.assert_close(y.cpu().double().numpy(), yr, A, "f16", "given codes %s" % (tuple(Wq.shape),))
