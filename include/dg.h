@@ -187,8 +187,9 @@ dg_status dg_decode_step_weights(const dg_linear* ops, int n_ops, void* ws, size
 
 /* Workspace bytes that dg_decode_step_weights needs for these ops (256 for
  * the persistent kernel's barrier, plus 32 KB of argmax partials when an op is
- * an lm_head, plus, per DG_LINEAR_W4A8 op at M = 1, its activations in the
- * kernel's layout: ceil(K/1024)*1024 + K/8 bytes rounded up to 256); for a
+ * an lm_head, plus, per int4 op at M = 1, its activations in the kernel's
+ * layout: DG_LINEAR_W4A8 ceil(K/1024)*1024 + K/8 bytes, DG_LINEAR_W4A16
+ * ceil(K/1024)*4096 bytes, each rounded up to 256); for a
  * single lm_head this also covers dg_lm_head_argmax.
  * 0 for n_ops <= 0.  Host-only; touches no device. */
 size_t dg_workspace_bytes(const dg_linear* ops, int n_ops);

@@ -501,13 +501,13 @@ static bool run_writes_weights(const dg_linear* ops, int n) {
     return any_overlap(out, w);
 }
 
-// W4A8 step phases whose activations are ready before the launch (given
-// codes, or quantized once in its prologue) get a copy in the kernel's
-// interleaved layout plus the chunk sums, written by the prologue into the
-// workspace after the barrier words and argmax partials.
-static size_t w4a8_layout_bytes(int K) {
-    const size_t nch = (size_t)(K / 32);
-    const size_t bytes = ((nch + 31) / 32) * 32 * 32 + nch * 4;
+// int4 step phases whose activations are ready before the launch get a copy
+// in the kernel's interleaved layout, written by the launch's prologue into
+// the workspace after the barrier words and argmax partials: W4A8 int8 codes
+// (given, or quantized in the prologue) plus the chunk sums; W4A16 fp32.
+static size_t int4_layout_bytes(int kind, int K) {
+    const size_t nch = (size_t)(K / 32), padded = ((nch + 31) / 32) * 32;
+    const size_t bytes = kind == DG_LINEAR_W4A8 ? padded * 32 + nch * 4 : padded * 128;
     return (bytes + 255) & ~(size_t)255;
 }
 static size_t step_scratch_offset(const dg_linear* ops, int n) {
@@ -518,7 +518,8 @@ static size_t step_scratch_offset(const dg_linear* ops, int n) {
 static size_t step_scratch_bytes(const dg_linear* ops, int n) {
     size_t b = 0;
     for (int i = 0; i < n; ++i)
-        if (ops[i].kind == DG_LINEAR_W4A8 && ops[i].M == 1) b += w4a8_layout_bytes(ops[i].K);
+        if ((ops[i].kind == DG_LINEAR_W4A8 || ops[i].kind == DG_LINEAR_W4A16) && ops[i].M == 1)
+            b += int4_layout_bytes(ops[i].kind, ops[i].K);
     return b;
 }
 
@@ -609,9 +610,9 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
                 sp.prequant = 1;
             }
         }
-        // W4A8: activations ready before the launch are laid out once by the
+        // int4: activations ready before the launch are laid out once by the
         // prologue and read from the workspace (no per-phase staging)
-        if (f == F_W4A8) {
+        if (f == F_W4A8 || f == F_W4A16) {
             unsigned char* scratch = static_cast<unsigned char*>(ws) + step_scratch_offset(ops, n);
             size_t off = 0;
             for (int q = 0; q < sp.nphase; ++q) {
@@ -620,7 +621,7 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
                 if (!(ph.flags & kPhasePreQuant) && !given) continue;
                 ph.flags |= kPhaseXLaid;
                 ph.xlay = scratch + off;
-                off += w4a8_layout_bytes(ph.K);
+                off += int4_layout_bytes(ops[0].kind, ph.K);
                 sp.prequant = 1;
             }
         }

@@ -107,9 +107,9 @@ __device__ float quantize_token_smem(const __half* x, int K, int8_t* q, float* r
 // The launch's prologue.  CTA b takes the b-th, (b+G)-th, ... phase flagged
 // kPhasePreQuant or kPhaseXLaid (each distinct input once, not once per CTA):
 // a kPhasePreQuant input is quantized with the arithmetic of k_quant_act into
-// the phase's x_i8 / x_scale; a kPhaseXLaid phase's codes (just quantized, or
-// given) are then written in the format's layout to its xlay, from where every
-// CTA's MACs read them.
+// the phase's x_i8 / x_scale; a kPhaseXLaid phase's activations (W4A8: the
+// codes just quantized, or given; W4A16: the fp16 input) are then written in
+// the format's layout to its xlay, from where every CTA's MACs read them.
 template <class P>
 __device__ void prologue(const StepParams& sp, int8_t* qbuf, float* red) {
     int j = 0;
@@ -127,7 +127,7 @@ __device__ void prologue(const StepParams& sp, int8_t* qbuf, float* red) {
             codes = qbuf;
         }
         if (ph.flags & kPhaseXLaid) {
-            ActIn a{nullptr, codes, ph.x_scale, ph.K, 1};
+            ActIn a{ph.x, codes, ph.x_scale, ph.K, 1};  // W4A16 reads x, W4A8 the codes
             P::stage_x(a, ph.xlay, 1);
         }
         __syncthreads();
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     unsigned nbar = 0;  // grid barriers passed
     plan_phases(sp, table, b, G, [](const StepPhase&, int n) { return (n + R - 1) / R; });
 
-    if constexpr (P::kIntAct) {
+    if constexpr (!P::kDirectX) {
         if (sp.prequant) {
             prologue<P>(sp, qraw, fred);
             ++nbar;
@@ -225,13 +225,13 @@ __global__ void __launch_bounds__(NW * 32, 1)
         float sx = 1.f;
         unsigned char* xs = xs_fmt;
         bool laid = false;
-        if constexpr (P::kIntAct) laid = (ph.flags & kPhaseXLaid) != 0;
+        if constexpr (!P::kDirectX) laid = (ph.flags & kPhaseXLaid) != 0;
         if (laid) {
             // laid out by the prologue: read from global memory in the MACs (the
             // prologue's writes are not in this SM's L1), no staging and no
             // CTA-wide meeting between phases
             xs = ph.xlay;
-            sx = __ldcg(ph.x_scale);
+            if constexpr (P::kIntAct) sx = __ldcg(ph.x_scale);
         } else if constexpr (!P::kDirectX) {
             // activations of this phase: raw bytes in rawx[p & 1] (copied ahead
             // during the previous phase when no barrier separates them), then

@@ -294,3 +294,37 @@ def test_w4a8_step_with_given_codes_reads_the_prologue_layout():
         yr, A, _ = oracle.gemv_w4a8(Wq.cpu().numpy(), bits(sc.cpu()), xq.cpu().numpy(),
                                     s.cpu().numpy(), group=grp)
         tol.assert_close(y.cpu().double().numpy(), yr, A, "f16", "given codes %s" % (tuple(Wq.shape),))
+
+
+def test_int4_step_mixing_laid_out_and_staged_activations_matches_sequential_calls():
+    """W4A16 ops: y1 = W1 x0 (x0 read-only: laid out by the prologue),
+    y2 = W2 y1 (y1 written in the launch: staged in shared memory after a
+    grid barrier), y3 = W3 x3 (laid out again); equal to the calls in order."""
+    need_gpu()
+    g = synth.generator(23)
+    K0, N1, N2, N3 = 2048, 4096, 1024, 3072
+    W1, W2, W3 = (synth.int4_packed(N, K, g).to(DEV) for N, K in ((N1, K0), (N2, N1), (N3, K0)))
+    S1, S2, S3 = (synth.uniform((N, K // 32), 1e-3, 1e-2, g, torch.float16).to(DEV)
+                  for N, K in ((N1, K0), (N2, N1), (N3, K0)))
+    x0 = synth.normal((1, K0), 1.0, g).to(DEV)
+    x3 = synth.normal((1, K0), 1.0, g).to(DEV)
+    y1 = torch.empty(1, N1, dtype=torch.float16, device=DEV)
+    y2 = torch.empty(1, N2, dtype=torch.float16, device=DEV)
+    y3 = torch.empty(1, N3, dtype=torch.float16, device=DEV)
+    ops = [dg.linear(dg.LINEAR_W4A16, W1, 1, N1, K0, w_scale=S1, x=x0, y=y1),
+           dg.linear(dg.LINEAR_W4A16, W2, 1, N2, N1, w_scale=S2, x=y1, y=y2),
+           dg.linear(dg.LINEAR_W4A16, W3, 1, N3, K0, w_scale=S3, x=x3, y=y3)]
+    plan = dg.StepPlan(ops, [W1, W2, W3, S1, S2, S3, x0, x3, y1, y2, y3])
+    ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=DEV)
+    dg.decode_step_weights(plan, ws)
+    sync()
+    dg.check_device_status()
+    r1, r2, r3 = torch.empty_like(y1), torch.empty_like(y2), torch.empty_like(y3)
+    dg.gemv_w4(W1, S1, r1, x_f16=x0)
+    dg.gemv_w4(W2, S2, r2, x_f16=r1)
+    dg.gemv_w4(W3, S3, r3, x_f16=x3)
+    sync()
+    for a, b in ((y1, r1), (y2, r2), (y3, r3)):
+        assert torch.equal(a, b)
+    yr, A = oracle.gemv_w4a16(W2.cpu().numpy(), bits(S2.cpu()), bits(r1.cpu()))
+    tol.assert_close(y2.cpu().double().numpy(), yr, A, "f16", "chained W4A16")
