@@ -365,11 +365,31 @@ def time_graph(g, stream, n, torch):
     return e0.elapsed_time(e1) / 1e3  # seconds
 
 
+def step_percentiles(g, stream, n, torch):
+    """Per-step device time of n graph replays, each between its own pair of
+    events on the launching stream: (median, p10, p90) in microseconds."""
+    import statistics
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+    torch.cuda.synchronize()
+    us = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
+    q = statistics.quantiles(us, n=10, method="inclusive")
+    return {"median": round(statistics.median(us), 3), "p10": round(q[0], 3),
+            "p90": round(q[-1], 3), "samples": n}
+
+
 # ---- CPU oracle (baseline / reference arm) ------------------------------------------
 
-def oracle_sample(w, budget_s):
+def oracle_sample(w, budget_s, nthreads=0):
     """Times the oracle on whole matrices of the workload until budget_s has
-    passed.  Returns (weight bytes done, seconds, description)."""
+    passed, on nthreads host threads (0: all cores).  Returns (weight bytes
+    done, seconds, description)."""
     import numpy as np
     import oracle
     kind, data = w.cpu_sample
@@ -382,7 +402,7 @@ def oracle_sample(w, budget_s):
     if kind == "fp":
         for L in data:
             for lin in L.linears:
-                oracle.gemv_fp(bits(lin.W), bits(L.inputs[lin.x_name]))
+                oracle.gemv_fp(bits(lin.W), bits(L.inputs[lin.x_name]), nthreads=nthreads)
                 done += lin.W.numel() * 2
                 mats += 1
                 if time.perf_counter() - t0 > budget_s:
@@ -396,10 +416,10 @@ def oracle_sample(w, budget_s):
             for lin in L.linears:
                 x = L.inputs[lin.x_name]
                 if kind == "w4a16":
-                    oracle.gemv_w4a16(lin.W.numpy(), bits(lin.scales), bits(x))
+                    oracle.gemv_w4a16(lin.W.numpy(), bits(lin.scales), bits(x), nthreads=nthreads)
                 else:
                     q, s = oracle.quant_act(bits(x))
-                    oracle.gemv_w4a8(lin.W.numpy(), bits(lin.scales), q, s)
+                    oracle.gemv_w4a8(lin.W.numpy(), bits(lin.scales), q, s, nthreads=nthreads)
                 done += lin.W.numel() + lin.scales.numel() * 2
                 mats += 1
                 if time.perf_counter() - t0 > budget_s:
@@ -412,7 +432,7 @@ def oracle_sample(w, budget_s):
         W, s_w, x = data
         q, sx = orc.quant_act(bits(x))
         while True:
-            orc.gemv_w8a8(W.numpy(), s_w.numpy(), q, sx)
+            orc.gemv_w8a8(W.numpy(), s_w.numpy(), q, sx, nthreads=nthreads)
             done += W.numel() + s_w.numel() * 4
             mats += 1
             if time.perf_counter() - t0 > budget_s:
@@ -521,6 +541,7 @@ def main():
     nrep = max(20, args.steps // 10)
     dsecs = time_graph(gd, s, nrep, torch)
     d_launch_s = dsecs / (nrep * dlaunch)
+    pct = step_percentiles(g, s, min(200, max(args.steps, 10)), torch)
     clk = clocks.stop()
 
     # end to end through the public API with host buffers
@@ -551,6 +572,7 @@ def main():
                      "us_per_launch": round(d_launch_s * 1e6, 3),
                      "bytes_per_launch": dbytes,
                      "traffic": recorded_traffic(dname)},
+        "step_us": pct,
         "clocks": clk,
         "e2e": e2e,
     }
@@ -561,6 +583,10 @@ def main():
             out["cpu_baseline"] = {"value": round(done / cs / 1e9, 4), "unit": "GB/s",
                                    "cores": os.cpu_count(), "kind": "oracle",
                                    "sample": desc + " (%.1f s)" % cs}
+            if args.cpu_budget > 0:  # the same oracle on one core
+                d1, c1, desc1 = oracle_sample(w, args.cpu_budget / 3, nthreads=1)
+                out["cpu_baseline"]["one_core"] = {"value": round(d1 / c1 / 1e9, 4),
+                                                   "sample": desc1 + " (%.1f s)" % c1}
         print(json.dumps(out), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -33,7 +33,12 @@
  *  - Determinism.  Each output is summed in a fixed order that depends only on
  *    K and the element format (never on N, M, the row offset or the launch
  *    grid), so repeated calls are bitwise identical and a row slice of W gives
- *    bitwise the same rows as the whole matrix.
+ *    bitwise the same rows as the whole matrix.  One exception, opt-in: a
+ *    per-op call (dg_gemv_*) with few rows (its row groups would fill fewer
+ *    than half the SMs) that is given workspace splits K across CTAs (split-K:
+ *    S fixed K ranges, partial sums in ws, a second kernel adding them in range
+ *    order); its order then also depends on N, M and the SM count, and is still
+ *    the same on every call.  Integer (W8A8) sums are exact either way.
  *  - Alignment.  W, x, xq and y must be 16-byte aligned; K must be a multiple
  *    of 8 (fp16/bf16), 16 (int8) or 32 (int4).
  */
@@ -97,7 +102,10 @@ typedef struct {
  * W [N][K], x [M][K], y [M][N], all of type t; 1 <= M <= 16 and M * K * 4
  * bytes within the shared memory of one CTA (DG_ERR_UNSUPPORTED otherwise).
  * Products are exact in fp32 and summed in fp32; y = round-to-nearest-even of
- * the fp32 sum.  ws may be NULL (this call needs no workspace). */
+ * the fp32 sum.  ws may be NULL.  With ws (16-byte aligned) of at least
+ * dg_workspace_bytes(&op, 1) bytes for the equivalent dg_linear, a call with
+ * few rows may split K across CTAs (see Determinism above); with less, or
+ * NULL, it does not.  The same holds for dg_gemv_w8a8 and dg_gemv_w4. */
 dg_status dg_gemv_f16(const void* W, const void* x, void* y, dg_ftype t, int M, int N, int K,
                       void* ws, size_t ws_bytes, dg_stream stream);
 
@@ -190,7 +198,9 @@ dg_status dg_decode_step_weights(const dg_linear* ops, int n_ops, void* ws, size
  * an lm_head, plus, per int4 op at M = 1, its activations in the kernel's
  * layout: DG_LINEAR_W4A8 ceil(K/1024)*1024 + K/8 bytes, DG_LINEAR_W4A16
  * ceil(K/1024)*4096 bytes, each rounded up to 256); for a
- * single lm_head this also covers dg_lm_head_argmax.
+ * single lm_head this also covers dg_lm_head_argmax; for a single op of at
+ * most 65536 outputs (M * N) it also covers split-K partials of a dg_gemv_*
+ * call (8 ranges x M x N x 4 bytes).
  * 0 for n_ops <= 0.  Host-only; touches no device. */
 size_t dg_workspace_bytes(const dg_linear* ops, int n_ops);
 

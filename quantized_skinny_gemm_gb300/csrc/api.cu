@@ -74,6 +74,7 @@ int* device_error_word() {
 struct Tune {
     int R = 0, KS = 0, CPS = 0, PF = -1, PDL = -1, STEP = -1, SPIN = -1, SNW = 0, MMA = -1;
     int RING = -1, TSB = 0, TNS = 0, TNC = 0;  // weight ring: on/off, KB per stage, stages, consumers
+    int KP = 0;                                // split-K ranges of a per-op launch (1 = off)
 };
 
 static Tune read_tune() {
@@ -98,6 +99,7 @@ static Tune read_tune() {
         else if (std::sscanf(tok, "TSB=%d", &v) == 1) t.TSB = v;
         else if (std::sscanf(tok, "TNS=%d", &v) == 1) t.TNS = v;
         else if (std::sscanf(tok, "TNC=%d", &v) == 1) t.TNC = v;
+        else if (std::sscanf(tok, "KP=%d", &v) == 1) t.KP = v;
     }
     return t;
 }
@@ -332,8 +334,41 @@ static dg_status launch_i8_mma(GemvParams& p, cudaStream_t s) {
     return to_status(gemv_i8_mma(&p, p.a.K, need < maxg ? need : maxg, s, nullptr));
 }
 
-// Launches ops[0..n) (same kind, same activations) as one kernel.
-static dg_status launch_group(const dg_linear* ops, int n, cudaStream_t s) {
+// Split-K across CTAs for a launch whose row groups would fill fewer than
+// half of the SMs (k or v alone, a few hundred rows): K is cut into S ranges
+// of each lane's chunk sequence (at most 8, at least two chunks per lane
+// each), CTAs write fp32 / int32 partials to the workspace and a second kernel
+// adds them in range order.  S follows the op's shape and the SM count.
+static int pick_kparts(const GemvLaunch& L, int N, int K) {
+    const int ks = pick_ks(L.fmt, K), slots = kWarps / ks;
+    const int n_rg = (N + L.R - 1) / L.R, need = (n_rg + slots - 1) / slots;
+    const int kelems = (L.fmt == F_F16 || L.fmt == F_BF16) ? 8 : L.fmt == F_I8 ? 16 : 32;
+    const int J = (K / kelems + ks * 32 - 1) / (ks * 32);  // chunks per lane
+    int S = tune().KP;
+    if (S <= 0) {
+        const int sms = sm_count();
+        if (need * 2 > sms) return 1;
+        S = sms / need;
+        if (S > 8) S = 8;
+        if (S > J / 2) S = J / 2;
+    }
+    if (S > J) S = J;
+    return S >= 2 ? S : 1;
+}
+
+// Workspace a per-op launch may use for split-K partials: 8 ranges of M x N
+// 4-byte sums, for launches small enough to split (device-independent).
+static size_t split_ws_bytes(const dg_linear& op) {
+    if (op.token) return 0;
+    const size_t outs = (size_t)op.M * (size_t)op.N;
+    if (outs > 65536) return 0;
+    return (8 * outs * 4 + 255) & ~(size_t)255;
+}
+
+// Launches ops[0..n) (same kind, same activations) as one kernel (two with
+// split-K, when ws holds the partials).
+static dg_status launch_group(const dg_linear* ops, int n, cudaStream_t s, void* ws = nullptr,
+                              size_t ws_bytes = 0) {
     GemvParams p;
     fill_common(p, ops[0]);
     int rows = 0;
@@ -353,6 +388,15 @@ static dg_status launch_group(const dg_linear* ops, int n, cudaStream_t s) {
     GemvLaunch L{fmt_of(ops[0].kind), pick_mt(ops[0].M), 0, false, ops[0].K, p.group, 0};
     L.R = pick_r(L.fmt, L.MT);
     configure(L, p);
+    if (ws && al16(ws)) {
+        const int S = pick_kparts(L, p.t.N, p.a.K);
+        if (S > 1 && ws_bytes >= (size_t)S * p.a.M * p.t.N * 4) {
+            p.kparts = S;
+            p.kpart = ws;
+            p.prefetch_bytes = 0;
+            L.grid *= S;  // configure gave one pass (grid = row-group blocks)
+        }
+    }
     return to_status(family(L, &p, s, nullptr));
 }
 
@@ -705,13 +749,13 @@ const char* dg_version(void) { return "dg 0.1 (sm_103a)"; }
 
 size_t dg_workspace_bytes(const dg_linear* ops, int n_ops) {
     if (!ops || n_ops <= 0) return 0;
-    return step_scratch_offset(ops, n_ops) + step_scratch_bytes(ops, n_ops);
+    size_t need = step_scratch_offset(ops, n_ops) + step_scratch_bytes(ops, n_ops);
+    for (int i = 0; i < n_ops; ++i) need = std::max(need, split_ws_bytes(ops[i]));
+    return need;
 }
 
 dg_status dg_gemv_f16(const void* W, const void* x, void* y, dg_ftype t, int M, int N, int K,
                       void* ws, size_t ws_bytes, dg_stream stream) {
-    (void)ws;
-    (void)ws_bytes;
     if (t != DG_F16 && t != DG_BF16) return DG_ERR_INVALID_ARG;
     dg_linear op;
     std::memset(&op, 0, sizeof op);
@@ -725,14 +769,12 @@ dg_status dg_gemv_f16(const void* W, const void* x, void* y, dg_ftype t, int M, 
     dg_status st = validate(op, false);
     if (st != DG_OK) return st;
     if ((st = check_smem(op)) != DG_OK) return st;
-    return launch_group(&op, 1, stream);
+    return launch_group(&op, 1, stream, ws, ws_bytes);
 }
 
 dg_status dg_gemv_w8a8(const int8_t* W, const float* w_scale, const int8_t* x, const float* x_scale,
                        void* y, int32_t* acc_out, int M, int N, int K, void* ws, size_t ws_bytes,
                        dg_stream stream) {
-    (void)ws;
-    (void)ws_bytes;
     dg_linear op;
     std::memset(&op, 0, sizeof op);
     op.kind = DG_LINEAR_W8A8;
@@ -748,14 +790,12 @@ dg_status dg_gemv_w8a8(const int8_t* W, const float* w_scale, const int8_t* x, c
     dg_status st = validate(op, false);
     if (st != DG_OK) return st;
     if ((st = check_smem(op)) != DG_OK) return st;
-    return launch_group(&op, 1, stream);
+    return launch_group(&op, 1, stream, ws, ws_bytes);
 }
 
 dg_status dg_gemv_w4(const uint8_t* Wq, const void* scales, int group_size, const void* x_f16,
                      const int8_t* x_i8, const float* x_scale, void* y, int M, int N, int K,
                      void* ws, size_t ws_bytes, dg_stream stream) {
-    (void)ws;
-    (void)ws_bytes;
     dg_linear op;
     std::memset(&op, 0, sizeof op);
     op.kind = x_i8 ? DG_LINEAR_W4A8 : DG_LINEAR_W4A16;
@@ -772,7 +812,7 @@ dg_status dg_gemv_w4(const uint8_t* Wq, const void* scales, int group_size, cons
     dg_status st = validate(op, false);
     if (st != DG_OK) return st;
     if ((st = check_smem(op)) != DG_OK) return st;
-    return launch_group(&op, 1, stream);
+    return launch_group(&op, 1, stream, ws, ws_bytes);
 }
 
 dg_status dg_quantize_act_i8(const void* x, int8_t* xq, float* x_scale, int M, int K,

@@ -60,6 +60,8 @@ struct GemvParams {
     int prefetch_bytes;      // per-CTA L2 prefetch issued before the dependency wait
     float* logits;           // lm_head: fp32 [N]
     ArgPart* part;           // lm_head: one partial per CTA
+    int kparts;              // split-K across CTAs: K ranges (1 = none)
+    void* kpart;             //   partial sums [kparts][M][N] (fp32 or int32 bits)
 };
 
 // ---- the persistent decode-step kernel's work list --------------------------------

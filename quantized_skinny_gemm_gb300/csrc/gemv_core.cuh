@@ -481,10 +481,13 @@ __device__ __forceinline__ void rows_of(const SegTable& t, int rg, bool active, 
 // active = false.
 // DX: one token, activations read from global memory at `xs` (coherent:
 // bypassing L1); otherwise `xs` is the staged shared-memory copy.
+// [cbeg, cend): the row's chunks to visit (a multiple of ks * 32 and the
+// row's end by default; split-K launches give each CTA one such range).
 template <class P, int MT, int R, bool DX = false>
 __device__ __forceinline__ void row_group(const RowRef (&rows)[R], bool active, const RowGeom& g,
                                           const unsigned char* xs, int* red,
-                                          typename P::Acc (&acc)[R][MT], bool coherent = false) {
+                                          typename P::Acc (&acc)[R][MT], bool coherent = false,
+                                          int cbeg = 0, int cend = -1) {
     using Acc = typename P::Acc;
     constexpr int U = Unroll<MT, R>::v;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -500,11 +503,12 @@ __device__ __forceinline__ void row_group(const RowRef (&rows)[R], bool active, 
         // use (chunks past the row's end are skipped), so a short row costs one
         // memory round trip; the sums still run in ascending chunk order.
         const int step = ks * 32;
-        for (int c = kw * 32 + lane; c < g.nchunks; c += U * step) {
+        const int ce = cend < 0 ? g.nchunks : cend;
+        for (int c = cbeg + kw * 32 + lane; c < ce; c += U * step) {
             typename P::Chunk ch[U][R];
 #pragma unroll
             for (int u = 0; u < U; ++u)
-                if (c + u * step < g.nchunks)
+                if (c + u * step < ce)
 #pragma unroll
                     for (int r = 0; r < R; ++r) P::load(ch[u][r], rows[r], c + u * step, g.gk, g.cpg);
             if constexpr (DX) {
@@ -512,9 +516,9 @@ __device__ __forceinline__ void row_group(const RowRef (&rows)[R], bool active, 
                 uint4 xn = P::load_x(xs, c, coherent);
 #pragma unroll
                 for (int u = 0; u < U; ++u)
-                    if (c + u * step < g.nchunks) {
+                    if (c + u * step < ce) {
                         const uint4 xv = xn;
-                        if (u + 1 < U && c + (u + 1) * step < g.nchunks)
+                        if (u + 1 < U && c + (u + 1) * step < ce)
                             xn = P::load_x(xs, c + (u + 1) * step, coherent);
 #pragma unroll
                         for (int r = 0; r < R; ++r) P::mac_direct(acc[r], ch[u][r], xv);
@@ -522,7 +526,7 @@ __device__ __forceinline__ void row_group(const RowRef (&rows)[R], bool active, 
             } else {
 #pragma unroll
                 for (int u = 0; u < U; ++u)
-                    if (c + u * step < g.nchunks)
+                    if (c + u * step < ce)
 #pragma unroll
                         for (int r = 0; r < R; ++r)
                             P::template mac<MT>(acc[r], ch[u][r], xs, c + u * step, g.K);
@@ -570,10 +574,20 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvP
     const int slot = warp / ks, kw = warp - slot * ks;
     const RowGeom g = row_geom<P>(p.a.K, p.group, ks);
     const int n_rg = (p.t.N + R - 1) / R;
+    // split-K across CTAs: CTA (sidx, bx) takes K range sidx of row groups bx,
+    // bx + gx, ...: the lane chunk indices j in [J sidx / S, J (sidx + 1) / S)
+    const int S = p.kparts > 1 ? p.kparts : 1;
+    const int gx = (int)gridDim.x / S, sidx = (int)blockIdx.x / gx, bx = (int)blockIdx.x - sidx * gx;
+    int cbeg = 0, cend = -1;
+    if (S > 1) {
+        const int stepc = ks * 32, J = (g.nchunks + stepc - 1) / stepc;
+        cbeg = (int)((long long)J * sidx / S) * stepc;
+        cend = min(g.nchunks, (int)((long long)J * (sidx + 1) / S) * stepc);
+    }
 
     // Weights do not depend on the previous kernel: warm L2 with the rows this
     // CTA streams first while that kernel drains.
-    if (p.prefetch_bytes > 0 && threadIdx.x < slots * R) {
+    if (p.prefetch_bytes > 0 && S == 1 && threadIdx.x < slots * R) {
         const int r = blockIdx.x * slots * R + threadIdx.x;
         RowRef z{};
         const RowRef rr = locate(p.t, r, g.rb, z);
@@ -599,12 +613,12 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvP
     int best_i = INT_MAX;
 
     for (int it = 0; it < p.iters; ++it) {
-        const int rg = (it * (int)gridDim.x + (int)blockIdx.x) * slots + slot;
+        const int rg = (it * gx + bx) * slots + slot;
         const bool active = rg < n_rg;
         RowRef rows[R];
         rows_of<R>(p.t, rg, active, g.rb, rows);
         Acc acc[R][MT];
-        row_group<P, MT, R, DX>(rows, active, g, xsrc, red, acc);
+        row_group<P, MT, R, DX>(rows, active, g, xsrc, red, acc, false, cbeg, cend);
 
         if (kw == 0 && active) {
 #pragma unroll
@@ -624,8 +638,13 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvP
 #pragma unroll
                     for (int m = 0; m < MT; ++m)
                         if (m < p.a.M && lane == ((r * MT + m) & 31)) {
-                            const float sx = p.a.x_scale ? __ldg(p.a.x_scale + m) : 1.f;
-                            P::store(rows[r], m, acc[r][m], sx);
+                            if (S > 1) {  // this K range's partial sum, for pass 2
+                                static_cast<int*>(p.kpart)[((size_t)sidx * p.a.M + m) * p.t.N +
+                                                           rows[r].global] = to_bits(acc[r][m]);
+                            } else {
+                                const float sx = p.a.x_scale ? __ldg(p.a.x_scale + m) : 1.f;
+                                P::store(rows[r], m, acc[r][m], sx);
+                            }
                         }
                 }
             }
@@ -650,6 +669,27 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvP
             p.part[blockIdx.x].v = bv;
             p.part[blockIdx.x].i = bi;
         }
+    }
+}
+
+// Split-K pass 2: adds each output's K-range partials in range order and
+// applies the format's epilogue, one thread per output.  int32 partials
+// (W8A8) add exactly, so those outputs equal the unsplit ones bit for bit.
+template <class P>
+__global__ void __launch_bounds__(256) k_split_finish(const __grid_constant__ GemvParams p) {
+    using Acc = typename P::Acc;
+    griddep_launch_dependents();
+    griddep_wait();
+    const int N = p.t.N, M = p.a.M, S = p.kparts;
+    const int* part = static_cast<const int*>(p.kpart);
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < M * N; i += gridDim.x * blockDim.x) {
+        const int m = i / N, row = i - m * N;
+        Acc acc = from_bits<Acc>(part[(size_t)m * N + row]);
+        for (int s = 1; s < S; ++s) acc += from_bits<Acc>(part[((size_t)s * M + m) * N + row]);
+        RowRef z{};
+        const RowRef rr = locate(p.t, row, 0, z);
+        const float sx = p.a.x_scale ? __ldg(p.a.x_scale + m) : 1.f;
+        P::store(rr, m, acc, sx);
     }
 }
 
@@ -687,7 +727,7 @@ cudaError_t run_r(int R, const GemvParams* p, int grid, size_t smem, cudaStream_
 
 // The instantiations the launch heuristic can pick.
 template <class P>
-cudaError_t run_family(const GemvLaunch& L, const GemvParams* p, cudaStream_t s, int* occ) {
+cudaError_t run_family_main(const GemvLaunch& L, const GemvParams* p, cudaStream_t s, int* occ) {
     const size_t smem = smem_bytes_for<P>(L.MT, L.K);
     if (L.argmax) {
         if constexpr (P::kIntAct && P::kElems == 16) {
@@ -711,6 +751,17 @@ cudaError_t run_family(const GemvLaunch& L, const GemvParams* p, cudaStream_t s,
             return run_one<P, 16, 1, false>(p, L.grid, smem, s, occ);
         default: return cudaErrorInvalidValue;
     }
+}
+
+// Launches the main kernel, and with split-K its pass 2 behind it.
+template <class P>
+cudaError_t run_family(const GemvLaunch& L, const GemvParams* p, cudaStream_t s, int* occ) {
+    cudaError_t e = run_family_main<P>(L, p, s, occ);
+    if (e != cudaSuccess || occ || !p || p->kparts <= 1 || L.argmax) return e;
+    const int total = p->a.M * p->t.N;
+    void* args[] = {const_cast<GemvParams*>(p)};
+    return launch_pdl(reinterpret_cast<const void*>(k_split_finish<P>), dim3((total + 255) / 256),
+                      dim3(256), 0, s, args);
 }
 
 }  // namespace dg

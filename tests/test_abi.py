@@ -111,6 +111,16 @@ def test_lm_head_validation_and_workspace(lib):
     assert dg.workspace_bytes([plain]) == 256  # the persistent step's barrier words
 
 
+def test_workspace_covers_split_k_partials_of_small_ops():
+    # a per-op call with at most 65536 outputs may split K into up to 8 ranges
+    # of M x N fp32 / int32 partials; larger ones never split
+    f16 = lambda N, M=1: dg.Linear(kind=dg.LINEAR_F16, M=M, N=N, K=1536, W=A, x=A, y=B)
+    assert dg.workspace_bytes([f16(256)]) == 8 * 256 * 4
+    assert dg.workspace_bytes([f16(1000, M=4)]) == 8 * 4000 * 4
+    assert dg.workspace_bytes([f16(65536)]) == 8 * 65536 * 4
+    assert dg.workspace_bytes([f16(65537)]) == 256
+
+
 def test_workspace_holds_the_w4a8_activation_layouts():
     # per W4A8 op at M = 1: ceil(K/32/32)*32 chunks x 32 bytes of interleaved
     # codes + K/32 int32 chunk sums, rounded up to 256 bytes, after the
@@ -125,7 +135,8 @@ def test_workspace_holds_the_w4a8_activation_layouts():
     assert dg.workspace_bytes([w4a8(14336), w4a8(4096)]) == 256 + (14336 + 1792) + 4608
     head_ws = dg.workspace_bytes([_head()])
     assert dg.workspace_bytes([w4a8(4096), _head()]) == head_ws + 4608
-    assert dg.workspace_bytes([w4a8(4096, M=2)]) == 256  # M > 1 runs per group
+    # M > 1 runs per group: no layout; the split-K bound 8 x M x N x 4 = 512
+    assert dg.workspace_bytes([w4a8(4096, M=2)]) == 512
     # W4A16: the fp32 interleaved activations, 128 bytes per 32-code chunk
     assert dg.workspace_bytes([w4a8(4096, kind=dg.LINEAR_W4A16, x=A, x_i8=None,
                                     x_scale=None)]) == 256 + 128 * 128
