@@ -302,21 +302,24 @@ static bool use_i8_mma(const dg_linear& op) {
     return gemv_i8_mma_smem(op.K) <= smem_optin_limit();
 }
 
+// The tile runs on the fp16 tensor path (exact, see gemv_i8_mma.cu) unless
+// DG_TUNE=MMA=1 selects the int8 one.
 static dg_status launch_i8_mma(GemvParams& p, cudaStream_t s) {
     static std::mutex mu;
-    static std::map<std::pair<int, int>, int> cache;
+    static std::map<std::tuple<int, int, int>, int> cache;
+    const bool f16 = tune().MMA != 1;
     int dev = 0;
     cudaGetDevice(&dev);
     int occ = 0;
     {
         std::lock_guard<std::mutex> g(mu);
-        auto it = cache.find({dev, p.a.K});
+        auto it = cache.find({dev, p.a.K, (int)f16});
         if (it != cache.end()) occ = it->second;
     }
     if (!occ) {
-        if (gemv_i8_mma(nullptr, p.a.K, 0, nullptr, &occ) != cudaSuccess || occ < 1) occ = 1;
+        if (gemv_i8_mma(nullptr, p.a.K, 0, nullptr, &occ, f16) != cudaSuccess || occ < 1) occ = 1;
         std::lock_guard<std::mutex> g(mu);
-        cache[{dev, p.a.K}] = occ;
+        cache[{dev, p.a.K, (int)f16}] = occ;
     }
     // split K over ks warps per 16-row tile (ks | K / 64) until the GPU has
     // about four warps per SM sub-partition to stream with
@@ -331,7 +334,7 @@ static dg_status launch_i8_mma(GemvParams& p, cudaStream_t s) {
     const int need = (tiles + per_cta - 1) / per_cta;
     int maxg = sm_count() * occ;
     if (maxg < 1) maxg = 1;
-    return to_status(gemv_i8_mma(&p, p.a.K, need < maxg ? need : maxg, s, nullptr));
+    return to_status(gemv_i8_mma(&p, p.a.K, need < maxg ? need : maxg, s, nullptr, f16));
 }
 
 // Split-K across CTAs for a launch whose row groups would fill fewer than

@@ -299,7 +299,7 @@ cudaError_t gemv_w4a16(const GemvLaunch& L, const GemvParams* p, cudaStream_t s,
 cudaError_t gemv_w4a8(const GemvLaunch& L, const GemvParams* p, cudaStream_t s, int* occ);
 size_t gemv_smem(Fmt f, int MT, int K, int group);
 // W8A8 for 8..16 tokens on the tensor cores (mma.sync s8, exact int32).
-cudaError_t gemv_i8_mma(const GemvParams* p, int K, int grid, cudaStream_t s, int* occ);
+cudaError_t gemv_i8_mma(const GemvParams* p, int K, int grid, cudaStream_t s, int* occ, bool f16);
 size_t gemv_i8_mma_smem(int K);
 
 // Host helpers of api.cu shared with the static-scratch lm_head entry point.
