@@ -483,13 +483,13 @@ __device__ __forceinline__ void rows_of(const SegTable& t, int rg, bool active, 
 // bypassing L1); otherwise `xs` is the staged shared-memory copy.
 // [cbeg, cend): the row's chunks to visit (a multiple of ks * 32 and the
 // row's end by default; split-K launches give each CTA one such range).
-template <class P, int MT, int R, bool DX = false>
+template <class P, int MT, int R, bool DX = false, int UOVR = 0>
 __device__ __forceinline__ void row_group(const RowRef (&rows)[R], bool active, const RowGeom& g,
                                           const unsigned char* xs, int* red,
                                           typename P::Acc (&acc)[R][MT], bool coherent = false,
                                           int cbeg = 0, int cend = -1) {
     using Acc = typename P::Acc;
-    constexpr int U = Unroll<MT, R>::v;
+    constexpr int U = UOVR > 0 ? UOVR : Unroll<MT, R>::v;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int ks = g.ks;
     const int kw = warp % ks;
@@ -563,7 +563,9 @@ __device__ __forceinline__ void row_group(const RowRef (&rows)[R], bool active, 
 
 // ---- the per-launch kernel ---------------------------------------------------------
 
-template <class P, int MT, int R, bool ARGMAX>
+// SPLIT: a split-K launch (grid = row-group blocks x p.kparts K ranges); the
+// unsplit instantiation carries none of its bookkeeping.
+template <class P, int MT, int R, bool ARGMAX, bool SPLIT>
 __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     using Acc = typename P::Acc;
@@ -576,10 +578,12 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvP
     const int n_rg = (p.t.N + R - 1) / R;
     // split-K across CTAs: CTA (sidx, bx) takes K range sidx of row groups bx,
     // bx + gx, ...: the lane chunk indices j in [J sidx / S, J (sidx + 1) / S)
-    const int S = p.kparts > 1 ? p.kparts : 1;
-    const int gx = (int)gridDim.x / S, sidx = (int)blockIdx.x / gx, bx = (int)blockIdx.x - sidx * gx;
+    const int S = SPLIT ? p.kparts : 1;
+    const int gx = SPLIT ? (int)gridDim.x / S : (int)gridDim.x;
+    const int sidx = SPLIT ? (int)blockIdx.x / gx : 0;
+    const int bx = (int)blockIdx.x - sidx * gx;
     int cbeg = 0, cend = -1;
-    if (S > 1) {
+    if constexpr (SPLIT) {
         const int stepc = ks * 32, J = (g.nchunks + stepc - 1) / stepc;
         cbeg = (int)((long long)J * sidx / S) * stepc;
         cend = min(g.nchunks, (int)((long long)J * (sidx + 1) / S) * stepc);
@@ -587,7 +591,7 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvP
 
     // Weights do not depend on the previous kernel: warm L2 with the rows this
     // CTA streams first while that kernel drains.
-    if (p.prefetch_bytes > 0 && S == 1 && threadIdx.x < slots * R) {
+    if (!SPLIT && p.prefetch_bytes > 0 && threadIdx.x < slots * R) {
         const int r = blockIdx.x * slots * R + threadIdx.x;
         RowRef z{};
         const RowRef rr = locate(p.t, r, g.rb, z);
@@ -638,7 +642,7 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvP
 #pragma unroll
                     for (int m = 0; m < MT; ++m)
                         if (m < p.a.M && lane == ((r * MT + m) & 31)) {
-                            if (S > 1) {  // this K range's partial sum, for pass 2
+                            if constexpr (SPLIT) {  // this K range's partial sum, for pass 2
                                 static_cast<int*>(p.kpart)[((size_t)sidx * p.a.M + m) * p.t.N +
                                                            rows[r].global] = to_bits(acc[r][m]);
                             } else {
@@ -704,7 +708,8 @@ size_t smem_bytes_for(int MT, int K) {
 // fit on one SM with this much dynamic shared memory.
 template <class P, int MT, int R, bool ARGMAX>
 cudaError_t run_one(const GemvParams* p, int grid, size_t smem, cudaStream_t s, int* occ) {
-    auto fn = k_gemv<P, MT, R, ARGMAX>;
+    const bool split = !ARGMAX && p && p->kparts > 1;
+    auto fn = split ? k_gemv<P, MT, R, ARGMAX, !ARGMAX> : k_gemv<P, MT, R, ARGMAX, false>;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
