@@ -172,10 +172,8 @@ def build_workload(name, dev, torch):
         w.unit_bytes = st.weight_bytes
         w.launches = st.n_launches
         w.run = lambda: dg.decode_step_weights(st.plan, st.ws, stream=s)
-        w.config = {"workload": "decode-step weight stream, 28-layer 1536-wide fp16 decoder "
-                                "(Qwen2.5-1.5B shape), 196 matrices, M=1",
-                    "weight_bytes_per_step": st.weight_bytes,
-                    "l2": "inputs 2.62 GB > 126 MB L2 (no flush)"}
+        w.config = workload_config(name)
+        assert w.config["weight_bytes_per_step"] == st.weight_bytes
         # the step runs as one persistent kernel launch: that launch dominates
         w.dominant = ("k_step<fp16> (persistent decode-step kernel, 28 layers)", w.run, 1,
                       st.weight_bytes)
@@ -192,13 +190,8 @@ def build_workload(name, dev, torch):
         w.unit_bytes = st.weight_bytes
         w.launches = st.n_launches
         w.run = lambda: dg.decode_step_weights(st.plan, st.ws, stream=s)
-        w.config = {"workload": ("decode-step weight stream, 4 layers of the 4096-wide int4 g32 "
-                                 "decoder, W4%s, M=1" if small else
-                                 "decode-step weight stream, 32-layer 4096-wide int4 g32 decoder "
-                                 "(Llama-3.1-8B shape) + 128256-row lm_head with argmax, W4%s, M=1")
-                                % act[1:].upper(),
-                    "weight_bytes_per_step": st.weight_bytes,
-                    "l2": "inputs %.2f GB > 126 MB L2 (no flush)" % (st.weight_bytes / 1e9)}
+        w.config = workload_config(name)
+        assert w.config["weight_bytes_per_step"] == st.weight_bytes
         w.dominant = ("k_step<int4 %s> (persistent decode-step kernel, 32 layers + lm_head)"
                       % act, w.run, 1, st.weight_bytes)
         w.cpu_sample = ("w4" + act, (layers, head, xh))
@@ -222,9 +215,8 @@ def build_workload(name, dev, torch):
         w.unit_bytes = W.numel() * 2
         w.launches = 2
         w.run = lambda: dg.decode_step_weights(plan, ws, stream=s)
-        w.config = {"workload": "lm_head 248320x2048 fp16 with fused greedy argmax, M=1",
-                    "weight_bytes_per_call": w.unit_bytes,
-                    "l2": "inputs 1.02 GB > 126 MB L2 (no flush)"}
+        w.config = workload_config(name)
+        assert w.config["weight_bytes_per_call"] == w.unit_bytes
         w.dominant = ("lm_head 248320x2048 fp16", w.run, 1, w.unit_bytes)
         w.cpu_sample = ("head", (W, x))
     elif name == "gateup_fp16":
@@ -253,9 +245,8 @@ def build_workload(name, dev, torch):
         w.unit_bytes = 4 * 2 * 8960 * 1536 * 2
         w.launches = plans.count_launches(list(plan.array))
         w.run = lambda: dg.decode_step_weights(plan, gws, stream=s)
-        w.config = {"workload": "fused gate|up 17920x1536 fp16 (4 distinct pairs per step), M=1",
-                    "weight_bytes_per_step": w.unit_bytes,
-                    "l2": "inputs 220 MB > 126 MB L2 (no flush)"}
+        w.config = workload_config(name)
+        assert w.config["weight_bytes_per_step"] == w.unit_bytes
         w.dominant = ("gate|up 17920x1536 fp16", w.run, 4, 2 * 8960 * 1536 * 2)
         w.cpu_sample = ("pairs", (pairs, x))
     elif name in ("gateup_w4a16", "gateup_w4a8"):
@@ -273,10 +264,8 @@ def build_workload(name, dev, torch):
         w.unit_bytes = st.weight_bytes
         w.launches = st.n_launches
         w.run = lambda: dg.decode_step_weights(st.plan, st.ws, stream=s)
-        w.config = {"workload": "fused gate|up 28672x4096 int4 g32 (2 layers per step), W4%s, M=1"
-                                % act[1:].upper(),
-                    "weight_bytes_per_step": st.weight_bytes,
-                    "l2": "inputs 132 MB > 126 MB L2 (no flush)"}
+        w.config = workload_config(name)
+        assert w.config["weight_bytes_per_step"] == st.weight_bytes
         w.dominant = ("gate|up 28672x4096 int4", w.run, 2, st.weight_bytes // 2)
         w.cpu_sample = ("w4" + act, (sub, None, None))
         w.dtype = "int4xf16" if act == "a16" else "int4xi8"
@@ -289,10 +278,8 @@ def build_workload(name, dev, torch):
         w.unit_bytes = st.weight_bytes
         w.launches = st.n_launches
         w.run = lambda: dg.decode_step_weights(st.plan, st.ws, stream=s)
-        w.config = {"workload": "decode-step weight stream, 4 layers of the 1536-wide fp16 "
-                                "decoder, 28 matrices, M=1",
-                    "weight_bytes_per_step": st.weight_bytes,
-                    "l2": "inputs 374 MB > 126 MB L2 (no flush)"}
+        w.config = workload_config(name)
+        assert w.config["weight_bytes_per_step"] == st.weight_bytes
         w.dominant = ("decode step (persistent kernel)", w.run, 1, st.weight_bytes)
         w.cpu_sample = ("fp", layers)
     elif name == "gemv_f16_2048" or name.startswith("w8a8_m"):
@@ -334,13 +321,66 @@ def build_workload(name, dev, torch):
         w.unit_bytes = C * per
         w.launches = C
         w.run = lambda: [c() for c in calls]
-        w.config = {"workload": desc, "bytes_per_call": per, "calls_per_step": C,
-                    "l2": "%d rotating weight copies, %.0f MB > 2x L2" % (C, C * per / 1e6)}
+        w.config = workload_config(name)
+        assert (w.config["bytes_per_call"], w.config["calls_per_step"]) == (per, C)
         w.dominant = (desc, w.run, C, per)
         w.keep = copies
     else:
         raise SystemExit("unknown workload %s" % name)
     return w
+
+
+def workload_config(name):
+    """The `config` object of a workload's JSON line, from its shapes alone
+    (no device work): both arms report the same one."""
+    fp16_layer = 1536 * (1536 + 256 + 256 + 1536 + 3 * 8960) * 2
+    int4_layer = 4096 * (4096 + 1024 + 1024 + 4096 + 3 * 14336)
+    int4_bytes = lambda n: n // 2 + n // 32 * 2  # packed codes + fp16 scales, group 32
+    if name == "decode_fp16":
+        return {"workload": "decode-step weight stream, 28-layer 1536-wide fp16 decoder "
+                            "(Qwen2.5-1.5B shape), 196 matrices, M=1",
+                "weight_bytes_per_step": 28 * fp16_layer,
+                "l2": "inputs 2.62 GB > 126 MB L2 (no flush)"}
+    if name == "decode_fp16_4l":
+        return {"workload": "decode-step weight stream, 4 layers of the 1536-wide fp16 "
+                            "decoder, 28 matrices, M=1",
+                "weight_bytes_per_step": 4 * fp16_layer,
+                "l2": "inputs 374 MB > 126 MB L2 (no flush)"}
+    if name.startswith("decode_int4"):
+        act = name[-3:]
+        small = "_4l_" in name
+        nbytes = int4_bytes(4 * int4_layer) if small else \
+            int4_bytes(32 * int4_layer + 128256 * 4096)
+        return {"workload": ("decode-step weight stream, 4 layers of the 4096-wide int4 g32 "
+                             "decoder, W4%s, M=1" if small else
+                             "decode-step weight stream, 32-layer 4096-wide int4 g32 decoder "
+                             "(Llama-3.1-8B shape) + 128256-row lm_head with argmax, W4%s, M=1")
+                            % act[1:].upper(),
+                "weight_bytes_per_step": nbytes,
+                "l2": "inputs %.2f GB > 126 MB L2 (no flush)" % (nbytes / 1e9)}
+    if name == "lm_head":
+        return {"workload": "lm_head 248320x2048 fp16 with fused greedy argmax, M=1",
+                "weight_bytes_per_call": 248320 * 2048 * 2,
+                "l2": "inputs 1.02 GB > 126 MB L2 (no flush)"}
+    if name == "gateup_fp16":
+        return {"workload": "fused gate|up 17920x1536 fp16 (4 distinct pairs per step), M=1",
+                "weight_bytes_per_step": 4 * 17920 * 1536 * 2,
+                "l2": "inputs 220 MB > 126 MB L2 (no flush)"}
+    if name in ("gateup_w4a16", "gateup_w4a8"):
+        return {"workload": "fused gate|up 28672x4096 int4 g32 (2 layers per step), W4%s, M=1"
+                            % name[-3:][1:].upper(),
+                "weight_bytes_per_step": int4_bytes(2 * 28672 * 4096),
+                "l2": "inputs 132 MB > 126 MB L2 (no flush)"}
+    if name == "gemv_f16_2048" or name.startswith("w8a8_m"):
+        if name == "gemv_f16_2048":
+            per, desc = 2048 * 2048 * 2, "fp16 GEMV 2048x2048, M=1"
+        else:
+            per = 14336 * 4096 + 14336 * 4
+            desc = "W8A8 14336x4096 int8 GEMV, M=%d" % int(name[len("w8a8_m"):])
+        C = -(-2 * L2_BYTES // per)
+        return {"workload": desc, "bytes_per_call": per, "calls_per_step": C,
+                "l2": "%d rotating weight copies, %.0f MB > 2x L2" % (C, C * per / 1e6)}
+    raise SystemExit("unknown workload %s" % name)
 
 
 def graph_of(fn, stream, torch):
@@ -696,6 +736,7 @@ def run_reference(args, world):
         w.cpu_sample = ("w8", (W_, s_w, x_))
         cfg = "W8A8 14336x4096 int8 GEMV, M=%d" % M
     # each step: one bounded sample (~1 s of oracle work)
+    main_cfg = workload_config(wl)
     for _ in range(args.warmup):
         oracle_sample(w, 0.0)
     done = secs = 0.0
@@ -709,7 +750,8 @@ def run_reference(args, world):
            "unit": "GB/s", "n_gpus": world, "steps": min(args.steps, 50), "warmup": args.warmup,
            "ms_per_step": round(secs / min(args.steps, 50) * 1e3, 3), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": cfg, "sample": "about 1 s of whole-matrix oracle calls per step"},
+           "config": dict(main_cfg, parallelism="single GPU box, host cores",
+                          sample="about 1 s of whole-matrix oracle calls per step (" + cfg + ")"),
            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": os.cpu_count(),
                             "kind": "oracle", "sample": desc},
            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
