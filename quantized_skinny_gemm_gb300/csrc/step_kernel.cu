@@ -407,7 +407,10 @@ cudaError_t step_run_nw(const StepParams* sp, int grid, size_t smem, cudaStream_
 template <class P>
 cudaError_t step_run(const StepParams* sp, int grid, size_t smem, cudaStream_t s, int* occ,
                      int max_k, int nw) {
-    (void)nw;  // every format runs 16 warps (StepCfg)
+    // W4A8 may run 20 warps (the host picks it only when no phase splits K:
+    // the split barriers' id ranges are disjoint up to 16 warps)
+    if constexpr (std::is_same<P, PolicyW4A8>::value)
+        if (nw == 20) return step_run_nw<P, 20>(sp, grid, smem, s, occ, max_k);
     return step_run_nw<P, StepCfg<P>::kWarps>(sp, grid, smem, s, occ, max_k);
 }
 
