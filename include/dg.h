@@ -129,7 +129,7 @@ dg_status dg_gemv_w8a8(const int8_t* W, const float* w_scale, const int8_t* x,
  * W4A8 when x_i8 != NULL:   acc_g = sum_{k in g} q * x_i8 (exact int32),
  *                           y = fp16( x_scale[m] * sum_g s[n][g] * acc_g ).
  * x_f16 [M][K] is read for W4A16 and ignored for W4A8.  1 <= M <= 16, and the
- * staged activations (4 bytes per element for W4A16, about 1 for W4A8) must
+ * staged activations (2 bytes per element for W4A16, about 1 for W4A8) must
  * fit one CTA's shared memory (DG_ERR_UNSUPPORTED otherwise). */
 dg_status dg_gemv_w4(const uint8_t* Wq, const void* scales, int group_size, const void* x_f16,
                      const int8_t* x_i8, const float* x_scale, void* y, int M, int N, int K,
@@ -197,7 +197,7 @@ dg_status dg_decode_step_weights(const dg_linear* ops, int n_ops, void* ws, size
  * the persistent kernel's barrier, plus 32 KB of argmax partials when an op is
  * an lm_head, plus, per int4 op at M = 1, its activations in the kernel's
  * layout: DG_LINEAR_W4A8 ceil(K/1024)*1024 + K/8 bytes, DG_LINEAR_W4A16
- * ceil(K/1024)*4096 bytes, each rounded up to 256); for a
+ * ceil(K/1024)*2048 bytes, each rounded up to 256); for a
  * single lm_head this also covers dg_lm_head_argmax; for a single op of at
  * most 65536 outputs (M * N) it also covers split-K partials of a dg_gemv_*
  * call (8 ranges x M x N x 4 bytes).

@@ -551,10 +551,10 @@ static bool run_writes_weights(const dg_linear* ops, int n) {
 // int4 step phases whose activations are ready before the launch get a copy
 // in the kernel's interleaved layout, written by the launch's prologue into
 // the workspace after the barrier words and argmax partials: W4A8 int8 codes
-// (given, or quantized in the prologue) plus the chunk sums; W4A16 fp32.
+// (given, or quantized in the prologue) plus the chunk sums; W4A16 fp16 pairs.
 static size_t int4_layout_bytes(int kind, int K) {
     const size_t nch = (size_t)(K / 32), padded = ((nch + 31) / 32) * 32;
-    const size_t bytes = kind == DG_LINEAR_W4A8 ? padded * 32 + nch * 4 : padded * 128;
+    const size_t bytes = kind == DG_LINEAR_W4A8 ? padded * 32 + nch * 4 : padded * 64;
     return (bytes + 255) & ~(size_t)255;
 }
 static size_t step_scratch_offset(const dg_linear* ops, int n) {

@@ -245,10 +245,12 @@ __device__ __forceinline__ size_t int4_x_piece(int c, int i, int pieces) {
 
 // Groupwise int4 weights with fp16 activations; 32 codes per chunk.  Chunk c
 // covers codes [32c, 32c + 32) of the row and uses the scale of group c / cpg
-// (cpg = group / 32).  Activations are staged as fp32 (exact) in the
-// interleaved layout, eight 16-byte pieces per chunk, each 8-block ordered
-// x0 x4 x1 x5 x2 x6 x3 x7 to line up with the unpacked pairs; q x is exact in
-// fp32 and each FMA rounds once.
+// (cpg = group / 32).  Activations are staged as fp16 in the interleaved
+// layout, four 16-byte pieces per chunk: piece i holds the pairs (x0,x4)
+// (x1,x5) (x2,x6) (x3,x7) of the chunk's i-th block of eight, lined up with the
+// unpacked code pairs.  Each code (exact in fp16) meets its activation in one
+// mixed-precision FMA (fp16 x fp16 + fp32: the product of a 4-bit code and an
+// 11-bit significand is exact, one rounding), in four chains, one per block.
 struct PolicyW4A16 {
     static constexpr int kElems = 32;
     static constexpr bool kIntAct = false;
@@ -257,7 +259,7 @@ struct PolicyW4A16 {
     struct Chunk { uint4 w; uint16_t s; };
 
     __host__ __device__ static size_t row_bytes(int K) { return (size_t)K / 2; }
-    __host__ __device__ static size_t token_bytes(int K) { return int4_x_token_bytes(K, 128); }
+    __host__ __device__ static size_t token_bytes(int K) { return int4_x_token_bytes(K, 64); }
     __host__ __device__ static size_t x_bytes(int MT, int K) { return (size_t)MT * token_bytes(K); }
 
     __device__ static void stage_x(const ActIn& a, unsigned char* xs, int MT) {
@@ -267,15 +269,11 @@ struct PolicyW4A16 {
         for (int i = threadIdx.x; i < MT * per_row; i += blockDim.x) {
             const int m = i / per_row, blk = i - m * per_row;
             const uint4 v = m < a.M ? src[i] : make_uint4(0, 0, 0, 0);
-            const float2 h01 = unpack2_f32<false>(v.x), h23 = unpack2_f32<false>(v.y);
-            const float2 h45 = unpack2_f32<false>(v.z), h67 = unpack2_f32<false>(v.w);
-            // block blk = word blk % 4 of chunk blk / 4: pieces 2w and 2w + 1
-            unsigned char* base = xs + m * tb;
-            const int c = blk >> 2, wd = blk & 3;
-            *reinterpret_cast<float4*>(base + int4_x_piece(c, 2 * wd, 8)) =
-                make_float4(h01.x, h45.x, h01.y, h45.y);  // x0 x4 x1 x5
-            *reinterpret_cast<float4*>(base + int4_x_piece(c, 2 * wd + 1, 8)) =
-                make_float4(h23.x, h67.x, h23.y, h67.y);  // x2 x6 x3 x7
+            // v = (x0,x1) (x2,x3) (x4,x5) (x6,x7) -> (x0,x4) (x1,x5) (x2,x6) (x3,x7)
+            const uint4 o = make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632),
+                                       __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
+            // block blk = word blk % 4 of chunk blk / 4
+            *reinterpret_cast<uint4*>(xs + m * tb + int4_x_piece(blk >> 2, blk & 3, 4)) = o;
         }
     }
     __device__ __forceinline__ static void load(Chunk& ch, const RowRef& r, int c, int gk, int cpg) {
@@ -296,18 +294,20 @@ struct PolicyW4A16 {
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             const unsigned char* xb = xs + m * tb;
-            // codes (c_i, c_i+4) against (x_i, x_i+4): two chains, one per half
-            float2 P = make_float2(0.f, 0.f);
+            float P[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float4 xa = *reinterpret_cast<const float4*>(xb + int4_x_piece(c, 2 * i, 8));
-                const float4 xc = *reinterpret_cast<const float4*>(xb + int4_x_piece(c, 2 * i + 1, 8));
-                P = fma2(unpack2_f32<false>(q[i][0]), make_float2(xa.x, xa.y), P);
-                P = fma2(unpack2_f32<false>(q[i][1]), make_float2(xa.z, xa.w), P);
-                P = fma2(unpack2_f32<false>(q[i][2]), make_float2(xc.x, xc.y), P);
-                P = fma2(unpack2_f32<false>(q[i][3]), make_float2(xc.z, xc.w), P);
+                const uint4 xp = *reinterpret_cast<const uint4*>(xb + int4_x_piece(c, i, 4));
+                const uint32_t xv[4] = {xp.x, xp.y, xp.z, xp.w};
+                float a = 0.f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {  // (c_j, c_j+4) against (x_j, x_j+4)
+                    a = fma_f16(lo16(q[i][j]), lo16(xv[j]), a);
+                    a = fma_f16(hi16(q[i][j]), hi16(xv[j]), a);
+                }
+                P[i] = a;
             }
-            acc[m] = fmaf(P.x + P.y, s, acc[m]);
+            acc[m] = fmaf((P[0] + P[1]) + (P[2] + P[3]), s, acc[m]);
         }
     }
     __device__ static float finish(const RowRef&, Acc a, float) { return a; }

@@ -137,11 +137,11 @@ def test_workspace_holds_the_w4a8_activation_layouts():
     assert dg.workspace_bytes([w4a8(4096), _head()]) == head_ws + 4608
     # M > 1 runs per group: no layout; the split-K bound 8 x M x N x 4 = 512
     assert dg.workspace_bytes([w4a8(4096, M=2)]) == 512
-    # W4A16: the fp32 interleaved activations, 128 bytes per 32-code chunk
+    # W4A16: the fp16 interleaved activations, 64 bytes per 32-code chunk
     assert dg.workspace_bytes([w4a8(4096, kind=dg.LINEAR_W4A16, x=A, x_i8=None,
-                                    x_scale=None)]) == 256 + 128 * 128
+                                    x_scale=None)]) == 256 + 128 * 64
     assert dg.workspace_bytes([w4a8(14336, kind=dg.LINEAR_W4A16, x=A, x_i8=None,
-                                    x_scale=None)]) == 256 + 14 * 32 * 128
+                                    x_scale=None)]) == 256 + 14 * 32 * 64
 
 
 def test_decode_step_validates_every_op_first(lib):
