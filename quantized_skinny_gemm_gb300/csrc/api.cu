@@ -75,6 +75,7 @@ struct Tune {
     int R = 0, KS = 0, CPS = 0, PF = -1, PDL = -1, STEP = -1, SPIN = -1, SNW = 0, MMA = -1;
     int RING = -1, TSB = 0, TNS = 0, TNC = 0;  // weight ring: on/off, KB per stage, stages, consumers
     int KP = 0;                                // split-K ranges of a per-op launch (1 = off)
+    int KS8 = -1;                              // rows of >= 16 KB split over 8 warps
 };
 
 static Tune read_tune() {
@@ -100,6 +101,7 @@ static Tune read_tune() {
         else if (std::sscanf(tok, "TNS=%d", &v) == 1) t.TNS = v;
         else if (std::sscanf(tok, "TNC=%d", &v) == 1) t.TNC = v;
         else if (std::sscanf(tok, "KP=%d", &v) == 1) t.KP = v;
+        else if (std::sscanf(tok, "KS8=%d", &v) == 1) t.KS8 = v;
     }
     return t;
 }
@@ -143,7 +145,7 @@ static int pick_ks(Fmt f, int K) {
     const int t = tune().KS;
     if (t == 1 || t == 2 || t == 4 || t == 8) return t;
     const size_t rb = elem_row_bytes(f, K);
-    if (rb >= 16384) return 4;
+    if (rb >= 16384) return tune().KS8 == 1 ? 8 : 4;
     if (rb >= 8192) return 2;
     return 1;
 }

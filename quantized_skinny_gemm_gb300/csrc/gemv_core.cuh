@@ -413,14 +413,15 @@ struct PolicyW4A8 {
     }
 };
 
-// Named barrier of warp `warp`'s slot when ks = 2 or 4 warps share a row.
+// Named barrier of warp `warp`'s slot when ks = 2, 4 or 8 warps share a row.
 // In a persistent kernel warps move through phases independently, so phases
 // with different ks can be live at once, and a named barrier must never be
-// used with two thread counts at the same time: the two splits take disjoint
-// ids, ks = 2 from 1 upward and ks = 4 from 14 downward (disjoint for up to
-// 16 warps; 0 is __syncthreads, 15 the weight ring's consumer barrier).
+// used with two thread counts at the same time: the splits take disjoint ids,
+// ks = 2 from 1 upward (1..8), ks = 8 at 9..10 and ks = 4 from 14 downward
+// (14..11), for up to 16 warps; 0 is __syncthreads, 15 the weight ring's
+// consumer barrier.
 __device__ __forceinline__ int slot_barrier(int warp, int ks) {
-    return ks == 4 ? 14 - warp / 4 : 1 + warp / ks;
+    return ks == 4 ? 14 - warp / 4 : ks == 8 ? 9 + warp / 8 : 1 + warp / ks;
 }
 
 // ---- the row-group computation shared by all kernels ------------------------------

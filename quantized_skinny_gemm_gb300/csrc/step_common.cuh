@@ -49,11 +49,14 @@ __device__ __forceinline__ int div_floor_small(int a, int d) {
     return q;
 }
 
-// v mod (NW / ks) for ks in {1, 2, 4} with compile-time divisors.
+// v mod (NW / ks), the slot count, for ks in {1, 2, 4, 8} with compile-time
+// divisors (NW / ks rounded down, as the kernels count slots).
 template <int NW>
 __device__ __forceinline__ int mod_slots(unsigned v, int ks) {
-    return ks == 1 ? (int)(v % (unsigned)NW)
-                   : ks == 2 ? (int)(v % (unsigned)(NW / 2)) : (int)(v % (unsigned)(NW / 4));
+    return ks == 1   ? (int)(v % (unsigned)NW)
+           : ks == 2 ? (int)(v % (unsigned)(NW / 2))
+           : ks == 4 ? (int)(v % (unsigned)(NW / 4))
+                     : (int)(v % (unsigned)(NW / 8));
 }
 
 // Per-phase values of one CTA, computed once per launch (plan_phases) so
@@ -102,10 +105,10 @@ __device__ void plan_phases(const StepParams& sp, PhaseSlice* table, int b, int 
     __syncthreads();
 }
 
-// v / (NW / ks) for ks in {1, 2, 4} with compile-time divisors.
+// v / (NW / ks) for ks in {1, 2, 4, 8} with compile-time divisors.
 template <int NW>
 __device__ __forceinline__ int div_slots(int v, int ks) {
-    return ks == 1 ? v / NW : ks == 2 ? v / (NW / 2) : v / (NW / 4);
+    return ks == 1 ? v / NW : ks == 2 ? v / (NW / 2) : ks == 4 ? v / (NW / 4) : v / (NW / 8);
 }
 
 // Greedy token of an lm_head phase from the G per-CTA partials, by one full

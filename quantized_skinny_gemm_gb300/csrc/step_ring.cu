@@ -38,10 +38,11 @@ namespace {
 
 constexpr int kXR = kRingXR;  // activation chunks per lane kept in registers
 constexpr int kConsumerBar = 15;  // named barrier of the consumer warps
-// Rows are dealt to slots in groups of kGroupRows / ks consecutive rows (about
+// Rows are dealt to slots in groups of group_rows(ks) consecutive rows (about
 // 12 KB of fp16 weights), so a phase of a few rows per CTA occupies a few
 // warps and each pays the phase's set-up once per group, not once per row.
 constexpr int kGroupRows = 4;
+__host__ __device__ constexpr int group_rows(int ks) { return ks < kGroupRows ? kGroupRows / ks : 1; }
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -474,9 +475,9 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1) k_step_ring(const __grid_con
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // per-phase slices and the dealing of row groups (kGroupRows / ks rows)
+    // per-phase slices and the dealing of row groups (group_rows(ks) rows)
     plan_phases(sp, table, b, G,
-                [](const StepPhase& ph, int n) { return (n + kGroupRows / ph.ks - 1) / (kGroupRows / ph.ks); });
+                [](const StepPhase& ph, int n) { return (n + group_rows(ph.ks) - 1) / group_rows(ph.ks); });
 
     if (warp == NC) {
         // ---- producer: one thread copies the CTA's row stream into the ring,
@@ -589,16 +590,18 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1) k_step_ring(const __grid_con
                 reduce_token(sp.part, G, sp.ph[p - 1].token);
         }
         const int ks = ph.ks;
-        const int slots = NC / ks;
+        const int slots = NC / ks;  // warps past slots * ks take no rows (ks = 8)
         const int slot = warp / ks, kw = warp - slot * ks;
+        const bool idle = slot >= slots;
         const int nchunks = ph.K / 8, step = ks * 32, c0 = kw * 32 + lane;
         const PhaseSlice sl = table[p];
         const int r0 = sl.r0, n = sl.n;
         // groups of rows are dealt round-robin over the whole step (continuing
         // where the previous phase stopped) so every slot streams a fair share
-        const int gr = kGroupRows / ks;
+        const int gr = group_rows(ks);
         const int lead = mod_slots<NC>(sl.deal0, ks);
-        const int mine = slot >= lead ? slot - lead : slot - lead + slots;
+        // an idle warp's first group is past the phase's last
+        const int mine = idle ? (n + gr - 1) / gr : slot >= lead ? slot - lead : slot - lead + slots;
         const bool head = (ph.flags & kPhaseHead) != 0;
         float best_v = NAN;
         int best_i = INT_MAX;
