@@ -282,11 +282,15 @@ def build_workload(name, dev, torch):
         assert w.config["weight_bytes_per_step"] == st.weight_bytes
         w.dominant = ("decode step (persistent kernel)", w.run, 1, st.weight_bytes)
         w.cpu_sample = ("fp", layers)
-    elif name == "gemv_f16_2048" or name.startswith("w8a8_m"):
+    elif name == "gemv_f16_2048" or name.startswith("w8a8_m") or name.startswith("fp16_m"):
         # one matrix called repeatedly; C rotating copies (> 2x L2 in total) keep
         # every call cold.  A step is one call on each copy.
         if name == "gemv_f16_2048":
             W, x = synth.gemv_f16_workload(seed=0)
+            per = W.numel() * 2
+        elif name.startswith("fp16_m"):
+            M = int(name[len("fp16_m"):])
+            W, x = synth.fp_case(14336, 4096, M, seed=0)
             per = W.numel() * 2
         else:
             M = int(name[len("w8a8_m"):])
@@ -300,11 +304,11 @@ def build_workload(name, dev, torch):
         xd = xin[ix]
         xd.copy_(x)
         copies = [W.to(dev) for _ in range(C)]
-        if name == "gemv_f16_2048":
+        if name == "gemv_f16_2048" or name.startswith("fp16_m"):
             calls = [lambda Wd=Wd, y=outs[iy]: dg.gemv_f16(Wd, xd, y, stream=s)
                      for Wd, iy in zip(copies, iys)]
             w.dtype = "f16"
-            desc = "fp16 GEMV 2048x2048, M=1"
+            desc = workload_config(name)["workload"]
             w.cpu_sample = ("pairs", ([(W, W)], x))
         else:
             swd = s_w.to(dev)
@@ -371,9 +375,12 @@ def workload_config(name):
                             % name[-3:][1:].upper(),
                 "weight_bytes_per_step": int4_bytes(2 * 28672 * 4096),
                 "l2": "inputs 132 MB > 126 MB L2 (no flush)"}
-    if name == "gemv_f16_2048" or name.startswith("w8a8_m"):
+    if name == "gemv_f16_2048" or name.startswith("w8a8_m") or name.startswith("fp16_m"):
         if name == "gemv_f16_2048":
             per, desc = 2048 * 2048 * 2, "fp16 GEMV 2048x2048, M=1"
+        elif name.startswith("fp16_m"):
+            per = 14336 * 4096 * 2
+            desc = "fp16 14336x4096 verify tile, M=%d" % int(name[len("fp16_m"):])
         else:
             per = 14336 * 4096 + 14336 * 4
             desc = "W8A8 14336x4096 int8 GEMV, M=%d" % int(name[len("w8a8_m"):])
@@ -516,7 +523,7 @@ def main():
                              "decode_int4_4l_a16", "decode_int4_4l_a8", "lm_head",
                              "gateup_fp16", "gateup_w4a16", "gateup_w4a8", "decode_fp16_4l",
                              "gemv_f16_2048", "w8a8_m1",
-                             "w8a8_m4", "w8a8_m16"])
+                             "w8a8_m4", "w8a8_m16", "fp16_m8", "fp16_m16"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--quick", action="store_true",
                     help="time the step only (no dominant-kernel, e2e, probe or CPU legs); "
@@ -730,6 +737,10 @@ def run_reference(args, world):
         W_, x_ = synth.gemv_f16_workload(seed=0)
         w.cpu_sample = ("pairs", ([(W_, W_)], x_))
         cfg = "fp16 GEMV 2048x2048, M=1"
+    elif wl.startswith("fp16_m"):
+        W_, x_ = synth.fp_case(14336, 4096, int(wl[len("fp16_m"):]), seed=0)
+        w.cpu_sample = ("pairs", ([(W_, W_)], x_))
+        cfg = "fp16 14336x4096 verify tile, M=%s" % wl[len("fp16_m"):]
     else:
         M = int(wl[len("w8a8_m"):])
         W_, s_w, x_ = synth.w8a8_workload(M=M, seed=0)

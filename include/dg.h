@@ -38,7 +38,10 @@
  *    than half the SMs) that is given workspace splits K across CTAs (split-K:
  *    S fixed K ranges, partial sums in ws, a second kernel adding them in range
  *    order); its order then also depends on N, M and the SM count, and is still
- *    the same on every call.  Integer (W8A8) sums are exact either way.
+ *    the same on every call.  Integer (W8A8) sums are exact either way.  fp16 /
+ *    bf16 calls with 8 <= M <= 16 run on the tensor cores (fp32 accumulate, K
+ *    split by a rule on K alone): their order differs from the M < 8 path's
+ *    and, within that path, still depends only on K.
  *  - Alignment.  W, x, xq and y must be 16-byte aligned; K must be a multiple
  *    of 8 (fp16/bf16), 16 (int8) or 32 (int4).
  */

@@ -370,6 +370,49 @@ static size_t split_ws_bytes(const dg_linear& op) {
     return (8 * outs * 4 + 255) & ~(size_t)255;
 }
 
+// Whether fp16 / bf16 with this many tokens runs on the tensor-core tile.
+static bool use_fp_mma(const dg_linear& op) {
+    if ((op.kind != DG_LINEAR_F16 && op.kind != DG_LINEAR_BF16) || op.M < 8 || op.K % 32 ||
+        tune().MMA == 0)
+        return false;
+    return gemv_fp_mma_smem(op.K) <= smem_optin_limit();
+}
+
+// K split of the fp16 / bf16 tile, from K alone (so a row's result does not
+// depend on N): the most warps (4, 2, 1) that divide the 32-wide k blocks and
+// leave each at least 16 of them.
+static int fp_mma_ks(int K) {
+    const int nblk = K / 32;
+    for (int ks = 4; ks > 1; ks /= 2)
+        if (nblk % ks == 0 && nblk / ks >= 16) return ks;
+    return 1;
+}
+
+static dg_status launch_fp_mma(GemvParams& p, bool bf16, cudaStream_t s) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int occ = 0;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = cache.find({dev, p.a.K, (int)bf16});
+        if (it != cache.end()) occ = it->second;
+    }
+    if (!occ) {
+        if (gemv_fp_mma(nullptr, bf16, p.a.K, 0, nullptr, &occ) != cudaSuccess || occ < 1) occ = 1;
+        std::lock_guard<std::mutex> g(mu);
+        cache[{dev, p.a.K, (int)bf16}] = occ;
+    }
+    p.ksplit = fp_mma_ks(p.a.K);
+    const int tiles = (p.t.N + 15) / 16;
+    const int per_cta = kWarps / p.ksplit;
+    const int need = (tiles + per_cta - 1) / per_cta;
+    int maxg = sm_count() * occ;
+    if (maxg < 1) maxg = 1;
+    return to_status(gemv_fp_mma(&p, bf16, p.a.K, need < maxg ? need : maxg, s, nullptr));
+}
+
 // Launches ops[0..n) (same kind, same activations) as one kernel (two with
 // split-K, when ws holds the partials).
 static dg_status launch_group(const dg_linear* ops, int n, cudaStream_t s, void* ws = nullptr,
@@ -390,6 +433,7 @@ static dg_status launch_group(const dg_linear* ops, int n, cudaStream_t s, void*
     p.t.nseg = n;
     p.t.N = rows;
     if (use_i8_mma(ops[0])) return launch_i8_mma(p, s);
+    if (use_fp_mma(ops[0])) return launch_fp_mma(p, ops[0].kind == DG_LINEAR_BF16, s);
     GemvLaunch L{fmt_of(ops[0].kind), pick_mt(ops[0].M), 0, false, ops[0].K, p.group, 0};
     L.R = pick_r(L.fmt, L.MT);
     configure(L, p);

@@ -301,6 +301,9 @@ size_t gemv_smem(Fmt f, int MT, int K, int group);
 // W8A8 for 8..16 tokens on the tensor cores (mma.sync s8, exact int32).
 cudaError_t gemv_i8_mma(const GemvParams* p, int K, int grid, cudaStream_t s, int* occ, bool f16);
 size_t gemv_i8_mma_smem(int K);
+// fp16 / bf16 for 8..16 tokens on the tensor cores (gemv_fp_mma.cu).
+cudaError_t gemv_fp_mma(const GemvParams* p, bool bf16, int K, int grid, cudaStream_t s, int* occ);
+size_t gemv_fp_mma_smem(int K);
 
 // Host helpers of api.cu shared with the static-scratch lm_head entry point.
 dg_status validate(const dg_linear& op, bool allow_quant_input);
