@@ -76,6 +76,7 @@ struct Tune {
     int RING = -1, TSB = 0, TNS = 0, TNC = 0;  // weight ring: on/off, KB per stage, stages, consumers
     int KP = 0;                                // split-K ranges of a per-op launch (1 = off)
     int KS8 = -1;                              // rows of >= 16 KB split over 8 warps
+    int W4MMA = -1;                            // W4A16 at one token on the tensor cores
 };
 
 static Tune read_tune() {
@@ -102,6 +103,7 @@ static Tune read_tune() {
         else if (std::sscanf(tok, "TNC=%d", &v) == 1) t.TNC = v;
         else if (std::sscanf(tok, "KP=%d", &v) == 1) t.KP = v;
         else if (std::sscanf(tok, "KS8=%d", &v) == 1) t.KS8 = v;
+        else if (std::sscanf(tok, "W4MMA=%d", &v) == 1) t.W4MMA = v;
     }
     return t;
 }
@@ -150,7 +152,18 @@ static int pick_ks(Fmt f, int K) {
     return 1;
 }
 
-static int pick_r(Fmt f, int MT) {
+// W4A16 at one token on the tensor cores (tiles of kW4MmaRows rows, one warp
+// each, K whole; K a multiple of kW4MmaSeg), selected with DG_TUNE=W4MMA=1.
+// Measured slower than the CUDA-core path on the int4 decoder (32-layer step
+// 1213-1663 us against 1235 us; fused gate|up 28-33 us against 23.6 us), so
+// not the default.
+static bool w4_mma(Fmt f, int MT, int K) {
+    return f == F_W4A16 && MT == 1 && K % kW4MmaSeg == 0 && tune().W4MMA == 1 &&
+           tune().MMA != 0 && w4_mma_smem(K) <= smem_optin_limit();
+}
+
+static int pick_r(Fmt f, int MT, int K) {
+    if (w4_mma(f, MT, K)) return kW4MmaRows;
     const int t = tune().R;
     if (t == 1 || t == 2 || t == 4) return t;
     if (MT == 1) return (f == F_W4A16 || f == F_W4A8) ? 2 : 1;
@@ -191,7 +204,7 @@ static int occupancy(const GemvLaunch& L) {
 
 // Fills L.grid and p.iters / ksplit / prefetch for a launch over p.N rows.
 static void configure(GemvLaunch& L, GemvParams& p) {
-    const int ks = pick_ks(L.fmt, p.a.K);
+    const int ks = L.R == kW4MmaRows ? 1 : pick_ks(L.fmt, p.a.K);
     const int slots = kWarps / ks;
     const int n_rg = (p.t.N + L.R - 1) / L.R;
     const int need = (n_rg + slots - 1) / slots;
@@ -345,10 +358,12 @@ static dg_status launch_i8_mma(GemvParams& p, cudaStream_t s) {
 // each), CTAs write fp32 / int32 partials to the workspace and a second kernel
 // adds them in range order.  S follows the op's shape and the SM count.
 static int pick_kparts(const GemvLaunch& L, int N, int K) {
-    const int ks = pick_ks(L.fmt, K), slots = kWarps / ks;
+    const bool mma = L.R == kW4MmaRows;
+    const int ks = mma ? 1 : pick_ks(L.fmt, K), slots = kWarps / ks;
     const int n_rg = (N + L.R - 1) / L.R, need = (n_rg + slots - 1) / slots;
     const int kelems = (L.fmt == F_F16 || L.fmt == F_BF16) ? 8 : L.fmt == F_I8 ? 16 : 32;
-    const int J = (K / kelems + ks * 32 - 1) / (ks * 32);  // chunks per lane
+    // chunks per lane (segments per warp on the tensor-core tile)
+    const int J = mma ? K / kW4MmaSeg : (K / kelems + ks * 32 - 1) / (ks * 32);
     int S = tune().KP;
     if (S <= 0) {
         const int sms = sm_count();
@@ -435,7 +450,7 @@ static dg_status launch_group(const dg_linear* ops, int n, cudaStream_t s, void*
     if (use_i8_mma(ops[0])) return launch_i8_mma(p, s);
     if (use_fp_mma(ops[0])) return launch_fp_mma(p, ops[0].kind == DG_LINEAR_BF16, s);
     GemvLaunch L{fmt_of(ops[0].kind), pick_mt(ops[0].M), 0, false, ops[0].K, p.group, 0};
-    L.R = pick_r(L.fmt, L.MT);
+    L.R = pick_r(L.fmt, L.MT, L.K);
     configure(L, p);
     if (ws && al16(ws)) {
         const int S = pick_kparts(L, p.t.N, p.a.K);
@@ -462,7 +477,7 @@ dg_status launch_head(const dg_linear& op, void* ws, cudaStream_t s) {
     p.logits = op.logits;
     p.part = static_cast<ArgPart*>(ws);
     GemvLaunch L{fmt_of(op.kind), 1, 0, true, op.K, p.group, 0};
-    L.R = pick_r(L.fmt, 1);
+    L.R = pick_r(L.fmt, 1, L.K);
     configure(L, p);
     cudaError_t e = family(L, &p, s, nullptr);
     if (e != cudaSuccess) return DG_ERR_CUDA;
@@ -476,7 +491,7 @@ int head_grid(const dg_linear& op) {
     p.t.nseg = 1;
     p.t.N = op.N;
     GemvLaunch L{fmt_of(op.kind), 1, 0, true, op.K, p.group, 0};
-    L.R = pick_r(L.fmt, 1);
+    L.R = pick_r(L.fmt, 1, L.K);
     configure(L, p);
     return L.grid;
 }
@@ -505,12 +520,12 @@ static bool step_eligible(const dg_linear& op) { return op.M == 1 && !op.acc_out
 
 // CTAs of the step kernel per SM (ring_nc = 0: k_step; else k_step_ring
 // with that many consumer warps).
-static int step_occupancy(Fmt f, int max_k, size_t smem, int ring_nc, int nw) {
+static int step_occupancy(Fmt f, int max_k, size_t smem, int ring_nc, int nw, bool w4m) {
     static std::mutex mu;
-    static std::map<std::tuple<int, int, int, size_t, int, int>, int> cache;
+    static std::map<std::tuple<int, int, int, size_t, int, int, int>, int> cache;
     int dev = 0;
     cudaGetDevice(&dev);
-    const auto key = std::make_tuple(dev, (int)f, max_k, smem, ring_nc, nw);
+    const auto key = std::make_tuple(dev, (int)f, max_k, smem, ring_nc, nw, (int)w4m);
     {
         std::lock_guard<std::mutex> g(mu);
         auto it = cache.find(key);
@@ -519,7 +534,7 @@ static int step_occupancy(Fmt f, int max_k, size_t smem, int ring_nc, int nw) {
     StepParams* none = nullptr;
     int occ = 0;
     const cudaError_t e = ring_nc ? step_ring_launch(f, none, 0, smem, nullptr, &occ, ring_nc)
-                                  : step_launch(f, none, 0, smem, nullptr, &occ, nw);
+                                  : step_launch(f, none, 0, smem, nullptr, &occ, nw, w4m);
     if (e != cudaSuccess) occ = 0;
     std::lock_guard<std::mutex> g(mu);
     cache[key] = occ;
@@ -625,6 +640,15 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
     static thread_local StepParams sp;
     const Fmt f = fmt_of(ops[0].kind);
     const bool always_sync = tune().STEP == 2;  // barrier between every pair of phases
+    // W4A16 on the tensor cores when every op of the run allows it and the
+    // warps' weight rings fit beside the activation buffers
+    bool w4m = true;
+    int run_k = 0;
+    for (int k = 0; k < n; ++k) {
+        w4m = w4m && w4_mma(f, 1, ops[k].K);
+        run_k = ops[k].K > run_k ? ops[k].K : run_k;
+    }
+    w4m = w4m && step_smem(f, run_k, true) <= smem_optin_limit();
     int i = 0;
     while (i < n) {
         std::memset(&sp, 0, sizeof sp);
@@ -667,7 +691,7 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
             ph.N = rows;
             ph.K = a.K;
             ph.group = a.group_size >= 32 ? a.group_size : 32;
-            ph.ks = pick_ks(f, a.K);
+            ph.ks = w4m ? 1 : pick_ks(f, a.K);
             ph.x = a.x;
             ph.xq = a.x_i8;
             ph.x_scale = const_cast<float*>(a.x_scale);
@@ -753,7 +777,7 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
                 }
             }
         }
-        if (!ring_nc) smem = step_smem(f, max_k);
+        if (!ring_nc) smem = step_smem(f, max_k, w4m);
         if (smem > smem_optin_limit()) return DG_ERR_UNSUPPORTED;
         // k_step runs 16 warps; W4A8 20 (one more row group in flight per SM
         // sub-partition: 883 -> 863 us for the 32-layer step) when no phase
@@ -762,13 +786,13 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
         bool split = false;
         for (int q = 0; q < sp.nphase; ++q) split = split || sp.ph[q].ks > 1;
         const int nw = split ? 16 : tune().SNW > 0 ? tune().SNW : f == F_W4A8 ? 20 : 16;
-        const int occ = step_occupancy(f, max_k, smem, ring_nc, nw);
+        const int occ = step_occupancy(f, max_k, smem, ring_nc, nw, w4m);
         if (occ < 1) return DG_ERR_UNSUPPORTED;
         const int grid = sm_count() * occ;
         if (grid > kMaxArgCtas) return DG_ERR_UNSUPPORTED;
         if (cudaMemsetAsync(ws, 0, 2 * sizeof(unsigned), s) != cudaSuccess) return DG_ERR_CUDA;
         const cudaError_t e = ring_nc ? step_ring_launch(f, &sp, grid, smem, s, nullptr, ring_nc)
-                                      : step_launch(f, &sp, grid, smem, s, nullptr, nw);
+                                      : step_launch(f, &sp, grid, smem, s, nullptr, nw, w4m);
         if (e != cudaSuccess) return DG_ERR_CUDA;
     }
     return DG_OK;

@@ -21,6 +21,7 @@
 
 #include <climits>
 #include <cmath>
+#include <type_traits>
 
 #include "dg_internal.cuh"
 
@@ -424,6 +425,174 @@ __device__ __forceinline__ int slot_barrier(int warp, int ks) {
     return ks == 4 ? 14 - warp / 4 : ks == 8 ? 9 + warp / 8 : 1 + warp / ks;
 }
 
+// ---- W4A16 at one token on the tensor cores ---------------------------------------
+//
+// On the CUDA cores each int4 weight with an fp16 activation costs about four
+// issued instructions (unpack, mixed FMA, activation load, loop), which holds
+// the stream far below HBM speed.  mma.sync m16n8k16 (fp16 operands, fp32
+// accumulation) takes the products and their sums off the FMA pipe: 16 weight
+// rows form the A operand, and the activations a B operand whose column n
+// collects chunk n (32 codes) of a 256-code segment, so that D[row][n] is the
+// chunk's partial sum; its group scale is applied afterwards in fp32.
+//
+// Thread (g = lane / 4, t = lane % 4) streams rows g and g + 8 of the tile
+// and, of every segment, chunks t and t + 4 (so one warp-wide copy reads 64
+// contiguous bytes of each of 8 rows).  In each of a segment's 16 MMAs its k
+// values 2t, 2t+1 are a code pair (c_j, c_j+4) of chunk t and its k values
+// 2t+8, 2t+9 the same pair of chunk t + 4 (the pairs unpack_int4x8_f16
+// yields).  Column n of B is then non-zero only in thread (g = n, t = n % 4),
+// fragment b0 for n < 4 and b1 for n >= 4, which holds the activations of that
+// pair in the interleaved layout; every other thread feeds zeros.  Thread
+// (g, t) finds D[g][2t], D[g][2t+1], D[g+8][2t], D[g+8][2t+1] in its
+// accumulator: the partials of chunks 2t and 2t + 1 of rows g and g + 8.  A
+// 4-bit code times an fp16 activation is exact; four independent MMA chains
+// (one per code pair) sum a chunk and are added in a fixed order; the lane
+// adds its scaled chunks in ascending order; a fixed xor butterfly joins the
+// quad.  The order follows K alone, never the row's place in the
+// tile, N or the grid.
+//
+// The host takes this path only on request: on the int4 decoder it measured
+// slower than the CUDA-core policy (PolicyW4A16) in every variant tried.
+//
+// Weights travel through a per-warp ring of kW4MmaStages segments in shared
+// memory, filled with cp.async kW4MmaStages - 1 segments ahead of use, so the
+// bytes in flight do not occupy registers.  Each thread reads back only the
+// 16-byte slots it copied itself: the copies' own completion (wait_group) is
+// the only ordering needed, and nothing waits on another thread.
+
+__device__ __forceinline__ void mma_m16n8k16_f16(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                 uint32_t a2, uint32_t a3, uint32_t b0,
+                                                 uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* src) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+constexpr int kW4MmaStages = 3;                     // segments in a warp's ring
+constexpr int kW4MmaStageBytes = 4 * 32 * 16;       // 4 slots of 16 B per lane
+constexpr int kW4MmaRingBytes = kW4MmaStages * kW4MmaStageBytes;  // per warp
+
+// wg / wh: codes of rows g and g + 8 (K / 2 bytes each); sg / sh: their fp16
+// group scales; xs: the activations in the interleaved layout (shared or
+// global memory); segments [sbeg, send); cpg = group / 32; ring: this warp's
+// kW4MmaRingBytes of shared memory.  Returns the sums of rows g (.x) and
+// g + 8 (.y), complete in all four lanes of the quad.
+__device__ __forceinline__ float2 w4a16_mma_rows(const unsigned char* wg, const unsigned char* wh,
+                                                 const uint16_t* sg, const uint16_t* sh,
+                                                 const unsigned char* xs, int sbeg, int send,
+                                                 int cpg, unsigned char* ring) {
+    constexpr int S = kW4MmaStages;
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const bool own_e = g == t, own_o = g == t + 4;
+    unsigned char* slot = ring + lane * 16;  // slot j of stage st: + (st * 4 + j) * 512
+    uint16_t sc[S][4];                       // group scales of the segments in flight
+
+    // segment s into stage st: its four 16-byte pieces (rows g, g + 8;
+    // chunks t, t + 4) and, into registers, the scales of chunks 2t, 2t + 1
+    auto issue = [&](int s, int st) {
+        const size_t off = (size_t)s * (kW4MmaSeg / 2) + (size_t)t * 16;
+        unsigned char* d = slot + st * kW4MmaStageBytes;
+        cp_async16(d, wg + off);
+        cp_async16(d + 512, wg + off + 64);
+        cp_async16(d + 1024, wh + off);
+        cp_async16(d + 1536, wh + off + 64);
+        const int c0 = s * 8 + 2 * t;
+        const int ga = group_of_chunk(c0, cpg), gb = group_of_chunk(c0 + 1, cpg);
+        sc[st][0] = ld_stream_u16(sg + ga);
+        sc[st][1] = ld_stream_u16(sg + gb);
+        sc[st][2] = ld_stream_u16(sh + ga);
+        sc[st][3] = ld_stream_u16(sh + gb);
+    };
+
+    uint4 xe = make_uint4(0u, 0u, 0u, 0u), xo = xe;  // B fragments: owners only
+    float yg = 0.f, yh = 0.f;
+#pragma unroll
+    for (int u = 0; u < S - 1; ++u) {
+        if (sbeg + u < send) issue(sbeg + u, u);
+        cp_async_commit();
+    }
+    for (int s0 = sbeg; s0 < send; s0 += S) {
+#pragma unroll
+        for (int u = 0; u < S; ++u) {
+            const int s = s0 + u;
+            if (s < send) {
+                if (s + S - 1 < send) issue(s + S - 1, (u + S - 1) % S);
+                cp_async_commit();
+                cp_async_wait<S - 1>();  // segment s (this thread's copies) has landed
+                const unsigned char* st = slot + u * kW4MmaStageBytes;
+                const uint4 w0 = *reinterpret_cast<const uint4*>(st);         // row g, chunk t
+                const uint4 w1 = *reinterpret_cast<const uint4*>(st + 512);   // row g, chunk t + 4
+                const uint4 w2 = *reinterpret_cast<const uint4*>(st + 1024);  // row g + 8, chunk t
+                const uint4 w3 = *reinterpret_cast<const uint4*>(st + 1536);  // row g + 8, chunk t + 4
+                const int ce = s * 8 + t;  // chunk t of the segment
+                // four accumulators (one per code pair j): MMA chains of four
+                // instead of sixteen dependent MMAs per segment
+                float acc[4][4] = {};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (own_e) xe = *reinterpret_cast<const uint4*>(xs + int4_x_piece(ce, i, 4));
+                    if (own_o) xo = *reinterpret_cast<const uint4*>(xs + int4_x_piece(ce + 4, i, 4));
+                    uint32_t qa[4], qb[4], qc[4], qd[4];
+                    unpack_int4x8_f16(word_of(w0, i), qa);
+                    unpack_int4x8_f16(word_of(w1, i), qb);
+                    unpack_int4x8_f16(word_of(w2, i), qc);
+                    unpack_int4x8_f16(word_of(w3, i), qd);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        mma_m16n8k16_f16(acc[j], qa[j], qc[j], qb[j], qd[j], word_of(xe, j),
+                                         word_of(xo, j));
+                }
+                float d[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) d[e] = (acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e]);
+                yg = fmaf(d[0], __half2float(__ushort_as_half(sc[u][0])), yg);
+                yg = fmaf(d[1], __half2float(__ushort_as_half(sc[u][1])), yg);
+                yh = fmaf(d[2], __half2float(__ushort_as_half(sc[u][2])), yh);
+                yh = fmaf(d[3], __half2float(__ushort_as_half(sc[u][3])), yh);
+            }
+        }
+    }
+    cp_async_wait<0>();  // (only empty groups remain; the ring is free for reuse)
+    yg += __shfl_xor_sync(0xffffffffu, yg, 1);
+    yh += __shfl_xor_sync(0xffffffffu, yh, 1);
+    yg += __shfl_xor_sync(0xffffffffu, yg, 2);
+    yh += __shfl_xor_sync(0xffffffffu, yh, 2);
+    return make_float2(yg, yh);
+}
+
+// Where k_gemv's warps' weight rings begin (after its activations, row-group
+// partials and argmax candidates).
+template <class P>
+__host__ __device__ size_t w4_ring_offset(int MT, int K) {
+    const bool direct = P::kDirectX && MT == 1;
+    size_t x = direct ? 0 : (P::x_bytes(MT, K) + 15) & ~(size_t)15;
+    return (x + (size_t)kWarps * 4 * MT * 4 + (size_t)kWarps * sizeof(ArgPart) + 15) &
+           ~(size_t)15;
+}
+
+// The per-launch kernel takes this path for W4A16, one token, R = 16.
+template <class P, int MT, int R>
+struct W4Mma {
+    static constexpr bool v = std::is_same<P, PolicyW4A16>::value && MT == 1 && R == kW4MmaRows;
+};
+
 // ---- the row-group computation shared by all kernels ------------------------------
 
 // Chunks per row loaded ahead of use: about eight loads in flight per lane.
@@ -617,6 +786,69 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvP
     float best_v = NAN;
     int best_i = INT_MAX;
 
+    if constexpr (W4Mma<P, MT, R>::v) {
+        // one warp per tile of 16 rows (ksplit = 1), on the tensor cores
+        const int nseg = g.K / kW4MmaSeg;
+        int sbeg = 0, send = nseg;
+        if constexpr (SPLIT) {
+            sbeg = (int)((long long)nseg * sidx / S);
+            send = (int)((long long)nseg * (sidx + 1) / S);
+        }
+        const int q = lane >> 2, t = lane & 3;
+        unsigned char* ring = smem + w4_ring_offset<P>(1, g.K) + (size_t)warp * kW4MmaRingBytes;
+        for (int it = 0; it < p.iters; ++it) {
+            const int tile = (it * gx + bx) * slots + slot;
+            if (tile >= n_rg) continue;
+            const int r0 = tile * kW4MmaRows;
+            RowRef z{};
+            const RowRef first = locate(p.t, r0, g.rb, z);
+            // rows past the end alias the tile's first row (loaded, dropped)
+            const RowRef ra = locate(p.t, r0 + q, g.rb, first);
+            const RowRef rb = locate(p.t, r0 + q + 8, g.rb, first);
+            const float2 y = w4a16_mma_rows(
+                ra.w, rb.w, static_cast<const uint16_t*>(ra.scale) + (size_t)ra.local * g.gk,
+                static_cast<const uint16_t*>(rb.scale) + (size_t)rb.local * g.gk, xsrc, sbeg, send,
+                g.cpg, ring);
+            if constexpr (ARGMAX) {
+                float v = NAN;
+                int i = INT_MAX;
+                if (t == 0) {
+                    if (ra.valid) {
+                        p.logits[ra.global] = y.x;
+                        v = y.x;
+                        i = ra.global;
+                    }
+                    if (rb.valid) {
+                        p.logits[rb.global] = y.y;
+                        if (arg_better(y.y, rb.global, v, i)) {
+                            v = y.y;
+                            i = rb.global;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+                    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+                    if (arg_better(ov, oi, v, i)) {
+                        v = ov;
+                        i = oi;
+                    }
+                }
+                if (lane == 0 && arg_better(v, i, best_v, best_i)) {
+                    best_v = v;
+                    best_i = i;
+                }
+            } else if constexpr (SPLIT) {
+                int* part = static_cast<int*>(p.kpart) + (size_t)sidx * p.t.N;
+                if (t == 0 && ra.valid) part[ra.global] = to_bits(y.x);
+                if (t == 1 && rb.valid) part[rb.global] = to_bits(y.y);
+            } else {
+                if (t == 0 && ra.valid) P::store(ra, 0, y.x, 1.f);
+                if (t == 1 && rb.valid) P::store(rb, 0, y.y, 1.f);
+            }
+        }
+    } else {
     for (int it = 0; it < p.iters; ++it) {
         const int rg = (it * gx + bx) * slots + slot;
         const bool active = rg < n_rg;
@@ -654,6 +886,7 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvP
                 }
             }
         }
+    }
     }
 
     if (ARGMAX) {
@@ -698,10 +931,15 @@ __global__ void __launch_bounds__(256) k_split_finish(const __grid_constant__ Ge
     }
 }
 
+// Shared memory of k_gemv: staged activations | row-group partials | per-warp
+// argmax candidates | (W4A16 tensor-core tiles, R = kW4MmaRows) the warps'
+// weight rings from w4_ring_offset on.
 template <class P>
-size_t smem_bytes_for(int MT, int K) {
+size_t smem_bytes_for(int MT, int K, int R = 0) {
     const bool direct = P::kDirectX && MT == 1;
     size_t x = direct ? 0 : (P::x_bytes(MT, K) + 15) & ~(size_t)15;
+    if (std::is_same<P, PolicyW4A16>::value && MT == 1 && R == kW4MmaRows)
+        return w4_ring_offset<P>(MT, K) + (size_t)kWarps * kW4MmaRingBytes;
     return x + (size_t)kWarps * 4 * MT * 4 + (size_t)kWarps * sizeof(ArgPart);
 }
 
@@ -727,6 +965,10 @@ cudaError_t run_r(int R, const GemvParams* p, int grid, size_t smem, cudaStream_
         case 1: return run_one<P, MT, 1, ARGMAX>(p, grid, smem, s, occ);
         case 2: return run_one<P, MT, 2, ARGMAX>(p, grid, smem, s, occ);
         case 4: return run_one<P, MT, 4, ARGMAX>(p, grid, smem, s, occ);
+        case kW4MmaRows:  // W4A16 at one token: tiles on the tensor cores
+            if constexpr (W4Mma<P, MT, kW4MmaRows>::v)
+                return run_one<P, MT, kW4MmaRows, ARGMAX>(p, grid, smem, s, occ);
+            return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
 }
@@ -734,7 +976,7 @@ cudaError_t run_r(int R, const GemvParams* p, int grid, size_t smem, cudaStream_
 // The instantiations the launch heuristic can pick.
 template <class P>
 cudaError_t run_family_main(const GemvLaunch& L, const GemvParams* p, cudaStream_t s, int* occ) {
-    const size_t smem = smem_bytes_for<P>(L.MT, L.K);
+    const size_t smem = smem_bytes_for<P>(L.MT, L.K, L.R);
     if (L.argmax) {
         if constexpr (P::kIntAct && P::kElems == 16) {
             return cudaErrorInvalidValue;  // no int8 lm_head
