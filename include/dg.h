@@ -44,6 +44,12 @@
  *    and, within that path, still depends only on K.
  *  - Alignment.  W, x, xq and y must be 16-byte aligned; K must be a multiple
  *    of 8 (fp16/bf16), 16 (int8) or 32 (int4).
+ *  - Tuning.  The environment variable DG_TUNE (comma-separated KEY=value,
+ *    read once per process) overrides launch choices for configuration
+ *    sweeps; unset, the defaults above hold.  Every setting stays within the
+ *    parity bound; KS, KS8 (warps per row), KP (split-K ranges), MMA (tensor-
+ *    core tiles off / int8 tile) and W4MMA=1 (W4A16 at one token on the tensor
+ *    cores) change a row's summation order, the others only the schedule.
  */
 #ifndef DG_H_
 #define DG_H_
