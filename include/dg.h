@@ -166,14 +166,18 @@ dg_status dg_lm_head_argmax(const dg_linear* head, void* ws, size_t ws_bytes, dg
  * a plugin whose host runtime owns all device memory through its own pool, or
  * code whose memory plan was fixed ahead of time.  (The pages have no
  * counterpart to this entry point.)  Same inputs, outputs and results as
- * dg_lm_head_argmax; the per-CTA partials live in a fixed 8 KB array inside
- * the library (1024 partials; every GPU that loads the library keeps it until
- * the process exits).
+ * dg_lm_head_argmax (the same kernels and launch configuration, so the same
+ * bits); the per-CTA partials live in a fixed 16 KB array inside the library
+ * (2048 partials; every GPU that loads the library keeps it until the
+ * process exits).  A head launches at most SMs x 8 CTAs (1216 on a 152-SM
+ * GB300), so every head fits there.
  *  - The first call on a device looks up that array's address (with the
  *    device current) and caches it: make that first call before any stream
- *    capture.  No call allocates or frees memory.
- *  - A head that would need more than 1024 partials returns DG_ERR_WORKSPACE
- *    and launches nothing.
+ *    capture.  The cached address belongs to the device's primary context:
+ *    do not keep using the library across a cudaDeviceReset of that device.
+ *    No call allocates or frees memory.
+ *  - A head that would need more than 2048 partials (a GPU with more than 256
+ *    SMs) returns DG_ERR_WORKSPACE and launches nothing.
  *  - Every call shares the array; nothing in it needs to start at zero (each
  *    call writes every partial it reads).  Calls that can overlap on the GPU
  *    (different streams, or different host threads on one device) race on the

@@ -11,14 +11,18 @@
 // library holds its kStaticArgParts * 8 bytes until the process exits.  Host
 // code cannot use the array's name as a device address, so the first call on
 // each device looks the address up with cudaGetSymbolAddress (with that device
-// current) and caches it; later calls reuse it.
+// current) and caches it; later calls reuse it.  The cache is keyed by
+// device ordinal only: a cudaDeviceReset invalidates it (documented in dg.h).
 #include <mutex>
 
 #include "dg_internal.cuh"
 
 namespace dg {
 
-constexpr int kStaticArgParts = 1024;  // 8 KB: one (value, index) per CTA
+// 16 KB: one (value, index) per CTA.  A head's grid is at most SMs x 8 CTAs
+// (k_gemv runs 256 threads and configure() caps CTAs per SM at 8): 1216 on a
+// 152-SM GB300, so the rejection below only triggers above 256 SMs.
+constexpr int kStaticArgParts = 2048;
 
 static __device__ __align__(256) ArgPart g_static_arg_parts[kStaticArgParts];
 

@@ -56,6 +56,10 @@ class DeviceStep:
     head_token: Optional[torch.Tensor] = None
     head_input: Optional[torch.Tensor] = None
     keep: list = field(default_factory=list)
+    # W4A8: per layer, input name -> (int8 codes [M][K], fp32 scale [M]) that
+    # the step writes when it quantizes that input (empty for W4A16)
+    act_codes: List[Dict[str, tuple]] = field(default_factory=list)
+    head_codes: Optional[tuple] = None
 
 
 def _nbytes(t):
@@ -154,6 +158,7 @@ def int4_decode_step(layers, head, x_head, device, act="a16", M=1, group=32) -> 
                     aout.reserve((head.N,), torch.float32), aout.reserve((1,), torch.int32))
     in_views, out_views = ain.build(device), aout.build(device)
     ops, keep, ins, outs = [], [], [], []
+    codes = []
     wbytes = 0
 
     def qbufs(x):
@@ -170,6 +175,7 @@ def int4_decode_step(layers, head, x_head, device, act="a16", M=1, group=32) -> 
             xin[k] = in_views[iid[k]]
             xin[k].copy_(v)
         qin = {k: qbufs(v) for k, v in xin.items()}
+        codes.append({k: v for k, v in qin.items() if v[0] is not None})
         ys = {}
         for lin in L.linears:
             W, S = lin.W.to(device), lin.scales.to(device)
@@ -183,12 +189,14 @@ def int4_decode_step(layers, head, x_head, device, act="a16", M=1, group=32) -> 
         ins.append(xin)
         outs.append(ys)
     logits = token = xh = None
+    hcodes = None
     if head is not None:
         W, S = head.W.to(device), head.scales.to(device)
         xh = in_views[head_ids[0]]
         xh.copy_(x_head)
         logits, token = out_views[head_ids[1]], out_views[head_ids[2]]
         xq, xs = qbufs(xh)
+        hcodes = (xq, xs) if xq is not None else None
         ops.append(linear(kind, W, 1, head.N, head.K, w_scale=S, x=xh, x_i8=xq, x_scale=xs,
                           logits=logits, token=token, group_size=group))
         keep += [W, S]
@@ -197,4 +205,4 @@ def int4_decode_step(layers, head, x_head, device, act="a16", M=1, group=32) -> 
     plan = StepPlan(ops, keep)
     ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=device)
     return DeviceStep(plan, ws, ins, outs, ain.buf, aout.buf, wbytes, count_launches(ops),
-                      logits, token, xh, keep=keep)
+                      logits, token, xh, keep=keep, act_codes=codes, head_codes=hcodes)

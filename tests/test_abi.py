@@ -111,6 +111,27 @@ def test_lm_head_validation_and_workspace(lib):
     assert dg.workspace_bytes([plain]) == 256  # the persistent step's barrier words
 
 
+def test_lm_head_noalloc_validation(lib):
+    """The workspace-free lm_head rejects bad heads on the host before any
+    CUDA call, with the statuses dg_lm_head_argmax uses."""
+    f = lib.dg_lm_head_argmax_noalloc
+    assert f(None, None) == INVALID
+    assert f(ctypes.byref(_head(token=None)), None) == INVALID
+    assert f(ctypes.byref(_head(logits=None)), None) == INVALID
+    assert f(ctypes.byref(_head(M=2)), None) == INVALID
+    assert f(ctypes.byref(_head(W=None)), None) == INVALID
+    assert f(ctypes.byref(_head(x=None)), None) == INVALID
+    assert f(ctypes.byref(_head(W=ODD)), None) == MISALIGNED
+    assert f(ctypes.byref(_head(K=60)), None) == MISALIGNED
+    assert f(ctypes.byref(_head(token=B + 2)), None) == MISALIGNED
+    assert f(ctypes.byref(_head(kind=dg.LINEAR_W8A8, w_scale=A, x_i8=A, x_scale=A, x=None)),
+             None) == UNSUPPORTED
+    # the package wrapper raises the same status
+    with pytest.raises(dg.DGError) as e:
+        dg.lm_head_argmax_noalloc(_head(M=2), stream=0)
+    assert e.value.status == INVALID
+
+
 def test_workspace_covers_split_k_partials_of_small_ops():
     # a per-op call with at most 65536 outputs may split K into up to 8 ranges
     # of M x N fp32 / int32 partials; larger ones never split

@@ -59,31 +59,93 @@ def int4_workload():
     return synth.decode_int4_workload(seed=0)
 
 
+def _slice_edge_rows(N, grids):
+    """Rows of an N-row phase next to the persistent kernel's CTA slice
+    boundaries (CTA b of G starts at floor(N b / G)), plus the first and last."""
+    rows = {0, N - 1}
+    for G in grids:
+        for b in range(1, G):
+            r = N * b // G
+            rows.update((r - 1, r))
+    return rows
+
+
+def _phase_rows(L, grids):
+    """For every matrix of a decoder layer: its rows at the slice edges of the
+    fused phase it belongs to (q|k|v, o, gate|up, down), in its own numbering."""
+    phases, cur, prev = [], [], None
+    for lin in L.linears:
+        if cur and lin.x_name != prev:
+            phases.append(cur)
+            cur = []
+        cur.append(lin)
+        prev = lin.x_name
+    phases.append(cur)
+    out = {}
+    for ph in phases:
+        N = sum(l.N for l in ph)
+        edges = _slice_edge_rows(N, grids)
+        base = 0
+        for l in ph:
+            out[l.name] = sorted({r - base for r in edges if base <= r < base + l.N} |
+                                 {0, l.N - 1})
+            base += l.N
+    return out
+
+
+def _check_codes(layers, codes, head_x=None, head_codes=None):
+    """The int8 codes and fp32 scales the step's quantizer wrote equal the
+    oracle's quantizer bit for bit."""
+    n = 0
+    for li, (L, qc) in enumerate(zip(layers, codes)):
+        for name, (xq, xs) in qc.items():
+            q, s = oracle.quant_act(bits(L.inputs[name]))
+            assert np.array_equal(xq.cpu().numpy(), q), "codes layer %d %s" % (li, name)
+            assert np.array_equal(xs.cpu().numpy().view(np.uint32), s.view(np.uint32)), \
+                "scale layer %d %s" % (li, name)
+            n += 1
+    if head_codes is not None:
+        q, s = oracle.quant_act(bits(head_x))
+        assert np.array_equal(head_codes[0].cpu().numpy(), q), "lm_head codes"
+        assert np.array_equal(head_codes[1].cpu().numpy().view(np.uint32), s.view(np.uint32))
+        n += 1
+    return n
+
+
 @pytest.mark.parametrize("act", ["a16", "a8"])
 def test_int4_decoder_step(int4_workload, act):
+    """Every row of every matrix of one layer; in all 32 layers, the rows at
+    the CTA slice boundaries of each fused phase (for one and two CTAs per SM)
+    and the first and last row of every matrix; the whole lm_head; (W4A8) the
+    codes and scales the step's quantizer wrote, bitwise."""
     layers, head, x_head = int4_workload
     step = plans.int4_decode_step(layers, head, x_head, DEV, act=act)
     assert step.weight_bytes == 4221370368
     dg.decode_step_weights(step.plan, step.ws)
     sync()
-    rng = np.random.default_rng(0)
-    for li in (0, 13, 31):
-        L = layers[li]
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    grids = (sms, 2 * sms)
+    full_layer = 13
+    for li, L in enumerate(layers):
+        edge = _phase_rows(L, grids)
         for lin in L.linears:
-            rows = rng.integers(0, lin.N, 96)
+            rows = None if li == full_layer else np.array(edge[lin.name], np.int64)
             x = L.inputs[lin.x_name]
             if act == "a16":
                 yr, A = oracle.gemv_w4a16(lin.W.numpy(), bits(lin.scales), bits(x), rows=rows)
             else:
                 q, s = oracle.quant_act(bits(x))
                 yr, A, _ = oracle.gemv_w4a8(lin.W.numpy(), bits(lin.scales), q, s, rows=rows)
-            y = step.outputs[li][lin.name].cpu().double().numpy()[:, rows]
+            y = step.outputs[li][lin.name].cpu().double().numpy()
+            if rows is not None:
+                y = y[:, rows]
             tol.assert_close(y, yr, A, "f16", "%s layer %d %s" % (act, li, lin.name))
     if act == "a16":
         lr, A = oracle.gemv_w4a16(head.W.numpy(), bits(head.scales), bits(x_head))
     else:
         q, s = oracle.quant_act(bits(x_head))
         lr, A, _ = oracle.gemv_w4a8(head.W.numpy(), bits(head.scales), q, s)
+        assert _check_codes(layers, step.act_codes, x_head, step.head_codes) == 4 * 32 + 1
     logits = step.head_logits.cpu().double().numpy()
     tol.assert_close(logits, lr[0], A[0], "f32", "%s lm_head" % act)
     tok = int(step.head_token.item())
@@ -139,9 +201,8 @@ def test_persistent_step_equals_per_op_calls_bitwise_int4(act):
     ref = _per_op_outputs(list(step.plan.array))
     for a, b in zip(got, ref):
         assert torch.equal(a, b)
-    if act == "a8":  # the codes the step wrote equal the oracle's quantizer
-        for L in layers:
-            pass
+    if act == "a8":  # the codes and scales the step wrote equal the oracle's quantizer
+        assert _check_codes(layers, step.act_codes, xh, step.head_codes) == 4 * 2 + 1
     # the lm_head token against the oracle
     if act == "a16":
         lr, A = oracle.gemv_w4a16(head.W.numpy(), bits(head.scales), bits(xh))
