@@ -47,9 +47,9 @@
  *  - Tuning.  The environment variable DG_TUNE (comma-separated KEY=value,
  *    read once per process) overrides launch choices for configuration
  *    sweeps; unset, the defaults above hold.  Every setting stays within the
- *    parity bound; KS, KS8 (warps per row), KP (split-K ranges), MMA (tensor-
- *    core tiles off / int8 tile) and W4MMA=1 (W4A16 at one token on the tensor
- *    cores) change a row's summation order, the others only the schedule.
+ *    parity bound; KS, KS8 (warps per row), KP (split-K ranges) and MMA
+ *    (tensor-core tiles off / int8 tile) change a row's summation order, the
+ *    others only the schedule.
  */
 #ifndef DG_H_
 #define DG_H_

@@ -76,7 +76,6 @@ struct Tune {
     int RING = -1, TSB = 0, TNS = 0, TNC = 0;  // weight ring: on/off, KB per stage, stages, consumers
     int KP = 0;                                // split-K ranges of a per-op launch (1 = off)
     int KS8 = -1;                              // rows of >= 16 KB split over 8 warps
-    int W4MMA = -1;                            // W4A16 at one token on the tensor cores
 };
 
 static Tune read_tune() {
@@ -103,7 +102,6 @@ static Tune read_tune() {
         else if (std::sscanf(tok, "TNC=%d", &v) == 1) t.TNC = v;
         else if (std::sscanf(tok, "KP=%d", &v) == 1) t.KP = v;
         else if (std::sscanf(tok, "KS8=%d", &v) == 1) t.KS8 = v;
-        else if (std::sscanf(tok, "W4MMA=%d", &v) == 1) t.W4MMA = v;
     }
     return t;
 }
@@ -152,21 +150,13 @@ static int pick_ks(Fmt f, int K) {
     return 1;
 }
 
-// W4A16 at one token on the tensor cores (tiles of kW4MmaRows rows, one warp
-// each, K whole; K a multiple of kW4MmaSeg), selected with DG_TUNE=W4MMA=1.
-// Measured slower than the CUDA-core path on the int4 decoder (32-layer step
-// 1213-1663 us against 1235 us; fused gate|up 28-33 us against 23.6 us), so
-// not the default.
-static bool w4_mma(Fmt f, int MT, int K) {
-    return f == F_W4A16 && MT == 1 && K % kW4MmaSeg == 0 && tune().W4MMA == 1 &&
-           tune().MMA != 0 && w4_mma_smem(K) <= smem_optin_limit();
-}
-
+// Rows per slot.  At one token: W4A16 four (its MAC loads each activation
+// piece once for all rows of the slot), W4A8 two, fp16 / bf16 and int8 one.
 static int pick_r(Fmt f, int MT, int K) {
-    if (w4_mma(f, MT, K)) return kW4MmaRows;
+    (void)K;
     const int t = tune().R;
     if (t == 1 || t == 2 || t == 4) return t;
-    if (MT == 1) return (f == F_W4A16 || f == F_W4A8) ? 2 : 1;
+    if (MT == 1) return f == F_W4A16 ? 4 : f == F_W4A8 ? 2 : 1;
     if (MT <= 4) return 2;
     if (f == F_I8) return MT >= 16 ? 4 : 2;
     return 1;
@@ -204,7 +194,7 @@ static int occupancy(const GemvLaunch& L) {
 
 // Fills L.grid and p.iters / ksplit / prefetch for a launch over p.N rows.
 static void configure(GemvLaunch& L, GemvParams& p) {
-    const int ks = L.R == kW4MmaRows ? 1 : pick_ks(L.fmt, p.a.K);
+    const int ks = pick_ks(L.fmt, p.a.K);
     const int slots = kWarps / ks;
     const int n_rg = (p.t.N + L.R - 1) / L.R;
     const int need = (n_rg + slots - 1) / slots;
@@ -358,12 +348,11 @@ static dg_status launch_i8_mma(GemvParams& p, cudaStream_t s) {
 // each), CTAs write fp32 / int32 partials to the workspace and a second kernel
 // adds them in range order.  S follows the op's shape and the SM count.
 static int pick_kparts(const GemvLaunch& L, int N, int K) {
-    const bool mma = L.R == kW4MmaRows;
-    const int ks = mma ? 1 : pick_ks(L.fmt, K), slots = kWarps / ks;
+    const int ks = pick_ks(L.fmt, K), slots = kWarps / ks;
     const int n_rg = (N + L.R - 1) / L.R, need = (n_rg + slots - 1) / slots;
     const int kelems = (L.fmt == F_F16 || L.fmt == F_BF16) ? 8 : L.fmt == F_I8 ? 16 : 32;
-    // chunks per lane (segments per warp on the tensor-core tile)
-    const int J = mma ? K / kW4MmaSeg : (K / kelems + ks * 32 - 1) / (ks * 32);
+    // chunks per lane
+    const int J = (K / kelems + ks * 32 - 1) / (ks * 32);
     int S = tune().KP;
     if (S <= 0) {
         const int sms = sm_count();
@@ -520,12 +509,12 @@ static bool step_eligible(const dg_linear& op) { return op.M == 1 && !op.acc_out
 
 // CTAs of the step kernel per SM (ring_nc = 0: k_step; else k_step_ring
 // with that many consumer warps).
-static int step_occupancy(Fmt f, int max_k, size_t smem, int ring_nc, int nw, bool w4m) {
+static int step_occupancy(Fmt f, int max_k, size_t smem, int ring_nc, int nw) {
     static std::mutex mu;
-    static std::map<std::tuple<int, int, int, size_t, int, int, int>, int> cache;
+    static std::map<std::tuple<int, int, int, size_t, int, int>, int> cache;
     int dev = 0;
     cudaGetDevice(&dev);
-    const auto key = std::make_tuple(dev, (int)f, max_k, smem, ring_nc, nw, (int)w4m);
+    const auto key = std::make_tuple(dev, (int)f, max_k, smem, ring_nc, nw);
     {
         std::lock_guard<std::mutex> g(mu);
         auto it = cache.find(key);
@@ -534,7 +523,7 @@ static int step_occupancy(Fmt f, int max_k, size_t smem, int ring_nc, int nw, bo
     StepParams* none = nullptr;
     int occ = 0;
     const cudaError_t e = ring_nc ? step_ring_launch(f, none, 0, smem, nullptr, &occ, ring_nc)
-                                  : step_launch(f, none, 0, smem, nullptr, &occ, nw, w4m);
+                                  : step_launch(f, none, 0, smem, nullptr, &occ, nw);
     if (e != cudaSuccess) occ = 0;
     std::lock_guard<std::mutex> g(mu);
     cache[key] = occ;
@@ -640,15 +629,6 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
     static thread_local StepParams sp;
     const Fmt f = fmt_of(ops[0].kind);
     const bool always_sync = tune().STEP == 2;  // barrier between every pair of phases
-    // W4A16 on the tensor cores when every op of the run allows it and the
-    // warps' weight rings fit beside the activation buffers
-    bool w4m = true;
-    int run_k = 0;
-    for (int k = 0; k < n; ++k) {
-        w4m = w4m && w4_mma(f, 1, ops[k].K);
-        run_k = ops[k].K > run_k ? ops[k].K : run_k;
-    }
-    w4m = w4m && step_smem(f, run_k, true) <= smem_optin_limit();
     int i = 0;
     while (i < n) {
         std::memset(&sp, 0, sizeof sp);
@@ -691,7 +671,7 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
             ph.N = rows;
             ph.K = a.K;
             ph.group = a.group_size >= 32 ? a.group_size : 32;
-            ph.ks = w4m ? 1 : pick_ks(f, a.K);
+            ph.ks = pick_ks(f, a.K);
             ph.x = a.x;
             ph.xq = a.x_i8;
             ph.x_scale = const_cast<float*>(a.x_scale);
@@ -777,7 +757,7 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
                 }
             }
         }
-        if (!ring_nc) smem = step_smem(f, max_k, w4m);
+        if (!ring_nc) smem = step_smem(f, max_k);
         if (smem > smem_optin_limit()) return DG_ERR_UNSUPPORTED;
         // k_step runs 16 warps; W4A8 20 (one more row group in flight per SM
         // sub-partition: 883 -> 863 us for the 32-layer step) when no phase
@@ -786,13 +766,13 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
         bool split = false;
         for (int q = 0; q < sp.nphase; ++q) split = split || sp.ph[q].ks > 1;
         const int nw = split ? 16 : tune().SNW > 0 ? tune().SNW : f == F_W4A8 ? 20 : 16;
-        const int occ = step_occupancy(f, max_k, smem, ring_nc, nw, w4m);
+        const int occ = step_occupancy(f, max_k, smem, ring_nc, nw);
         if (occ < 1) return DG_ERR_UNSUPPORTED;
         const int grid = sm_count() * occ;
         if (grid > kMaxArgCtas) return DG_ERR_UNSUPPORTED;
         if (cudaMemsetAsync(ws, 0, 2 * sizeof(unsigned), s) != cudaSuccess) return DG_ERR_CUDA;
         const cudaError_t e = ring_nc ? step_ring_launch(f, &sp, grid, smem, s, nullptr, ring_nc)
-                                      : step_launch(f, &sp, grid, smem, s, nullptr, nw, w4m);
+                                      : step_launch(f, &sp, grid, smem, s, nullptr, nw);
         if (e != cudaSuccess) return DG_ERR_CUDA;
     }
     return DG_OK;

@@ -51,12 +51,6 @@ struct ArgPart {
     int32_t i;
 };
 
-// W4A16 at one token on the tensor cores (K a multiple of kW4MmaSeg): one
-// warp per tile of kW4MmaRows rows, K in segments of kW4MmaSeg codes (eight
-// 32-code chunks, one per column of the MMA's B operand).
-constexpr int kW4MmaRows = 16;
-constexpr int kW4MmaSeg = 256;
-
 struct GemvParams {
     SegTable t;
     ActIn a;
@@ -291,7 +285,7 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaS
 struct GemvLaunch {
     Fmt fmt;
     int MT;        // token tile: 1, 2, 4, 8 or 16 (>= M)
-    int R;         // rows per slot: 1, 2 or 4; kW4MmaRows: W4A16 tensor-core tile (one warp)
+    int R;         // rows per slot: 1, 2 or 4
     bool argmax;   // lm_head epilogue (MT == 1)
     int K, group;
     int grid;
@@ -319,18 +313,15 @@ int head_grid(const dg_linear& op);
 
 // Persistent decode-step kernel (step_kernel.cu): one cooperative launch over
 // sp.nphase phases of format f, with nw warps per CTA (16, or 0 for the
-// format's default); w4m: W4A16 phases on the tensor cores (every phase's K a
-// multiple of kW4MmaSeg, ks = 1).  occ != nullptr: report CTAs per SM instead.
+// format's default).  occ != nullptr: report CTAs per SM instead.
 cudaError_t step_launch(Fmt f, const StepParams* sp, int grid, size_t smem, cudaStream_t s,
-                        int* occ, int nw, bool w4m);
+                        int* occ, int nw);
 // The weight-ring variant of the persistent step (fp16 / bf16 weights, one
 // token): `nc` consumer warps (8 or 12) plus one producer warp per CTA.
 size_t step_ring_overhead(int nc);
 cudaError_t step_ring_launch(Fmt f, const StepParams* sp, int grid, size_t smem, cudaStream_t s,
                              int* occ, int nc);
-size_t step_smem(Fmt f, int max_k, bool w4m);
-// Shared memory of a W4A16 per-op launch on the tensor-core tile.
-size_t w4_mma_smem(int K);
+size_t step_smem(Fmt f, int max_k);
 cudaError_t launch_wait_selftest(unsigned limit, int* err, cudaStream_t s);
 
 cudaError_t launch_argmax_pass2(const ArgPart* part, int nparts, int32_t* token, cudaStream_t s);

@@ -94,6 +94,7 @@ __device__ __forceinline__ float2 unpack2_f32(uint32_t w) {
 template <bool BF16>
 struct PolicyFP {
     static constexpr int kElems = 8;
+    static constexpr bool kMacRows = false;  // one row per mac() call
     static constexpr bool kIntAct = false;
     static constexpr bool kDirectX = true;  // M = 1 reads x from global memory
     using Acc = float;
@@ -111,8 +112,9 @@ struct PolicyFP {
             dst[i] = m < a.M ? src[i] : make_uint4(0, 0, 0, 0);
         }
     }
-    __device__ __forceinline__ static void load(Chunk& ch, const RowRef& r, int c, int, int) {
-        ch.w = ld_stream16(r.w + (size_t)c * 16);
+    __device__ __forceinline__ static void load(Chunk& ch, const unsigned char* wrow, const uint16_t*,
+                                                int c, int) {
+        ch.w = ld_stream16(wrow + (unsigned)c * 16u);
     }
     __device__ __forceinline__ static float mac2(uint32_t w, uint32_t x, float a) {
         if (BF16) {
@@ -163,6 +165,7 @@ struct PolicyFP {
 // int8 weights x int8 activations, exact int32 sums; 16 elements per chunk.
 struct PolicyI8 {
     static constexpr int kElems = 16;
+    static constexpr bool kMacRows = false;  // one row per mac() call
     static constexpr bool kIntAct = true;
     static constexpr bool kDirectX = false;
     using Acc = int;
@@ -180,8 +183,9 @@ struct PolicyI8 {
             dst[i] = m < a.M ? src[i] : make_uint4(0, 0, 0, 0);
         }
     }
-    __device__ __forceinline__ static void load(Chunk& ch, const RowRef& r, int c, int, int) {
-        ch.w = ld_stream16(r.w + (size_t)c * 16);
+    __device__ __forceinline__ static void load(Chunk& ch, const unsigned char* wrow, const uint16_t*,
+                                                int c, int) {
+        ch.w = ld_stream16(wrow + (unsigned)c * 16u);
     }
     template <int MT>
     __device__ __forceinline__ static void mac(Acc (&acc)[MT], const Chunk& ch,
@@ -226,6 +230,10 @@ __device__ __forceinline__ void unpack_int4x8_f16(uint32_t w, uint32_t (&q)[4]) 
     q[3] = h2_as_u32(__hfma2(u32_as_h2(and_xor(w8, 0x00F000F0u, 0x64806480u)), k16th, k72));
 }
 
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
 // Shared-memory layout of int4 activations: chunk c (32 codes) of a token is
 // cut into 16-byte pieces, and piece i of chunk c sits at
 //     ((c / 32) * pieces + i) * 512 + (c % 32) * 16
@@ -236,12 +244,14 @@ __host__ __device__ __forceinline__ size_t int4_x_token_bytes(int K, int piece_b
     const size_t nch = (size_t)(K / 32);
     return ((nch + 31) / 32) * 32 * (size_t)piece_bytes_per_chunk;
 }
-// Scale group of chunk c when cpg chunks share a scale (no division in the
-// common case of one 32-code group per chunk).
-__device__ __forceinline__ int group_of_chunk(int c, int cpg) { return cpg == 1 ? c : c / cpg; }
+// Scale group of chunk c when cpg chunks share a scale: a shift when cpg is a
+// power of two (cps = log2 cpg), a division otherwise (cps < 0).
+__device__ __forceinline__ int group_of_chunk(int c, int cpg, int cps) {
+    return cps >= 0 ? c >> cps : c / cpg;
+}
 
-__device__ __forceinline__ size_t int4_x_piece(int c, int i, int pieces) {
-    return ((size_t)(c >> 5) * pieces + i) * 512 + (size_t)(c & 31) * 16;
+__device__ __forceinline__ unsigned int4_x_piece(int c, int i, int pieces) {
+    return ((unsigned)(c >> 5) * (unsigned)pieces + (unsigned)i) * 512u + (unsigned)(c & 31) * 16u;
 }
 
 // Groupwise int4 weights with fp16 activations; 32 codes per chunk.  Chunk c
@@ -251,7 +261,10 @@ __device__ __forceinline__ size_t int4_x_piece(int c, int i, int pieces) {
 // (x1,x5) (x2,x6) (x3,x7) of the chunk's i-th block of eight, lined up with the
 // unpacked code pairs.  Each code (exact in fp16) meets its activation in one
 // mixed-precision FMA (fp16 x fp16 + fp32: the product of a 4-bit code and an
-// 11-bit significand is exact, one rounding), in four chains, one per block.
+// 11-bit significand is exact, one rounding).  Per row and token a chunk runs
+// two chains (blocks 0 and 2, blocks 1 and 3, in ascending k), which meet once
+// before the group scale is applied.  All rows of a slot go through one call,
+// so each activation piece is loaded once for all of them.
 struct PolicyW4A16 {
     static constexpr int kElems = 32;
     static constexpr bool kIntAct = false;
@@ -277,38 +290,53 @@ struct PolicyW4A16 {
             *reinterpret_cast<uint4*>(xs + m * tb + int4_x_piece(blk >> 2, blk & 3, 4)) = o;
         }
     }
-    __device__ __forceinline__ static void load(Chunk& ch, const RowRef& r, int c, int gk, int cpg) {
-        ch.w = ld_stream16(r.w + (size_t)c * 16);
-        ch.s = ld_stream_u16(static_cast<const uint16_t*>(r.scale) + (size_t)r.local * gk +
-                             group_of_chunk(c, cpg));
+    // wrow: the row's codes; srow: the row's group scales; grp: chunk c's group
+    __device__ __forceinline__ static void load(Chunk& ch, const unsigned char* wrow,
+                                                const uint16_t* srow, int c, int grp) {
+        ch.w = ld_stream16(wrow + (unsigned)c * 16u);
+        ch.s = ld_stream_u16(srow + grp);
     }
-    template <int MT>
-    __device__ __forceinline__ static void mac(Acc (&acc)[MT], const Chunk& ch,
-                                               const unsigned char* xs, int c, int K) {
-        uint32_t q[4][4];
-        unpack_int4x8_f16(ch.w.x, q[0]);
-        unpack_int4x8_f16(ch.w.y, q[1]);
-        unpack_int4x8_f16(ch.w.z, q[2]);
-        unpack_int4x8_f16(ch.w.w, q[3]);
-        const float s = __half2float(__ushort_as_half(ch.s));
-        const size_t tb = token_bytes(K);
+    static constexpr bool kMacRows = true;  // mac_rows() takes the whole slot
+    template <int MT, int R>
+    __device__ __forceinline__ static void mac_rows(Acc (&acc)[R][MT], const Chunk (&ch)[R],
+                                                    const unsigned char* xs, int c, int K) {
+        mac_rows_at<MT, R>(acc, ch, xs + int4_x_piece(c, 0, 4), token_bytes(K));
+    }
+    // xc: piece 0 of the chunk's activations of token 0 (piece i at + 512 i,
+    // token m at + m tb)
+    template <int MT, int R>
+    __device__ __forceinline__ static void mac_rows_at(Acc (&acc)[R][MT], const Chunk (&ch)[R],
+                                                       const unsigned char* xc, size_t tb) {
+        float a[R][MT][2];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            const unsigned char* xb = xs + m * tb;
-            float P[4];
+        for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint4 xp = *reinterpret_cast<const uint4*>(xb + int4_x_piece(c, i, 4));
+            for (int m = 0; m < MT; ++m) a[r][m][0] = a[r][m][1] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {  // block i of the chunk: codes 8i .. 8i + 7
+            uint32_t q[R][4];
+#pragma unroll
+            for (int r = 0; r < R; ++r) unpack_int4x8_f16(word_of(ch[r].w, i), q[r]);
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                const uint4 xp = *reinterpret_cast<const uint4*>(xc + m * tb + i * 512);
                 const uint32_t xv[4] = {xp.x, xp.y, xp.z, xp.w};
-                float a = 0.f;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {  // (c_j, c_j+4) against (x_j, x_j+4)
-                    a = fma_f16(lo16(q[i][j]), lo16(xv[j]), a);
-                    a = fma_f16(hi16(q[i][j]), hi16(xv[j]), a);
+                for (int r = 0; r < R; ++r) {
+                    float& ar = a[r][m][i & 1];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {  // (c_j, c_j+4) against (x_j, x_j+4)
+                        ar = fma_f16(lo16(q[r][j]), lo16(xv[j]), ar);
+                        ar = fma_f16(hi16(q[r][j]), hi16(xv[j]), ar);
+                    }
                 }
-                P[i] = a;
             }
-            acc[m] = fmaf((P[0] + P[1]) + (P[2] + P[3]), s, acc[m]);
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float s = __half2float(__ushort_as_half(ch[r].s));
+#pragma unroll
+            for (int m = 0; m < MT; ++m) acc[r][m] = fmaf(a[r][m][0] + a[r][m][1], s, acc[r][m]);
         }
     }
     __device__ static float finish(const RowRef&, Acc a, float) { return a; }
@@ -326,6 +354,7 @@ struct PolicyW4A16 {
 // int32 sum of each 32-chunk.
 struct PolicyW4A8 {
     static constexpr int kElems = 32;
+    static constexpr bool kMacRows = false;  // one row per mac() call
     static constexpr bool kIntAct = true;
     static constexpr bool kDirectX = false;
     using Acc = float;
@@ -372,10 +401,11 @@ struct PolicyW4A8 {
             xsum[i] = s;
         }
     }
-    __device__ __forceinline__ static void load(Chunk& ch, const RowRef& r, int c, int gk, int cpg) {
-        ch.w = ld_stream16(r.w + (size_t)c * 16);
-        ch.s = ld_stream_u16(static_cast<const uint16_t*>(r.scale) + (size_t)r.local * gk +
-                             group_of_chunk(c, cpg));
+    // wrow: the row's codes; srow: the row's group scales; grp: chunk c's group
+    __device__ __forceinline__ static void load(Chunk& ch, const unsigned char* wrow,
+                                                const uint16_t* srow, int c, int grp) {
+        ch.w = ld_stream16(wrow + (unsigned)c * 16u);
+        ch.s = ld_stream_u16(srow + grp);
     }
     template <int MT>
     __device__ __forceinline__ static void mac(Acc (&acc)[MT], const Chunk& ch,
@@ -425,174 +455,6 @@ __device__ __forceinline__ int slot_barrier(int warp, int ks) {
     return ks == 4 ? 14 - warp / 4 : ks == 8 ? 9 + warp / 8 : 1 + warp / ks;
 }
 
-// ---- W4A16 at one token on the tensor cores ---------------------------------------
-//
-// On the CUDA cores each int4 weight with an fp16 activation costs about four
-// issued instructions (unpack, mixed FMA, activation load, loop), which holds
-// the stream far below HBM speed.  mma.sync m16n8k16 (fp16 operands, fp32
-// accumulation) takes the products and their sums off the FMA pipe: 16 weight
-// rows form the A operand, and the activations a B operand whose column n
-// collects chunk n (32 codes) of a 256-code segment, so that D[row][n] is the
-// chunk's partial sum; its group scale is applied afterwards in fp32.
-//
-// Thread (g = lane / 4, t = lane % 4) streams rows g and g + 8 of the tile
-// and, of every segment, chunks t and t + 4 (so one warp-wide copy reads 64
-// contiguous bytes of each of 8 rows).  In each of a segment's 16 MMAs its k
-// values 2t, 2t+1 are a code pair (c_j, c_j+4) of chunk t and its k values
-// 2t+8, 2t+9 the same pair of chunk t + 4 (the pairs unpack_int4x8_f16
-// yields).  Column n of B is then non-zero only in thread (g = n, t = n % 4),
-// fragment b0 for n < 4 and b1 for n >= 4, which holds the activations of that
-// pair in the interleaved layout; every other thread feeds zeros.  Thread
-// (g, t) finds D[g][2t], D[g][2t+1], D[g+8][2t], D[g+8][2t+1] in its
-// accumulator: the partials of chunks 2t and 2t + 1 of rows g and g + 8.  A
-// 4-bit code times an fp16 activation is exact; four independent MMA chains
-// (one per code pair) sum a chunk and are added in a fixed order; the lane
-// adds its scaled chunks in ascending order; a fixed xor butterfly joins the
-// quad.  The order follows K alone, never the row's place in the
-// tile, N or the grid.
-//
-// The host takes this path only on request: on the int4 decoder it measured
-// slower than the CUDA-core policy (PolicyW4A16) in every variant tried.
-//
-// Weights travel through a per-warp ring of kW4MmaStages segments in shared
-// memory, filled with cp.async kW4MmaStages - 1 segments ahead of use, so the
-// bytes in flight do not occupy registers.  Each thread reads back only the
-// 16-byte slots it copied itself: the copies' own completion (wait_group) is
-// the only ordering needed, and nothing waits on another thread.
-
-__device__ __forceinline__ void mma_m16n8k16_f16(float (&d)[4], uint32_t a0, uint32_t a1,
-                                                 uint32_t a2, uint32_t a3, uint32_t b0,
-                                                 uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
-    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
-
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* src) {
-    const unsigned d = (unsigned)__cvta_generic_to_shared(smem_dst);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-constexpr int kW4MmaStages = 3;                     // segments in a warp's ring
-constexpr int kW4MmaStageBytes = 4 * 32 * 16;       // 4 slots of 16 B per lane
-constexpr int kW4MmaRingBytes = kW4MmaStages * kW4MmaStageBytes;  // per warp
-
-// wg / wh: codes of rows g and g + 8 (K / 2 bytes each); sg / sh: their fp16
-// group scales; xs: the activations in the interleaved layout (shared or
-// global memory); segments [sbeg, send); cpg = group / 32; ring: this warp's
-// kW4MmaRingBytes of shared memory.  Returns the sums of rows g (.x) and
-// g + 8 (.y), complete in all four lanes of the quad.
-__device__ __forceinline__ float2 w4a16_mma_rows(const unsigned char* wg, const unsigned char* wh,
-                                                 const uint16_t* sg, const uint16_t* sh,
-                                                 const unsigned char* xs, int sbeg, int send,
-                                                 int cpg, unsigned char* ring) {
-    constexpr int S = kW4MmaStages;
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const bool own_e = g == t, own_o = g == t + 4;
-    unsigned char* slot = ring + lane * 16;  // slot j of stage st: + (st * 4 + j) * 512
-    uint16_t sc[S][4];                       // group scales of the segments in flight
-
-    // segment s into stage st: its four 16-byte pieces (rows g, g + 8;
-    // chunks t, t + 4) and, into registers, the scales of chunks 2t, 2t + 1
-    auto issue = [&](int s, int st) {
-        const size_t off = (size_t)s * (kW4MmaSeg / 2) + (size_t)t * 16;
-        unsigned char* d = slot + st * kW4MmaStageBytes;
-        cp_async16(d, wg + off);
-        cp_async16(d + 512, wg + off + 64);
-        cp_async16(d + 1024, wh + off);
-        cp_async16(d + 1536, wh + off + 64);
-        const int c0 = s * 8 + 2 * t;
-        const int ga = group_of_chunk(c0, cpg), gb = group_of_chunk(c0 + 1, cpg);
-        sc[st][0] = ld_stream_u16(sg + ga);
-        sc[st][1] = ld_stream_u16(sg + gb);
-        sc[st][2] = ld_stream_u16(sh + ga);
-        sc[st][3] = ld_stream_u16(sh + gb);
-    };
-
-    uint4 xe = make_uint4(0u, 0u, 0u, 0u), xo = xe;  // B fragments: owners only
-    float yg = 0.f, yh = 0.f;
-#pragma unroll
-    for (int u = 0; u < S - 1; ++u) {
-        if (sbeg + u < send) issue(sbeg + u, u);
-        cp_async_commit();
-    }
-    for (int s0 = sbeg; s0 < send; s0 += S) {
-#pragma unroll
-        for (int u = 0; u < S; ++u) {
-            const int s = s0 + u;
-            if (s < send) {
-                if (s + S - 1 < send) issue(s + S - 1, (u + S - 1) % S);
-                cp_async_commit();
-                cp_async_wait<S - 1>();  // segment s (this thread's copies) has landed
-                const unsigned char* st = slot + u * kW4MmaStageBytes;
-                const uint4 w0 = *reinterpret_cast<const uint4*>(st);         // row g, chunk t
-                const uint4 w1 = *reinterpret_cast<const uint4*>(st + 512);   // row g, chunk t + 4
-                const uint4 w2 = *reinterpret_cast<const uint4*>(st + 1024);  // row g + 8, chunk t
-                const uint4 w3 = *reinterpret_cast<const uint4*>(st + 1536);  // row g + 8, chunk t + 4
-                const int ce = s * 8 + t;  // chunk t of the segment
-                // four accumulators (one per code pair j): MMA chains of four
-                // instead of sixteen dependent MMAs per segment
-                float acc[4][4] = {};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    if (own_e) xe = *reinterpret_cast<const uint4*>(xs + int4_x_piece(ce, i, 4));
-                    if (own_o) xo = *reinterpret_cast<const uint4*>(xs + int4_x_piece(ce + 4, i, 4));
-                    uint32_t qa[4], qb[4], qc[4], qd[4];
-                    unpack_int4x8_f16(word_of(w0, i), qa);
-                    unpack_int4x8_f16(word_of(w1, i), qb);
-                    unpack_int4x8_f16(word_of(w2, i), qc);
-                    unpack_int4x8_f16(word_of(w3, i), qd);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        mma_m16n8k16_f16(acc[j], qa[j], qc[j], qb[j], qd[j], word_of(xe, j),
-                                         word_of(xo, j));
-                }
-                float d[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) d[e] = (acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e]);
-                yg = fmaf(d[0], __half2float(__ushort_as_half(sc[u][0])), yg);
-                yg = fmaf(d[1], __half2float(__ushort_as_half(sc[u][1])), yg);
-                yh = fmaf(d[2], __half2float(__ushort_as_half(sc[u][2])), yh);
-                yh = fmaf(d[3], __half2float(__ushort_as_half(sc[u][3])), yh);
-            }
-        }
-    }
-    cp_async_wait<0>();  // (only empty groups remain; the ring is free for reuse)
-    yg += __shfl_xor_sync(0xffffffffu, yg, 1);
-    yh += __shfl_xor_sync(0xffffffffu, yh, 1);
-    yg += __shfl_xor_sync(0xffffffffu, yg, 2);
-    yh += __shfl_xor_sync(0xffffffffu, yh, 2);
-    return make_float2(yg, yh);
-}
-
-// Where k_gemv's warps' weight rings begin (after its activations, row-group
-// partials and argmax candidates).
-template <class P>
-__host__ __device__ size_t w4_ring_offset(int MT, int K) {
-    const bool direct = P::kDirectX && MT == 1;
-    size_t x = direct ? 0 : (P::x_bytes(MT, K) + 15) & ~(size_t)15;
-    return (x + (size_t)kWarps * 4 * MT * 4 + (size_t)kWarps * sizeof(ArgPart) + 15) &
-           ~(size_t)15;
-}
-
-// The per-launch kernel takes this path for W4A16, one token, R = 16.
-template <class P, int MT, int R>
-struct W4Mma {
-    static constexpr bool v = std::is_same<P, PolicyW4A16>::value && MT == 1 && R == kW4MmaRows;
-};
-
 // ---- the row-group computation shared by all kernels ------------------------------
 
 // Chunks per row loaded ahead of use: about eight loads in flight per lane.
@@ -603,9 +465,11 @@ struct Unroll {
 
 // Geometry of one launch or phase, uniform over the CTA.
 struct RowGeom {
-    int K, nchunks, gk, cpg, ks;
+    int K, nchunks, gk, cpg, cps, ks;   // cps: log2(cpg), or -1 if cpg is no power of two
     size_t rb;
 };
+
+__device__ __forceinline__ int log2_or_neg(int v) { return (v & (v - 1)) == 0 ? __ffs(v) - 1 : -1; }
 
 template <class P>
 __device__ __forceinline__ RowGeom row_geom_gk(int K, int group, int ks, int gk) {
@@ -614,6 +478,7 @@ __device__ __forceinline__ RowGeom row_geom_gk(int K, int group, int ks, int gk)
     g.nchunks = K / P::kElems;
     g.gk = gk;
     g.cpg = group / 32;
+    g.cps = log2_or_neg(g.cpg);
     g.ks = ks;
     g.rb = P::row_bytes(K);
     return g;
@@ -626,6 +491,7 @@ __device__ __forceinline__ RowGeom row_geom(int K, int group, int ks) {
     g.nchunks = K / P::kElems;
     g.gk = K / group;
     g.cpg = group / 32;
+    g.cps = log2_or_neg(g.cpg);
     g.ks = ks;
     g.rb = P::row_bytes(K);
     return g;
@@ -645,6 +511,65 @@ __device__ __forceinline__ void rows_of(const SegTable& t, int rg, bool active, 
     }
 }
 
+// The slot loop of W4A16 at one token when one warp owns a row (ks = 1), the
+// whole row is summed (no split-K) and a scale group spans a power of two of
+// chunks, at most 32 (group <= 1024): lane l visits chunks l, l + 32, ... in
+// ascending order, U of them per batch, through row pointers advanced by
+// constant strides.  Same loads and the same arithmetic, in the same order,
+// as row_group, so the two give identical bits; this one issues fewer
+// integer instructions per chunk.
+template <class P, int R, int U>
+__device__ __forceinline__ void row_group_w4_ks1(const RowRef (&rows)[R], const RowGeom& g,
+                                                 const unsigned char* xs, float (&acc)[R][1]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[r][0] = 0.f;
+    const int nj = (g.nchunks - lane + 31) >> 5;   // this lane's chunks
+    const int sstep = 32 >> g.cps;                  // scale groups per 32 chunks
+    const unsigned char* wp[R];
+    const uint16_t* sp[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        wp[r] = rows[r].w + lane * 16;
+        sp[r] = static_cast<const uint16_t*>(rows[r].scale) + (size_t)rows[r].local * g.gk +
+                (lane >> g.cps);
+    }
+    const unsigned char* xp = xs + lane * 16;       // chunk lane + 32 j: + 2048 j
+    int j = 0;
+    for (; j + U <= nj; j += U) {
+        typename P::Chunk ch[U][R];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                ch[u][r].w = ld_stream16(wp[r] + u * 512);
+                ch[u][r].s = ld_stream_u16(sp[r] + u * sstep);
+            }
+#pragma unroll
+        for (int u = 0; u < U; ++u) P::template mac_rows_at<1, R>(acc, ch[u], xp + u * 2048, 0);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            wp[r] += U * 512;
+            sp[r] += U * sstep;
+        }
+        xp += U * 2048;
+    }
+    for (; j < nj; ++j) {
+        typename P::Chunk ch[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            ch[r].w = ld_stream16(wp[r]);
+            ch[r].s = ld_stream_u16(sp[r]);
+            wp[r] += 512;
+            sp[r] += sstep;
+        }
+        P::template mac_rows_at<1, R>(acc, ch, xp, 0);
+        xp += 2048;
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[r][0] = warp_sum(acc[r][0]);
+}
+
 // Streams R rows for this lane and returns the per-row sums, complete in every
 // lane of the slot's first warp (kw == 0).  With ks > 1 the slot's warps meet
 // at the slot's named barrier, so all of them must call it; inactive slots pass
@@ -659,7 +584,7 @@ __device__ __forceinline__ void row_group(const RowRef (&rows)[R], bool active, 
                                           typename P::Acc (&acc)[R][MT], bool coherent = false,
                                           int cbeg = 0, int cend = -1) {
     using Acc = typename P::Acc;
-    constexpr int U = UOVR > 0 ? UOVR : Unroll<MT, R>::v;
+    constexpr int UB = UOVR > 0 ? UOVR : Unroll<MT, R>::v;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int ks = g.ks;
     const int kw = warp % ks;
@@ -668,19 +593,41 @@ __device__ __forceinline__ void row_group(const RowRef (&rows)[R], bool active, 
 #pragma unroll
         for (int m = 0; m < MT; ++m) acc[r][m] = Acc(0);
 
+    if constexpr (P::kMacRows && MT == 1 && !DX) {
+        if (ks == 1 && cbeg == 0 && cend < 0 && g.cps >= 0 && g.cps <= 5) {
+            if (active) row_group_w4_ks1<P, R, UB>(rows, g, xs, acc);
+            return;
+        }
+    }
     if (active) {
         // Batches of U chunks per row, all loads of a batch issued before any
         // use (chunks past the row's end are skipped), so a short row costs one
         // memory round trip; the sums still run in ascending chunk order.
+        // W4A16 at one token reaches this general loop only for rare shapes
+        // (split rows, split-K, odd group sizes): one chunk per batch there
+        // keeps its registers below the fast loop's
+        constexpr int U = (P::kMacRows && MT == 1) ? 1 : UB;
         const int step = ks * 32;
         const int ce = cend < 0 ? g.nchunks : cend;
+        // per-row bases, once per row group: codes, and (int4) the group scales
+        const unsigned char* wrow[R];
+        const uint16_t* srow[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            wrow[r] = rows[r].w;
+            srow[r] = P::kElems == 32 ? static_cast<const uint16_t*>(rows[r].scale) +
+                                            (size_t)rows[r].local * g.gk
+                                      : nullptr;
+        }
         for (int c = cbeg + kw * 32 + lane; c < ce; c += U * step) {
             typename P::Chunk ch[U][R];
 #pragma unroll
             for (int u = 0; u < U; ++u)
-                if (c + u * step < ce)
+                if (c + u * step < ce) {
+                    const int grp = P::kElems == 32 ? group_of_chunk(c + u * step, g.cpg, g.cps) : 0;
 #pragma unroll
-                    for (int r = 0; r < R; ++r) P::load(ch[u][r], rows[r], c + u * step, g.gk, g.cpg);
+                    for (int r = 0; r < R; ++r) P::load(ch[u][r], wrow[r], srow[r], c + u * step, grp);
+                }
             if constexpr (DX) {
                 // one activation chunk (an L1 hit, mostly) kept in flight ahead of the MACs
                 uint4 xn = P::load_x(xs, c, coherent);
@@ -693,6 +640,10 @@ __device__ __forceinline__ void row_group(const RowRef (&rows)[R], bool active, 
 #pragma unroll
                         for (int r = 0; r < R; ++r) P::mac_direct(acc[r], ch[u][r], xv);
                     }
+            } else if constexpr (P::kMacRows) {
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (c + u * step < ce) P::template mac_rows<MT, R>(acc, ch[u], xs, c + u * step, g.K);
             } else {
 #pragma unroll
                 for (int u = 0; u < U; ++u)
@@ -786,69 +737,7 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvP
     float best_v = NAN;
     int best_i = INT_MAX;
 
-    if constexpr (W4Mma<P, MT, R>::v) {
-        // one warp per tile of 16 rows (ksplit = 1), on the tensor cores
-        const int nseg = g.K / kW4MmaSeg;
-        int sbeg = 0, send = nseg;
-        if constexpr (SPLIT) {
-            sbeg = (int)((long long)nseg * sidx / S);
-            send = (int)((long long)nseg * (sidx + 1) / S);
-        }
-        const int q = lane >> 2, t = lane & 3;
-        unsigned char* ring = smem + w4_ring_offset<P>(1, g.K) + (size_t)warp * kW4MmaRingBytes;
-        for (int it = 0; it < p.iters; ++it) {
-            const int tile = (it * gx + bx) * slots + slot;
-            if (tile >= n_rg) continue;
-            const int r0 = tile * kW4MmaRows;
-            RowRef z{};
-            const RowRef first = locate(p.t, r0, g.rb, z);
-            // rows past the end alias the tile's first row (loaded, dropped)
-            const RowRef ra = locate(p.t, r0 + q, g.rb, first);
-            const RowRef rb = locate(p.t, r0 + q + 8, g.rb, first);
-            const float2 y = w4a16_mma_rows(
-                ra.w, rb.w, static_cast<const uint16_t*>(ra.scale) + (size_t)ra.local * g.gk,
-                static_cast<const uint16_t*>(rb.scale) + (size_t)rb.local * g.gk, xsrc, sbeg, send,
-                g.cpg, ring);
-            if constexpr (ARGMAX) {
-                float v = NAN;
-                int i = INT_MAX;
-                if (t == 0) {
-                    if (ra.valid) {
-                        p.logits[ra.global] = y.x;
-                        v = y.x;
-                        i = ra.global;
-                    }
-                    if (rb.valid) {
-                        p.logits[rb.global] = y.y;
-                        if (arg_better(y.y, rb.global, v, i)) {
-                            v = y.y;
-                            i = rb.global;
-                        }
-                    }
-                }
-#pragma unroll
-                for (int o = 4; o < 32; o <<= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-                    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-                    if (arg_better(ov, oi, v, i)) {
-                        v = ov;
-                        i = oi;
-                    }
-                }
-                if (lane == 0 && arg_better(v, i, best_v, best_i)) {
-                    best_v = v;
-                    best_i = i;
-                }
-            } else if constexpr (SPLIT) {
-                int* part = static_cast<int*>(p.kpart) + (size_t)sidx * p.t.N;
-                if (t == 0 && ra.valid) part[ra.global] = to_bits(y.x);
-                if (t == 1 && rb.valid) part[rb.global] = to_bits(y.y);
-            } else {
-                if (t == 0 && ra.valid) P::store(ra, 0, y.x, 1.f);
-                if (t == 1 && rb.valid) P::store(rb, 0, y.y, 1.f);
-            }
-        }
-    } else {
+    {
     for (int it = 0; it < p.iters; ++it) {
         const int rg = (it * gx + bx) * slots + slot;
         const bool active = rg < n_rg;
@@ -932,14 +821,11 @@ __global__ void __launch_bounds__(256) k_split_finish(const __grid_constant__ Ge
 }
 
 // Shared memory of k_gemv: staged activations | row-group partials | per-warp
-// argmax candidates | (W4A16 tensor-core tiles, R = kW4MmaRows) the warps'
-// weight rings from w4_ring_offset on.
+// argmax candidates.
 template <class P>
-size_t smem_bytes_for(int MT, int K, int R = 0) {
+size_t smem_bytes_for(int MT, int K) {
     const bool direct = P::kDirectX && MT == 1;
     size_t x = direct ? 0 : (P::x_bytes(MT, K) + 15) & ~(size_t)15;
-    if (std::is_same<P, PolicyW4A16>::value && MT == 1 && R == kW4MmaRows)
-        return w4_ring_offset<P>(MT, K) + (size_t)kWarps * kW4MmaRingBytes;
     return x + (size_t)kWarps * 4 * MT * 4 + (size_t)kWarps * sizeof(ArgPart);
 }
 
@@ -965,10 +851,6 @@ cudaError_t run_r(int R, const GemvParams* p, int grid, size_t smem, cudaStream_
         case 1: return run_one<P, MT, 1, ARGMAX>(p, grid, smem, s, occ);
         case 2: return run_one<P, MT, 2, ARGMAX>(p, grid, smem, s, occ);
         case 4: return run_one<P, MT, 4, ARGMAX>(p, grid, smem, s, occ);
-        case kW4MmaRows:  // W4A16 at one token: tiles on the tensor cores
-            if constexpr (W4Mma<P, MT, kW4MmaRows>::v)
-                return run_one<P, MT, kW4MmaRows, ARGMAX>(p, grid, smem, s, occ);
-            return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
 }
@@ -976,7 +858,7 @@ cudaError_t run_r(int R, const GemvParams* p, int grid, size_t smem, cudaStream_
 // The instantiations the launch heuristic can pick.
 template <class P>
 cudaError_t run_family_main(const GemvLaunch& L, const GemvParams* p, cudaStream_t s, int* occ) {
-    const size_t smem = smem_bytes_for<P>(L.MT, L.K, L.R);
+    const size_t smem = smem_bytes_for<P>(L.MT, L.K);
     if (L.argmax) {
         if constexpr (P::kIntAct && P::kElems == 16) {
             return cudaErrorInvalidValue;  // no int8 lm_head

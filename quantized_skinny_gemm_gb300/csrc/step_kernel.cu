@@ -20,10 +20,11 @@
 
 namespace dg {
 
-// Rows per slot (M = 1): int4 rows are short, so two per warp keep enough
-// loads in flight.
+// Rows per slot (M = 1): int4 rows are short, so several per warp keep enough
+// loads in flight; W4A16 takes four (each activation piece is loaded once for
+// the four rows; two chunks of each row are in flight per batch).
 template <class P>
-struct StepRows { static constexpr int v = P::kElems == 32 ? 2 : 1; };
+struct StepRows { static constexpr int v = P::kMacRows ? 4 : P::kElems == 32 ? 2 : 1; };
 // fp16 / bf16 (16 warps): two rows per slot, six chunks of each per batch (a
 // 1536-wide row in one round trip); measured against one row per slot at 24
 // warps: 475 -> 459 us for the 28-layer 1536-wide step, fewer warps per small
@@ -32,7 +33,7 @@ template <class P, int NW>
 struct StepRowsNW { static constexpr int v = (!P::kIntAct && P::kElems == 8 && NW == 16) ? 2 : StepRows<P>::v; };
 template <class P, int NW>
 struct StepUnroll { static constexpr int v = (!P::kIntAct && P::kElems == 8 && NW == 16) ? 6 : 0; };
-constexpr int kStepRMax = 2;
+constexpr int kStepRMax = 4;
 
 // Warps per CTA (one CTA per SM): the default for each format, or 16.
 template <class P>
@@ -181,8 +182,7 @@ __device__ __forceinline__ void async_wait_all() {
 }
 
 // Shared memory of k_step: phase table | staged activations | two raw
-// activation buffers | scratch (sized for the largest CTA); the W4A16
-// tensor-core variant adds the warps' weight rings after it.
+// activation buffers | scratch (sized for the largest CTA).
 template <class P>
 __host__ __device__ size_t step_smem_for(int max_k) {
     constexpr int NW = 32;  // the largest CTA any format uses
@@ -191,67 +191,12 @@ __host__ __device__ size_t step_smem_for(int max_k) {
            (P::kDirectX ? 0 : (size_t)max_k + 16);
 }
 
-// One tile of a W4A16 phase on the tensor cores: rows [first, first + 16) of
-// the phase, those below r1 kept (the rest alias the first row: loaded,
-// dropped); stored, or for an lm_head written as logits and folded into this
-// warp's greedy candidate (lane 0).
-__device__ __forceinline__ void w4_mma_unit(const StepPhase& ph, int first, int r1,
-                                            const RowGeom& g, const unsigned char* xs, bool head,
-                                            float& best_v, int& best_i, unsigned char* ring) {
-    const int lane = threadIdx.x & 31, q = lane >> 2, t = lane & 3;
-    const bool va = first + q < r1, vb = first + q + 8 < r1;
-    const RowRef f = locate_step(ph, first, g.rb);
-    const RowRef ra = va ? locate_step(ph, first + q, g.rb) : f;
-    const RowRef rb = vb ? locate_step(ph, first + q + 8, g.rb) : f;
-    const float2 y = w4a16_mma_rows(
-        ra.w, rb.w, static_cast<const uint16_t*>(ra.scale) + (size_t)ra.local * g.gk,
-        static_cast<const uint16_t*>(rb.scale) + (size_t)rb.local * g.gk, xs, 0,
-        g.K / kW4MmaSeg, g.cpg, ring);
-    if (head) {
-        float v = NAN;
-        int i = INT_MAX;
-        if (t == 0) {
-            if (va) {
-                ph.logits[ra.global] = y.x;
-                v = y.x;
-                i = ra.global;
-            }
-            if (vb) {
-                ph.logits[rb.global] = y.y;
-                if (arg_better(y.y, rb.global, v, i)) {
-                    v = y.y;
-                    i = rb.global;
-                }
-            }
-        }
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-            if (arg_better(ov, oi, v, i)) {
-                v = ov;
-                i = oi;
-            }
-        }
-        if (lane == 0 && arg_better(v, i, best_v, best_i)) {
-            best_v = v;
-            best_i = i;
-        }
-    } else {
-        if (t == 0 && va) PolicyW4A16::store(ra, 0, y.x, 1.f);
-        if (t == 1 && vb) PolicyW4A16::store(rb, 0, y.y, 1.f);
-    }
-}
-
-// W4M: every phase is W4A16 on the tensor cores (tiles of kW4MmaRows rows,
-// one warp each); the CUDA-core row groups are compiled out, and vice versa.
-template <class P, int NW, bool W4M = false>
+template <class P, int NW>
 __global__ void __launch_bounds__(NW * 32, 1)
     k_step(const __grid_constant__ StepParams sp, int max_k) {
     extern __shared__ __align__(16) unsigned char smem[];
     using Acc = typename P::Acc;
     constexpr int R = StepRowsNW<P, NW>::v;
-    constexpr int UR = W4M ? kW4MmaRows : R;  // rows of one work unit
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int G = gridDim.x, b = blockIdx.x;
 
@@ -268,14 +213,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
     float* sx_smem = fred + NW;
     int8_t* qraw = reinterpret_cast<int8_t*>(sx_smem + 4);
     bool staged_ahead = false;  // this phase's raw activations are already in flight
-    unsigned char* ring = nullptr;  // this warp's weight ring (W4A16 tensor-core tiles)
-    if constexpr (W4M)
-        ring = smem + ((step_smem_for<P>(max_k) + 15) & ~(size_t)15) +
-               (size_t)warp * kW4MmaRingBytes;
 
     unsigned nbar = 0;  // grid barriers passed
-    // work units: row groups of R rows, or W4A16 tensor-core tiles
-    plan_phases(sp, table, b, G, [](const StepPhase&, int n) { return (n + UR - 1) / UR; });
+    // work units: row groups of R rows
+    plan_phases(sp, table, b, G, [](const StepPhase&, int n) { return (n + R - 1) / R; });
 
     if constexpr (!P::kDirectX) {
         if (sp.prequant) {
@@ -354,14 +295,14 @@ __global__ void __launch_bounds__(NW * 32, 1)
             xs = static_cast<unsigned char*>(const_cast<void*>(ph.x));
         }
         const bool coherent = (ph.flags & kPhaseXWritten) != 0;
-
-        const int ks = ph.ks;
-        const int slots = NW / ks;
-        const int slot = warp / ks, kw = warp - slot * ks;
+        const int ks = ph.ks;                  // 1, 2, 4 or 8 warps per row
+        const int lks = __ffs(ks) - 1;
+        const int slots = NW >> lks;
+        const int slot = warp >> lks, kw = warp & (ks - 1);
         const PhaseSlice sl = table[p];
         const RowGeom g = row_geom_gk<P>(ph.K, ph.group, ks, sl.gk);
         const int r0 = sl.r0, r1 = sl.r0 + sl.n;
-        const int n_rg = (sl.n + UR - 1) / UR;
+        const int n_rg = (sl.n + R - 1) / R;
         // row groups are dealt round-robin over the whole step (continuing
         // where the previous phase stopped) so every warp streams a fair share
         const int lead = mod_slots<NW>(sl.deal0, ks);
@@ -374,10 +315,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
 
         for (int it = 0; it < iters; ++it) {
             const int rg = mine + it * slots;
-            if constexpr (W4M) {  // (ks = 1: one warp per tile)
-                w4_mma_unit(ph, r0 + rg * kW4MmaRows, r1, g, xs, head, best_v, best_i, ring);
-                continue;
-            }
             const bool active = true;
             RowRef rows[R];
             {
@@ -447,10 +384,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
 }
 
 
-template <class P, int NW, bool W4M = false>
+template <class P, int NW>
 cudaError_t step_run_nw(const StepParams* sp, int grid, size_t smem, cudaStream_t s, int* occ,
                         int max_k) {
-    auto fn = k_step<P, NW, W4M>;
+    auto fn = k_step<P, NW>;
     constexpr int threads = NW * 32;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -474,9 +411,7 @@ cudaError_t step_run_nw(const StepParams* sp, int grid, size_t smem, cudaStream_
 
 template <class P>
 cudaError_t step_run(const StepParams* sp, int grid, size_t smem, cudaStream_t s, int* occ,
-                     int max_k, int nw, bool w4m) {
-    if constexpr (std::is_same<P, PolicyW4A16>::value)
-        if (w4m) return step_run_nw<P, StepCfg<P>::kWarps, true>(sp, grid, smem, s, occ, max_k);
+                     int max_k, int nw) {
     // W4A8 may run 20 warps (the host picks it only when no phase splits K:
     // the split barriers' id ranges are disjoint up to 16 warps)
     if constexpr (std::is_same<P, PolicyW4A8>::value)
@@ -484,32 +419,29 @@ cudaError_t step_run(const StepParams* sp, int grid, size_t smem, cudaStream_t s
     return step_run_nw<P, StepCfg<P>::kWarps>(sp, grid, smem, s, occ, max_k);
 }
 
-size_t step_smem(Fmt f, int max_k, bool w4m) {
+size_t step_smem(Fmt f, int max_k) {
     switch (f) {
         case F_F16:
         case F_BF16: return step_smem_for<PolicyFP<false>>(max_k);
         case F_I8: return step_smem_for<PolicyI8>(max_k);
-        case F_W4A16:
-            return w4m ? ((step_smem_for<PolicyW4A16>(max_k) + 15) & ~(size_t)15) +
-                             (size_t)StepCfg<PolicyW4A16>::kWarps * kW4MmaRingBytes
-                       : step_smem_for<PolicyW4A16>(max_k);
+        case F_W4A16: return step_smem_for<PolicyW4A16>(max_k);
         case F_W4A8: return step_smem_for<PolicyW4A8>(max_k);
     }
     return 0;
 }
 
 cudaError_t step_launch(Fmt f, const StepParams* sp, int grid, size_t smem, cudaStream_t s,
-                        int* occ, int nw, bool w4m) {
+                        int* occ, int nw) {
     int max_k = 0;
     if (sp)
         for (int p = 0; p < sp->nphase; ++p)
             if (sp->ph[p].K > max_k) max_k = sp->ph[p].K;
     switch (f) {
-        case F_F16: return step_run<PolicyFP<false>>(sp, grid, smem, s, occ, max_k, nw, w4m);
-        case F_BF16: return step_run<PolicyFP<true>>(sp, grid, smem, s, occ, max_k, nw, w4m);
-        case F_I8: return step_run<PolicyI8>(sp, grid, smem, s, occ, max_k, nw, w4m);
-        case F_W4A16: return step_run<PolicyW4A16>(sp, grid, smem, s, occ, max_k, nw, w4m);
-        case F_W4A8: return step_run<PolicyW4A8>(sp, grid, smem, s, occ, max_k, nw, w4m);
+        case F_F16: return step_run<PolicyFP<false>>(sp, grid, smem, s, occ, max_k, nw);
+        case F_BF16: return step_run<PolicyFP<true>>(sp, grid, smem, s, occ, max_k, nw);
+        case F_I8: return step_run<PolicyI8>(sp, grid, smem, s, occ, max_k, nw);
+        case F_W4A16: return step_run<PolicyW4A16>(sp, grid, smem, s, occ, max_k, nw);
+        case F_W4A8: return step_run<PolicyW4A8>(sp, grid, smem, s, occ, max_k, nw);
     }
     return cudaErrorInvalidValue;
 }

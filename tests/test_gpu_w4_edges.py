@@ -1,15 +1,8 @@
-"""W4A16 at one token: tile and segment edges and group sizes against the
-oracle, row slices bitwise equal to the whole matrix, decode-step row slices
-that straddle fused segments bitwise equal to the per-op calls, a ragged int4
-lm_head with a tie across tiles.  The parent runs them on the default
-CUDA-core path; a child process runs them, with the int4 GEMV and step tests,
-on the tensor-core tile (mma.sync m16n8k16: 16 weight rows per warp tile,
-each column of the B operand one 32-code chunk, the chunk's group scale
-applied in fp32), which DG_TUNE=W4MMA=1 selects."""
-import os
-import subprocess
-import sys
-
+"""W4A16 at one token: row-group and chunk-batch edges and group sizes against
+the oracle, row slices bitwise equal to the whole matrix (a row's place in its
+four-row slot must not change its result), decode-step row slices that
+straddle fused segments bitwise equal to the per-op calls, a ragged int4
+lm_head with a tie across row groups."""
 import numpy as np
 import pytest
 import torch
@@ -21,11 +14,6 @@ from quantized_skinny_gemm_gb300 import synth
 from gpu_util import DEV, bits, need_gpu, sync
 
 pytestmark = pytest.mark.gpu
-
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-TILE = "W4MMA=1" in os.environ.get("DG_TUNE", "")
-parent_only = pytest.mark.skipif(TILE, reason="run by the parent pytest")
-
 
 def _case(N, K, group, seed):
     g = synth.generator(seed)
@@ -42,12 +30,16 @@ def _gemv(Wq, sc, x, group=32):
     return y
 
 
-# one row, a full tile, a ragged tile; 1, 3 (odd: the last batch of two
-# segments half full) and 5 segments; groups of 64, 128 and 256 (two to eight
-# chunks per scale); a few thousand rows
+# one row, a full and a ragged row group; one to fourteen chunks per lane
+# (batches of two chunks, the last one partial); groups of 64, 128 and 256
+# (two to eight chunks per scale); a few thousand rows; and the general slot
+# loop: a 96-code group (no power of two), rows of 16384 codes (two warps per
+# row) and a 2048-code group (more than 32 chunks per scale)
 @pytest.mark.parametrize("N,K,group", [(1, 256, 32), (16, 256, 32), (17, 256, 32),
                                        (7, 768, 32), (250, 1280, 32), (300, 1024, 64),
-                                       (300, 1024, 128), (129, 2304, 256), (4097, 512, 32)])
+                                       (300, 1024, 128), (129, 2304, 256), (4097, 512, 32),
+                                       (6, 288, 32), (5, 14336, 32), (33, 9216, 128),
+                                       (40, 288, 96), (20, 16384, 32), (9, 4096, 2048)])
 def test_tile_edges_against_the_oracle(N, K, group):
     need_gpu()
     Wq, sc, x = _case(N, K, group, seed=N + K + group)
@@ -57,15 +49,15 @@ def test_tile_edges_against_the_oracle(N, K, group):
 
 
 def test_row_slices_equal_the_whole_matrix_bitwise():
-    """A row's place in its row group or tile changes with the slice (row 500
-    sits at position 4 of its 16-row tile in the whole matrix, 0 in the slice
-    from 500): its result must not."""
+    """A row's place in its row group changes with the slice (row 501 sits at
+    position 1 of its four-row slot in the whole matrix, 0 in the slice from
+    501): its result must not."""
     need_gpu()
     N, K = 1000, 1024
     Wq, sc, x = _case(N, K, 32, seed=5)
     Wd, sd, xd = Wq.to(DEV), sc.to(DEV), x.to(DEV)
     full = _gemv(Wd, sd, xd)
-    for r0, r1 in ((3, 21), (500, 517), (993, 1000), (16, 48), (0, 1)):
+    for r0, r1 in ((3, 21), (501, 517), (993, 1000), (16, 48), (0, 1), (2, 3)):
         part = _gemv(Wd[r0:r1].contiguous(), sd[r0:r1].contiguous(), xd)
         assert torch.equal(part, full[:, r0:r1]), (r0, r1)
 
@@ -100,9 +92,9 @@ def test_step_tiles_straddling_fused_segments_equal_the_per_op_calls():
 
 
 def test_ragged_int4_head_and_a_tie_across_tiles():
-    """1000 rows (the last tile half full); rows 5 and 17 (tiles 0 and 1)
-    hold the same winning codes and scales: equal logits, the lower index
-    wins; the logits match the oracle."""
+    """1000 rows; rows 5 and 17 (different row groups and warps) hold the same
+    winning codes and scales: equal logits, the lower index wins; the logits
+    match the oracle."""
     need_gpu()
     N, K = 1000, 512
     Wq, sc, x = _case(N, K, 32, seed=41)
@@ -124,19 +116,3 @@ def test_ragged_int4_head_and_a_tie_across_tiles():
     lr, A = oracle.gemv_w4a16(Wq.numpy(), bits(sc), bits(x))
     tol.assert_close(lg.double().numpy(), lr[0], A[0], "f32", "ragged int4 head")
     assert int(np.argmax(lg.numpy())) == 5
-
-
-@parent_only
-def test_tensor_core_w4a16_tile_in_a_child_process():
-    need_gpu()
-    env = dict(os.environ, DG_TUNE="W4MMA=1")
-    files = [os.path.join(ROOT, "tests", f) for f in ("test_gpu_w4.py", "test_gpu_w4_mma.py")]
-    step = os.path.join(ROOT, "tests", "test_gpu_decode_step.py")
-    split = os.path.join(ROOT, "tests", "test_gpu_split_k.py::test_w4_split_k")
-    r = subprocess.run([sys.executable, "-m", "pytest", *files, split,
-                        step + "::test_persistent_step_equals_per_op_calls_bitwise_int4",
-                        step + "::test_int4_step_mixing_laid_out_and_staged_activations_matches_"
-                        "sequential_calls", "-q", "-x", "-p", "no:cacheprovider", "-m", "gpu"],
-                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
-    assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-4000:]
-    assert " passed" in r.stdout and "failed" not in r.stdout
