@@ -24,8 +24,22 @@ exact int64 for integer accumulators), summed in ascending k:
   two's-complement nibble unpacking, one fp16 scale per group of 32 k.
 * ``quant_act`` -- per-token symmetric int8 quantization of the activations for
   W8A8 / W4A8, decided in IEEE fp32.
-* ``quant_w8`` / ``quant_w4`` / ``dequant_w4`` -- weight quantizers used only by
-  the round-trip pins.
+* ``quant_w8`` / ``quant_w4`` / ``dequant_w4`` -- weight quantizers (per-channel
+  int8, groupwise int4), the definitions the load-time packers must reproduce
+  bit for bit ("vLLM Arm CPU optimizations", section "Dense layer weight
+  prepacking": weights are put in the kernel's format once, at warm-up).
+* ``silu`` / ``gemv_swiglu_*`` / ``gemv_residual_*`` -- the epilogues a decoder
+  applies right after the weight stream (SwiGLU after gate|up, a residual add
+  after o and down); the pages only motivate removing the extra launches
+  around the stream (EdgeFM, section 2.C, graph-accelerated decode), so the
+  definitions are the plain ones: silu(v) = v / (1 + e^-v), h = silu(g) * u,
+  y = r + W x.
+* ``causal_conv1d_update`` -- one decode step of a depthwise causal 1-D
+  convolution over a rolling window ("MiniCPM-V on Orange Pi AIPro": the scalar
+  causal-conv1d baseline that became a vectorized step kernel): per channel c,
+  v = b[c] + sum_j w[c][j] u[j], u = the channel's last W-1 inputs (oldest
+  first) followed by the new input; y = v or silu(v); the window then drops
+  its oldest input and appends the new one.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (brute force, closed forms, library special cases, invariants, hand-written
@@ -287,3 +301,86 @@ def dequant_w4(codes, scales, group=32):
     N, K = c.shape
     s = decode_f16(_bits16(scales)).reshape(N, K // group)
     return (c.reshape(N, K // group, group) * s[:, :, None]).reshape(N, K)
+
+
+# ---- epilogues and the causal-conv1d decode step -----------------------------
+
+def silu(v):
+    """v / (1 + exp(-v)) in fp64 (v * sigmoid(v))."""
+    v = np.asarray(v, np.float64)
+    with np.errstate(over="ignore"):
+        return v / (1.0 + np.exp(-v))
+
+
+def gemv_swiglu_fp(Wg, Wu, x, fmt="f16", rows=None, nthreads=0):
+    """h = silu(Wg x) * (Wu x) per row, from the exact fp64 products.
+    Returns (h, g, u, A_g, A_u), each [M][nrows]."""
+    g, Ag = gemv_fp(Wg, x, fmt, rows=rows, nthreads=nthreads)
+    u, Au = gemv_fp(Wu, x, fmt, rows=rows, nthreads=nthreads)
+    return silu(g) * u, g, u, Ag, Au
+
+
+def gemv_swiglu_w4a16(Wg, Sg, Wu, Su, x, group=32, rows=None, nthreads=0):
+    g, Ag = gemv_w4a16(Wg, Sg, x, group, rows=rows, nthreads=nthreads)
+    u, Au = gemv_w4a16(Wu, Su, x, group, rows=rows, nthreads=nthreads)
+    return silu(g) * u, g, u, Ag, Au
+
+
+def gemv_swiglu_w4a8(Wg, Sg, Wu, Su, xq, s_x, group=32, rows=None, nthreads=0):
+    g, Ag, _ = gemv_w4a8(Wg, Sg, xq, s_x, group, rows=rows, nthreads=nthreads)
+    u, Au, _ = gemv_w4a8(Wu, Su, xq, s_x, group, rows=rows, nthreads=nthreads)
+    return silu(g) * u, g, u, Ag, Au
+
+
+def gemv_residual_fp(W, x, r, fmt="f16", rows=None, nthreads=0):
+    """y = r + W x (r fp16 / bf16 [M][N]); returns (y, A) with A = sum |w x|."""
+    y, A = gemv_fp(W, x, fmt, rows=rows, nthreads=nthreads)
+    rb = (decode_bf16 if fmt == "bf16" else decode_f16)(_bits16(r)).reshape(y.shape[0], -1)
+    if rows is not None:
+        rb = rb[:, _c(rows, np.int64)]
+    return rb + y, A
+
+
+def gemv_residual_w4a16(Wq, scales, x, r, group=32, rows=None, nthreads=0):
+    y, A = gemv_w4a16(Wq, scales, x, group, rows=rows, nthreads=nthreads)
+    rb = decode_f16(_bits16(r)).reshape(y.shape[0], -1)
+    if rows is not None:
+        rb = rb[:, _c(rows, np.int64)]
+    return rb + y, A
+
+
+def causal_conv1d_update(x, state, w, bias=None, act="silu"):
+    """One decode step of a depthwise causal conv1d.
+
+    x fp16 bits [M][C] (the new input), state fp16 bits [M][C][W-1] (each
+    channel's last W-1 inputs, oldest first), w fp16 bits [C][W] (tap j
+    multiplies window position j, position W-1 being the new input), bias fp16
+    bits [C] or None, act "silu" or "none".
+    Returns (y [M][C] fp64, v [M][C] the pre-activation sum, A [M][C] =
+    |b| + sum_j |w_j u_j|, new_state fp16 bits [M][C][W-1]).  The sum runs in
+    fp64 over j ascending, after the bias."""
+    xb = _bits16(x)
+    C = xb.shape[-1]
+    xb = xb.reshape(-1, C)
+    M = xb.shape[0]
+    wb = _bits16(w).reshape(C, -1)
+    Wd = wb.shape[1]
+    sb = _bits16(state).reshape(M, C, Wd - 1)
+    wv = decode_f16(wb).reshape(C, Wd)
+    u = np.concatenate([decode_f16(sb).reshape(M, C, Wd - 1),
+                        decode_f16(xb).reshape(M, C, 1)], axis=2)
+    bv = decode_f16(_bits16(bias)).reshape(C) if bias is not None else np.zeros(C)
+    v = np.empty((M, C))
+    A = np.empty((M, C))
+    for m in range(M):
+        acc = bv.copy()
+        aa = np.abs(bv)
+        for j in range(Wd):
+            t = wv[:, j] * u[m, :, j]
+            acc = acc + t
+            aa = aa + np.abs(t)
+        v[m] = acc
+        A[m] = aa
+    y = silu(v) if act == "silu" else v
+    new_state = np.concatenate([sb[:, :, 1:], xb.reshape(M, C, 1)], axis=2)
+    return y, v, A, new_state

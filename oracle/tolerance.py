@@ -10,6 +10,15 @@ Floating-point outputs:   |y - y_ref| <= 1e-3 * A + ulp_out(y_ref)
   (bounded by K * 2^-24 * A) and, for int4 x fp16, fp32 group sums; the ulp
   term covers the final rounding to the output type.
 Integer outputs (int32 accumulators, int8 codes, quantization scales): exact.
+Epilogues evaluated in fp32 by the kernel after its fp32 sums (SiLU with the
+  library exp, a product, a sum with the residual) carry the sums' error
+  through the function: with e = 1e-3 * A + ulp_f32(v) for an fp32 sum v and
+  |silu'| <= 1.1 everywhere,
+    silu(v):        1.1 e + 2^-20 |silu(v)| + ulp_out
+    silu(g) * u:    1.1 e_g |u| + |silu(g)| e_u + 1.1 e_g e_u + 2^-20 |h| + ulp_out
+  where 2^-20 relative covers the fp32 evaluation of the function (a few
+  fp32 roundings and the library exp).  A residual add y = r + W x is a sum
+  with one more exact term: the plain bound with A = sum |w x|.
 Greedy argmax: with b_i = 1e-3 * A_i + ulp_f32(logit_i), the token must equal
   the oracle's when its top-1 beats top-2 by more than b_top1 + b_top2;
   otherwise it must be a near-tie candidate: ref[token] >= v1 - b_top1 - b_token.
@@ -81,3 +90,45 @@ def argmax_check(token, logits_ref, A_ref):
     if not (0 <= token < v.size):
         return False, False
     return bool(v[token] >= v[i1] - b[i1] - b[token]), False
+
+
+ACT_REL = 2.0 ** -20
+SILU_SLOPE = 1.1   # max |d/dv (v sigmoid(v))| = 1.0998...
+
+
+def _silu(v):
+    v = np.asarray(v, np.float64)
+    with np.errstate(over="ignore"):
+        return v / (1.0 + np.exp(-v))
+
+
+def bound_silu(v_ref, A, out="f16"):
+    """Bound for y = silu(v) where the kernel's fp32 sum v errs by 1e-3 A."""
+    v = np.asarray(v_ref, np.float64)
+    e = REL * np.asarray(A, np.float64) + ulp_f32(v)
+    y = _silu(v)
+    return SILU_SLOPE * e + ACT_REL * np.abs(y) + _ULP[out](y)
+
+
+def bound_swiglu(g_ref, u_ref, A_g, A_u, out="f16"):
+    """Bound for h = silu(g) * u from two fp32 sums g, u."""
+    g = np.asarray(g_ref, np.float64)
+    u = np.asarray(u_ref, np.float64)
+    eg = REL * np.asarray(A_g, np.float64) + ulp_f32(g)
+    eu = REL * np.asarray(A_u, np.float64) + ulp_f32(u)
+    h = _silu(g) * u
+    return (SILU_SLOPE * eg * np.abs(u) + np.abs(_silu(g)) * eu + SILU_SLOPE * eg * eu
+            + ACT_REL * np.abs(h) + _ULP[out](h))
+
+
+def assert_within(y, y_ref, bnd, what=""):
+    """|y - y_ref| <= bnd elementwise (an explicit bound array)."""
+    y = np.asarray(y, np.float64)
+    yr = np.asarray(y_ref, np.float64)
+    bad = ~(np.abs(y - yr) <= np.asarray(bnd, np.float64))
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        det = ["%s: y=%r ref=%r bound=%r" % (tuple(i), y[tuple(i)], yr[tuple(i)],
+                                              np.asarray(bnd)[tuple(i)]) for i in idx]
+        raise AssertionError("%s: %d of %d outside tolerance; first: %s"
+                             % (what, int(bad.sum()), bad.size, "; ".join(det)))

@@ -398,3 +398,125 @@ def test_thread_count_and_row_subset_do_not_change_results():
     ya, _ = oracle.gemv_w4a16(packed, scales, x[:, :128], nthreads=1)
     yb, _ = oracle.gemv_w4a16(packed, scales, x[:, :128], rows=[89, 0], nthreads=4)
     assert np.array_equal(yb, ya[:, [89, 0]])
+
+
+# ---- SiLU, SwiGLU, residual, causal-conv1d step -------------------------------
+
+def test_silu_closed_forms_and_reflection():
+    assert oracle.silu(0.0) == 0.0
+    # sigmoid(ln 3) = 3/4 exactly, so silu(ln 3) = 0.75 ln 3
+    assert abs(oracle.silu(math.log(3.0)) - 0.75 * math.log(3.0)) < 1e-15
+    assert abs(oracle.silu(40.0) - 40.0) < 1e-12             # v sigmoid(v) -> v
+    assert abs(oracle.silu(-40.0) / (-40.0 * math.exp(-40.0)) - 1.0) < 1e-12  # -> v e^v
+    v = np.random.default_rng(3).normal(0, 4, 1000)
+    # sigmoid(-v) = 1 - sigmoid(v)  =>  silu(-v) = silu(v) - v
+    assert np.allclose(oracle.silu(-v), oracle.silu(v) - v, rtol=0, atol=1e-12)
+    # and torch's own fp64 silu
+    ref = torch.nn.functional.silu(torch.from_numpy(v)).numpy()
+    assert np.allclose(oracle.silu(v), ref, rtol=1e-15, atol=1e-300)
+
+
+def _dq(bits16):
+    return np.asarray(bits16, np.uint16).view(np.float16).astype(np.float64)
+
+
+def test_swiglu_equals_silu_of_gate_times_up_by_fp64_matmul():
+    g = torch.Generator().manual_seed(11)
+    Wg = (torch.randn(37, 96, generator=g) * 0.3).half().numpy()
+    Wu = (torch.randn(37, 96, generator=g) * 0.3).half().numpy()
+    x = torch.randn(3, 96, generator=g).half().numpy()
+    h, gg, uu, Ag, Au = oracle.gemv_swiglu_fp(Wg, Wu, x)
+    G = x.astype(np.float64) @ Wg.astype(np.float64).T
+    Uu = x.astype(np.float64) @ Wu.astype(np.float64).T
+    assert np.allclose(gg, G, rtol=0, atol=1e-12) and np.allclose(uu, Uu, rtol=0, atol=1e-12)
+    assert np.allclose(h, (G / (1 + np.exp(-G))) * Uu, rtol=1e-14, atol=1e-14)
+    # gate and up are not interchangeable
+    assert not np.allclose(h, (Uu / (1 + np.exp(-Uu))) * G, rtol=1e-3, atol=1e-3)
+    assert np.allclose(Ag, np.abs(x.astype(np.float64)) @ np.abs(Wg.astype(np.float64)).T)
+
+
+def test_swiglu_w4a16_uses_each_matrix_with_its_own_scales():
+    Wq, sc, x = _w4_small(29, 128, seed=12)
+    Wq2, sc2, _ = _w4_small(29, 128, seed=13)
+    h, gg, uu, _, _ = oracle.gemv_swiglu_w4a16(Wq, sc, Wq2, sc2, x)
+    G = x.astype(np.float64) @ oracle.dequant_w4(oracle.unpack_w4(Wq).reshape(29, 128), sc).T
+    Uu = x.astype(np.float64) @ oracle.dequant_w4(oracle.unpack_w4(Wq2).reshape(29, 128), sc2).T
+    assert np.allclose(h, oracle.silu(G) * Uu, rtol=1e-13, atol=1e-13)
+
+
+def _w4_small(N, K, seed):
+    g = torch.Generator().manual_seed(seed)
+    codes = torch.randint(-8, 8, (N, K), generator=g, dtype=torch.int16)
+    nib = codes & 0xF
+    Wq = (nib[:, 0::2] | (nib[:, 1::2] << 4)).to(torch.uint8).numpy()
+    sc = (torch.rand(N, K // 32, generator=g) * 0.01 + 0.001).half().numpy()
+    x = torch.randn(1, K, generator=g).half().numpy()
+    return Wq, sc, x
+
+
+def test_residual_adds_r_to_the_product():
+    g = torch.Generator().manual_seed(14)
+    W = (torch.randn(21, 64, generator=g) * 0.1).half().numpy()
+    x = torch.randn(2, 64, generator=g).half().numpy()
+    r = torch.randn(2, 21, generator=g).half().numpy()
+    y, A = oracle.gemv_residual_fp(W, x, r)
+    ref = r.astype(np.float64) + x.astype(np.float64) @ W.astype(np.float64).T
+    assert np.allclose(y, ref, rtol=0, atol=1e-12)
+    rows = np.array([20, 3, 0])
+    ys, _ = oracle.gemv_residual_fp(W, x, r, rows=rows)
+    assert np.array_equal(ys, y[:, rows])
+
+
+def _conv_case(M, C, Wd, seed):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(M, C, generator=g).half().numpy()
+    st = torch.randn(M, C, Wd - 1, generator=g).half().numpy()
+    w = (torch.randn(C, Wd, generator=g) * 0.5).half().numpy()
+    b = (torch.randn(C, generator=g) * 0.1).half().numpy()
+    return x, st, w, b
+
+
+def test_conv1d_step_one_hot_taps_and_all_ones():
+    x, st, w, b = _conv_case(2, 9, 4, seed=15)
+    e_new = np.zeros((9, 4), np.float16)
+    e_new[:, 3] = 1
+    y, v, _, ns = oracle.causal_conv1d_update(x, st, e_new, None, act="none")
+    assert np.array_equal(y, x.astype(np.float64))            # newest tap: y = x
+    e_old = np.zeros((9, 4), np.float16)
+    e_old[:, 0] = 1
+    y, _, _, _ = oracle.causal_conv1d_update(x, st, e_old, None, act="none")
+    assert np.array_equal(y, st[:, :, 0].astype(np.float64))  # oldest tap
+    ones = np.ones((9, 4), np.float16)
+    y, _, A, _ = oracle.causal_conv1d_update(x, st, ones, b, act="none")
+    win = np.concatenate([st.astype(np.float64), x.astype(np.float64)[:, :, None]], axis=2)
+    assert np.allclose(y, b.astype(np.float64) + win.sum(axis=2), rtol=0, atol=1e-12)
+    assert np.allclose(A, np.abs(b.astype(np.float64)) + np.abs(win).sum(axis=2))
+    # the window drops its oldest input and appends the new one
+    assert np.array_equal(ns[:, :, :2].view(np.uint16), st[:, :, 1:].view(np.uint16))
+    assert np.array_equal(ns[:, :, 2].view(np.uint16), x.view(np.uint16))
+
+
+def test_conv1d_steps_equal_numpy_convolve_over_a_sequence():
+    """Stepping from a zero window over a sequence gives the causal
+    convolution: y_t = sum_j w[j] s[t - (W-1) + j] = np.convolve(s, w[::-1])[t]."""
+    g = torch.Generator().manual_seed(16)
+    C, Wd, T = 5, 4, 11
+    seq = torch.randn(T, C, generator=g).half().numpy()
+    w = (torch.randn(C, Wd, generator=g) * 0.5).half().numpy()
+    st = np.zeros((1, C, Wd - 1), np.float16)
+    for t in range(T):
+        y, _, _, st = oracle.causal_conv1d_update(seq[t][None], st, w, None, act="none")
+        for c in range(C):
+            ref = np.convolve(seq[:, c].astype(np.float64), w[c, ::-1].astype(np.float64))[t]
+            assert abs(y[0, c] - ref) <= 1e-12 * (1 + abs(ref))
+
+
+def test_conv1d_step_brute_force_fractions_and_silu():
+    x, st, w, b = _conv_case(2, 6, 3, seed=17)
+    y, v, A, _ = oracle.causal_conv1d_update(x, st, w, b, act="silu")
+    for m in range(2):
+        for c in range(6):
+            u = [Fraction(float(q)) for q in st[m, c]] + [Fraction(float(x[m, c]))]
+            ex = Fraction(float(b[c])) + sum(Fraction(float(w[c, j])) * u[j] for j in range(3))
+            assert abs(Fraction(v[m, c]) - ex) <= Fraction(1, 2 ** 50) * (1 + abs(ex))
+    assert np.allclose(y, v / (1 + np.exp(-v)), rtol=1e-15, atol=0)

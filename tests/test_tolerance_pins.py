@@ -87,3 +87,38 @@ def test_argmax_rule_pins_clear_winners_and_accepts_only_near_ties():
     assert tol.argmax_check(1, tie, np.zeros(4))[0]
     assert tol.argmax_check(2, tie, np.zeros(4))[0]
     assert not tol.argmax_check(0, tie, np.zeros(4))[0]
+
+
+def test_silu_slope_constant_bounds_the_derivative_and_is_tight():
+    v = np.linspace(-30, 30, 600001)
+    s = 1 / (1 + np.exp(-v))
+    d = s * (1 + v * (1 - s))
+    assert np.max(np.abs(d)) <= tol.SILU_SLOPE
+    assert np.max(np.abs(d)) > 1.09   # 1.0998...: a looser slope would hide errors
+
+
+def test_silu_and_swiglu_bounds_cover_input_errors_at_their_edge():
+    """Perturb the fp32 sums by exactly their own error budget (the worst
+    case): the bounds still hold, and each term of the SwiGLU bound is
+    needed somewhere."""
+    rng = np.random.default_rng(5)
+    n = 200000
+    g = rng.normal(0, 3, n)
+    u = rng.normal(0, 3, n)
+    Ag = np.abs(g) * rng.uniform(1, 50, n)
+    Au = np.abs(u) * rng.uniform(1, 50, n)
+    eg = tol.REL * Ag + tol.ulp_f32(g)
+    eu = tol.REL * Au + tol.ulp_f32(u)
+    sg = rng.choice([-1.0, 1.0], n)
+    su = rng.choice([-1.0, 1.0], n)
+    silu = lambda t: t / (1 + np.exp(-t))
+    h0 = silu(g) * u
+    h1 = silu(g + sg * eg) * (u + su * eu)
+    b = tol.bound_swiglu(g, u, Ag, Au, "f32")
+    assert np.all(np.abs(h1 - h0) <= b)
+    # dropping the |silu(g)| e_u term breaks it
+    part = b - np.abs(silu(g)) * eu
+    assert np.any(np.abs(h1 - h0) > part)
+    # the silu bound
+    bs = tol.bound_silu(g, Ag, "f32")
+    assert np.all(np.abs(silu(g + sg * eg) - silu(g)) <= bs)
