@@ -47,7 +47,7 @@
  *  - Tuning.  The environment variable DG_TUNE (comma-separated KEY=value,
  *    read once per process) overrides launch choices for configuration
  *    sweeps; unset, the defaults above hold.  Every setting stays within the
- *    parity bound; KS, KS8 (warps per row), KP (split-K ranges) and MMA
+ *    parity bound; KS (warps per row), KP (split-K ranges) and MMA
  *    (tensor-core tiles off / int8 tile) change a row's summation order, the
  *    others only the schedule.
  */

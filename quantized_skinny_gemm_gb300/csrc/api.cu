@@ -73,9 +73,7 @@ int* device_error_word() {
 // barrier between every pair of phases of the persistent kernel.
 struct Tune {
     int R = 0, KS = 0, CPS = 0, PF = -1, PDL = -1, STEP = -1, SPIN = -1, SNW = 0, MMA = -1;
-    int RING = -1, TSB = 0, TNS = 0, TNC = 0;  // weight ring: on/off, KB per stage, stages, consumers
     int KP = 0;                                // split-K ranges of a per-op launch (1 = off)
-    int KS8 = -1;                              // rows of >= 16 KB split over 8 warps
 };
 
 static Tune read_tune() {
@@ -96,12 +94,7 @@ static Tune read_tune() {
         else if (std::sscanf(tok, "SPIN=%d", &v) == 1) t.SPIN = v;
         else if (std::sscanf(tok, "SNW=%d", &v) == 1) t.SNW = v;
         else if (std::sscanf(tok, "MMA=%d", &v) == 1) t.MMA = v;
-        else if (std::sscanf(tok, "RING=%d", &v) == 1) t.RING = v;
-        else if (std::sscanf(tok, "TSB=%d", &v) == 1) t.TSB = v;
-        else if (std::sscanf(tok, "TNS=%d", &v) == 1) t.TNS = v;
-        else if (std::sscanf(tok, "TNC=%d", &v) == 1) t.TNC = v;
         else if (std::sscanf(tok, "KP=%d", &v) == 1) t.KP = v;
-        else if (std::sscanf(tok, "KS8=%d", &v) == 1) t.KS8 = v;
     }
     return t;
 }
@@ -145,7 +138,7 @@ static int pick_ks(Fmt f, int K) {
     const int t = tune().KS;
     if (t == 1 || t == 2 || t == 4 || t == 8) return t;
     const size_t rb = elem_row_bytes(f, K);
-    if (rb >= 16384) return tune().KS8 == 1 ? 8 : 4;
+    if (rb >= 16384) return 4;
     if (rb >= 8192) return 2;
     return 1;
 }
@@ -490,13 +483,6 @@ static size_t head_ws_bytes() { return (size_t)kMaxArgCtas * sizeof(ArgPart); }
 // Decode-step workspace: [0, 256) the persistent kernel's barrier words,
 // then the argmax partials when the step has an lm_head.
 constexpr size_t kStepHeader = 256;
-// Weight ring of the fp16 / bf16 step kernel: 6 stages of 36 KB in flight per
-// SM (a copy's worth of bytes for the HBM latency several times over); a
-// stage grows to the longest row when one row does not fit.
-constexpr size_t kRingStageBytes = 36864;
-constexpr int kRingStages = 6;
-constexpr int kRingMaxStages = 16;
-
 // ---- the persistent decode-step path -----------------------------------------------
 
 static bool same_group(const dg_linear& a, const dg_linear& b) {
@@ -507,14 +493,13 @@ static bool same_group(const dg_linear& a, const dg_linear& b) {
 // Ops the persistent kernel runs: one token, no int32 accumulator output.
 static bool step_eligible(const dg_linear& op) { return op.M == 1 && !op.acc_out; }
 
-// CTAs of the step kernel per SM (ring_nc = 0: k_step; else k_step_ring
-// with that many consumer warps).
-static int step_occupancy(Fmt f, int max_k, size_t smem, int ring_nc, int nw) {
+// CTAs of the step kernel per SM.
+static int step_occupancy(Fmt f, int max_k, size_t smem, int nw) {
     static std::mutex mu;
-    static std::map<std::tuple<int, int, int, size_t, int, int>, int> cache;
+    static std::map<std::tuple<int, int, int, size_t, int>, int> cache;
     int dev = 0;
     cudaGetDevice(&dev);
-    const auto key = std::make_tuple(dev, (int)f, max_k, smem, ring_nc, nw);
+    const auto key = std::make_tuple(dev, (int)f, max_k, smem, nw);
     {
         std::lock_guard<std::mutex> g(mu);
         auto it = cache.find(key);
@@ -522,8 +507,7 @@ static int step_occupancy(Fmt f, int max_k, size_t smem, int ring_nc, int nw) {
     }
     StepParams* none = nullptr;
     int occ = 0;
-    const cudaError_t e = ring_nc ? step_ring_launch(f, none, 0, smem, nullptr, &occ, ring_nc)
-                                  : step_launch(f, none, 0, smem, nullptr, &occ, nw);
+    const cudaError_t e = step_launch(f, none, 0, smem, nullptr, &occ, nw);
     if (e != cudaSuccess) occ = 0;
     std::lock_guard<std::mutex> g(mu);
     cache[key] = occ;
@@ -586,8 +570,8 @@ static void weight_ranges(const dg_linear& op, std::vector<Range>& v) {
 }
 
 // True when an op of ops[0..n) writes into the weights or scales of an op of
-// the same run.  The persistent kernels read weights without coherence (and
-// the weight ring copies them ahead of any barrier), so such a run goes to the
+// the same run.  The persistent kernel reads weights without coherence, so
+// such a run goes to the
 // per-launch path, which keeps the ops' order.
 static bool run_writes_weights(const dg_linear* ops, int n) {
     std::vector<Range> w, out, rd;
@@ -727,37 +711,7 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
         sp.part = reinterpret_cast<ArgPart*>(static_cast<unsigned char*>(ws) + kStepHeader);
         sp.err = device_error_word();
         if (!sp.err) return DG_ERR_CUDA;
-        // fp16 / bf16 with the weight ring selected (DG_TUNE=RING=1; measured
-        // slower than k_step on the decoder shapes, so not the default): when
-        // whole rows fit a stage and at least two stages fit shared memory
-        int ring_nc = 0;
-        size_t smem = 0;
-        if ((f == F_F16 || f == F_BF16) && tune().RING == 1) {
-            const int nc = tune().TNC == 8 ? 8 : 12;
-            const size_t rb_max = (size_t)max_k * 2;
-            size_t sb = tune().TSB > 0 ? (size_t)tune().TSB * 1024 : kRingStageBytes;
-            if (sb < rb_max) sb = (rb_max + 127) & ~(size_t)127;
-            const size_t over = step_ring_overhead(nc), lim = smem_optin_limit();
-            int ns = lim > over ? (int)((lim - over) / sb) : 0;
-            ns = std::min(ns, tune().TNS > 0 ? tune().TNS : kRingStages);
-            ns = std::min(ns, kRingMaxStages);
-            if (ns >= 2) {
-                ring_nc = nc;
-                sp.nstage = ns;
-                sp.stage_bytes = (int)sb;
-                smem = (size_t)ns * sb + over;
-                // activations that no op of the launch writes, of phases whose
-                // lanes keep them in registers, travel in the ring ahead of
-                // their rows (the producer copies them before any barrier)
-                for (int q = 0; q < sp.nphase; ++q) {
-                    StepPhase& ph = sp.ph[q];
-                    const int nch = ph.K / 8, stp = ph.ks * 32;
-                    if (!(ph.flags & kPhaseXWritten) && (nch + stp - 1) / stp <= kRingXR)
-                        ph.flags |= kPhaseXRing;
-                }
-            }
-        }
-        if (!ring_nc) smem = step_smem(f, max_k);
+        const size_t smem = step_smem(f, max_k);
         if (smem > smem_optin_limit()) return DG_ERR_UNSUPPORTED;
         // k_step runs 16 warps; W4A8 20 (one more row group in flight per SM
         // sub-partition: 883 -> 863 us for the 32-layer step) when no phase
@@ -766,13 +720,12 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
         bool split = false;
         for (int q = 0; q < sp.nphase; ++q) split = split || sp.ph[q].ks > 1;
         const int nw = split ? 16 : tune().SNW > 0 ? tune().SNW : f == F_W4A8 ? 20 : 16;
-        const int occ = step_occupancy(f, max_k, smem, ring_nc, nw);
+        const int occ = step_occupancy(f, max_k, smem, nw);
         if (occ < 1) return DG_ERR_UNSUPPORTED;
         const int grid = sm_count() * occ;
         if (grid > kMaxArgCtas) return DG_ERR_UNSUPPORTED;
         if (cudaMemsetAsync(ws, 0, 2 * sizeof(unsigned), s) != cudaSuccess) return DG_ERR_CUDA;
-        const cudaError_t e = ring_nc ? step_ring_launch(f, &sp, grid, smem, s, nullptr, ring_nc)
-                                      : step_launch(f, &sp, grid, smem, s, nullptr, nw);
+        const cudaError_t e = step_launch(f, &sp, grid, smem, s, nullptr, nw);
         if (e != cudaSuccess) return DG_ERR_CUDA;
     }
     return DG_OK;

@@ -74,14 +74,9 @@ enum StepFlags : int {
     kPhaseBarrier = 4,    // grid barrier before the phase
     kPhaseXWritten = 8,   // activations written earlier in this launch
     kPhasePreQuant = 16,  // activations quantized in the launch's prologue
-    kPhaseXRing = 32,     // k_step_ring: x travels in the weight ring ahead of the rows
     kPhaseXLaid = 64      // the prologue wrote x in the format's layout at xlay: the
                           // MACs read it from global memory (no staging, no meeting)
 };
-
-// k_step_ring keeps a lane's activation chunks of a phase in registers when
-// they number at most this (rows of up to 9 * 32 * ks chunks).
-constexpr int kRingXR = 9;
 
 struct StepSeg {
     const void* W;
@@ -116,8 +111,6 @@ struct StepParams {
     unsigned* bar;        // 2 zeroed words: arrivals, generation
     ArgPart* part;        // one partial per CTA (lm_head phases)
     int* err;             // device error word
-    int nstage;           // weight ring (k_step_ring): stages
-    int stage_bytes;      //   and bytes per stage (a multiple of 128)
 };
 
 // StepParams travels as a kernel parameter (at most 32,764 bytes).
@@ -316,11 +309,6 @@ int head_grid(const dg_linear& op);
 // format's default).  occ != nullptr: report CTAs per SM instead.
 cudaError_t step_launch(Fmt f, const StepParams* sp, int grid, size_t smem, cudaStream_t s,
                         int* occ, int nw);
-// The weight-ring variant of the persistent step (fp16 / bf16 weights, one
-// token): `nc` consumer warps (8 or 12) plus one producer warp per CTA.
-size_t step_ring_overhead(int nc);
-cudaError_t step_ring_launch(Fmt f, const StepParams* sp, int grid, size_t smem, cudaStream_t s,
-                             int* occ, int nc);
 size_t step_smem(Fmt f, int max_k);
 cudaError_t launch_wait_selftest(unsigned limit, int* err, cudaStream_t s);
 

@@ -449,8 +449,7 @@ struct PolicyW4A8 {
 // with different ks can be live at once, and a named barrier must never be
 // used with two thread counts at the same time: the splits take disjoint ids,
 // ks = 2 from 1 upward (1..8), ks = 8 at 9..10 and ks = 4 from 14 downward
-// (14..11), for up to 16 warps; 0 is __syncthreads, 15 the weight ring's
-// consumer barrier.
+// (14..11), for up to 16 warps; 0 is __syncthreads.
 __device__ __forceinline__ int slot_barrier(int warp, int ks) {
     return ks == 4 ? 14 - warp / 4 : ks == 8 ? 9 + warp / 8 : 1 + warp / ks;
 }

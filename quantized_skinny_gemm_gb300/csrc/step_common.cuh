@@ -1,7 +1,5 @@
-// Helpers shared by the two persistent decode-step kernels (k_step, which
-// streams weights through registers, and k_step_ring, which streams them
-// through a shared-memory ring): row addressing within a phase, the CTA row
-// slices, and the greedy-token reduction of an lm_head phase.
+// Helpers of the persistent decode-step kernel: row addressing within a phase,
+// the CTA row slices, and the greedy-token reduction of an lm_head phase.
 #pragma once
 
 #include "gemv_core.cuh"
