@@ -85,6 +85,21 @@ typedef enum {
     DG_LINEAR_W4A8 = 4   /* as W4A16 but x_i8 + x_scale; y fp16 */
 } dg_kind;
 
+/* Epilogue applied to an op's fp32 result before it is rounded to y
+ * (dg_linear.epilogue); the pages motivate only removing the launches around
+ * the weight stream (EdgeFM, section 2.C, graph-accelerated decode), so these
+ * are the plain decoder definitions:
+ *   DG_EPI_RESIDUAL: y = x * W^T + residual     (residual [M][N], y's type)
+ *   DG_EPI_SWIGLU:   y = silu(x * W^T) * (x * W2^T),  silu(v) = v / (1 + e^-v)
+ *                    (W the gate projection, W2 the up projection: same kind,
+ *                    shape and group; w2_scale their scales for int4 kinds).
+ * Both are evaluated in fp32 on the sums and rounded once into y; y may be
+ * the residual itself (an in-place add: each element is read, then written,
+ * by the same thread).  Not for
+ * lm_heads (token != NULL), nor with acc_out; SwiGLU is not offered for
+ * DG_LINEAR_W8A8 (DG_ERR_UNSUPPORTED). */
+typedef enum { DG_EPI_NONE = 0, DG_EPI_RESIDUAL = 1, DG_EPI_SWIGLU = 2 } dg_epilogue;
+
 /* One linear op: y = x * W^T in the format `kind`.
  * For the quantized-activation kinds (W8A8, W4A8), x_i8 [M][K] and x_scale[M]
  * are read; if `x` (fp16 [M][K]) is also given, dg_decode_step_weights first
@@ -104,6 +119,11 @@ typedef struct {
     float* logits;
     int32_t* token;
     int32_t* acc_out;      /* W8A8 only, optional: exact int32 accumulators [M][N] */
+    int32_t epilogue;      /* dg_epilogue (0 = none) */
+    int32_t reserved;      /* must be 0 */
+    const void* residual;  /* DG_EPI_RESIDUAL */
+    const void* W2;        /* DG_EPI_SWIGLU: up-projection weights */
+    const void* w2_scale;  /* DG_EPI_SWIGLU: their scales (int4 kinds) */
 } dg_linear;
 
 /* FP16 / BF16 weights (paragraph on the custom M=1 cube matmul of the Orange
@@ -143,6 +163,54 @@ dg_status dg_gemv_w8a8(const int8_t* W, const float* w_scale, const int8_t* x,
 dg_status dg_gemv_w4(const uint8_t* Wq, const void* scales, int group_size, const void* x_f16,
                      const int8_t* x_i8, const float* x_scale, void* y, int M, int N, int K,
                      void* ws, size_t ws_bytes, dg_stream stream);
+
+/* One op described by a dg_linear (any kind except an lm_head; any epilogue),
+ * M <= 16, as one launch (two with split-K).  Same arithmetic as the
+ * dg_gemv_* entry points of its kind; ws as for them (may be NULL; an op
+ * with an epilogue never splits K).  W8A8 / W4A8 ops read x_i8 / x_scale
+ * and must not carry fp16 x here (quantize first with dg_quantize_act_i8). */
+dg_status dg_linear_forward(const dg_linear* op, void* ws, size_t ws_bytes, dg_stream stream);
+
+/* Elementwise fp16 epilogues as separate launches (what a decoder runs when
+ * they are not fused into the weight stream; same fp32 arithmetic):
+ *   dg_swiglu:       h[i] = fp16( silu(g[i]) * u[i] )
+ *   dg_residual_add: out[i] = fp16( a[i] + b[i] )
+ * n elements; pointers 16-byte aligned, n a multiple of 8; out may alias a
+ * or b (elementwise), h may alias g or u. */
+dg_status dg_swiglu(const void* g, const void* u, void* h, int n, dg_stream stream);
+dg_status dg_residual_add(const void* a, const void* b, void* out, int n, dg_stream stream);
+
+/* One decode step of a depthwise causal 1-D convolution (the causal-conv1d
+ * step kernel of "MiniCPM-V on Orange Pi AIPro (Ascend 310B)"; the page gives
+ * no formula, this is the plain definition).  For token m and channel c, with
+ * u = state[m][c][0 .. width-2] (oldest first) followed by x[m][c]:
+ *   v = bias[c] + sum_{j < width} w[c][j] * u[j]     (fp32: exact products,
+ *       one rounding per term, j ascending after the bias)
+ *   y[m][c] = fp16(act == DG_ACT_SILU ? silu(v) : v)
+ * then state[m][c] becomes u[1 .. width-1] (the oldest input drops out).
+ * x, y fp16 [M][C]; state fp16 [M][C][width-1] (read and rewritten in place);
+ * w fp16 [C][width]; bias fp16 [C] or NULL.  2 <= width <= 8, C a multiple
+ * of 8, pointers 16-byte aligned; y must not overlap state. */
+typedef enum { DG_ACT_NONE = 0, DG_ACT_SILU = 1 } dg_act;
+dg_status dg_causal_conv1d_update(const void* x, void* state, const void* w, const void* bias,
+                                  void* y, int M, int C, int width, int act, dg_stream stream);
+
+/* Load-time weight quantizers and packers ("vLLM Arm CPU optimizations",
+ * section "Dense layer weight prepacking": weights are put in the kernels'
+ * format once, at warm-up).  Decided in IEEE fp32, as the library's kernels
+ * expect them; W fp16 [N][K] (16-byte aligned, K a multiple of 16 / of
+ * group_size).
+ *   dg_quantize_weights_i8: s[n] = max_k |W[n][k]| / 127 (1 for an all-zero
+ *     row), Wq[n][k] = clamp(rne(W / s), -127, 127)  -> DG_LINEAR_W8A8 input.
+ *   dg_quantize_weights_w4: per group of group_size k, s = fp16(amax / 7)
+ *     raised to the smallest fp16 subnormal if it rounds to 0 (1 for an
+ *     all-zero group), code = clamp(rne(W / s), -7, 7), packed two per byte
+ *     (k = 2j in bits 0-3 of byte j, k = 2j+1 in bits 4-7); scales fp16
+ *     [N][K/group_size]  -> DG_LINEAR_W4A16 / W4A8 input. */
+dg_status dg_quantize_weights_i8(const void* W, int8_t* Wq, float* w_scale, int N, int K,
+                                 dg_stream stream);
+dg_status dg_quantize_weights_w4(const void* W, uint8_t* Wq, void* scales, int N, int K,
+                                 int group_size, dg_stream stream);
 
 /* Per-token symmetric int8 activations for W8A8 / W4A8 (same page, same
  * sections).  x fp16 [M][K] -> xq int8 [M][K], x_scale float [M]:
@@ -198,6 +266,9 @@ dg_status dg_lm_head_argmax_noalloc(const dg_linear* head, dg_stream stream);
  * same bits as calling dg_gemv_* / dg_lm_head_argmax op by op.
  * For W8A8 / W4A8 ops that carry fp16 `x`, the step quantizes x exactly as
  * dg_quantize_act_i8 does and also writes the codes / scale to x_i8 / x_scale.
+ * Ops may carry epilogues (dg_epilogue): a SwiGLU op streams W and W2 row by
+ * row in pairs, and an op reading another op's output (the down projection
+ * reading the SwiGLU result) waits for it like any other dependency.
  * Weights and scales must stay unchanged during the step (they are read
  * early).  ws: dg_workspace_bytes(ops, n_ops) bytes, 16-byte aligned, owned
  * by the caller; the step overwrites it (nothing needs to be zeroed first).

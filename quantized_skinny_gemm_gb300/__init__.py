@@ -14,6 +14,8 @@ __all__ = [
     "DGError", "Linear", "StepPlan", "F16", "BF16", "LINEAR_F16", "LINEAR_BF16",
     "LINEAR_W8A8", "LINEAR_W4A16", "LINEAR_W4A8", "gemv_f16", "gemv_w8a8", "gemv_w4",
     "quantize_act_i8", "lm_head_argmax", "lm_head_argmax_noalloc", "decode_step_weights", "workspace_bytes",
+    "EPI_NONE", "EPI_RESIDUAL", "EPI_SWIGLU", "ACT_NONE", "ACT_SILU", "linear_forward", "swiglu",
+    "residual_add", "causal_conv1d_update", "quantize_weights_i8", "quantize_weights_w4",
     "check_device_status", "selftest_wait_timeout", "status_string", "probe_copy", "probe_read", "version",
     "library_path", "load",
 ]
@@ -23,6 +25,8 @@ _LIB_PATH = os.path.join(_PKG, "libdg.so")
 
 F16, BF16 = 0, 1
 LINEAR_F16, LINEAR_BF16, LINEAR_W8A8, LINEAR_W4A16, LINEAR_W4A8 = range(5)
+EPI_NONE, EPI_RESIDUAL, EPI_SWIGLU = range(3)
+ACT_NONE, ACT_SILU = range(2)
 _STATUS = ["DG_OK", "DG_ERR_INVALID_ARG", "DG_ERR_UNSUPPORTED", "DG_ERR_MISALIGNED",
            "DG_ERR_WORKSPACE", "DG_ERR_CUDA", "DG_ERR_TIMEOUT"]
 
@@ -42,6 +46,8 @@ class Linear(ctypes.Structure):
         ("W", ctypes.c_void_p), ("w_scale", ctypes.c_void_p), ("x", ctypes.c_void_p),
         ("x_i8", ctypes.c_void_p), ("x_scale", ctypes.c_void_p), ("y", ctypes.c_void_p),
         ("logits", ctypes.c_void_p), ("token", ctypes.c_void_p), ("acc_out", ctypes.c_void_p),
+        ("epilogue", ctypes.c_int32), ("reserved", ctypes.c_int32), ("residual", ctypes.c_void_p),
+        ("W2", ctypes.c_void_p), ("w2_scale", ctypes.c_void_p),
     ]
 
 
@@ -72,6 +78,12 @@ def load():
         "dg_check_device_status": [P],
         "dg_selftest_wait_timeout": [ctypes.c_uint, P],
         "dg_probe_copy": [P, P, Z, P],
+        "dg_linear_forward": [P, P, Z, P],
+        "dg_swiglu": [P, P, P, I, P],
+        "dg_residual_add": [P, P, P, I, P],
+        "dg_causal_conv1d_update": [P, P, P, P, P, I, I, I, I, P],
+        "dg_quantize_weights_i8": [P, P, P, I, I, P],
+        "dg_quantize_weights_w4": [P, P, P, I, I, I, P],
         "dg_probe_read": [P, Z, P, P],
     }
     for name, args in sig.items():
@@ -144,10 +156,49 @@ def quantize_act_i8(x, xq, x_scale, stream=None):
 
 
 def linear(kind, W, M, N, K, w_scale=None, x=None, x_i8=None, x_scale=None, y=None,
-           logits=None, token=None, acc_out=None, group_size=32):
+           logits=None, token=None, acc_out=None, group_size=32, epilogue=EPI_NONE,
+           residual=None, W2=None, w2_scale=None):
     """Builds a Linear descriptor from tensors (pointers only; keep the tensors alive)."""
     return Linear(kind, M, N, K, group_size, _ptr(W), _ptr(w_scale), _ptr(x), _ptr(x_i8),
-                  _ptr(x_scale), _ptr(y), _ptr(logits), _ptr(token), _ptr(acc_out))
+                  _ptr(x_scale), _ptr(y), _ptr(logits), _ptr(token), _ptr(acc_out), epilogue, 0,
+                  _ptr(residual), _ptr(W2), _ptr(w2_scale))
+
+
+def linear_forward(op, ws=None, stream=None):
+    """Runs one op described by a Linear (any kind but an lm_head; any epilogue)."""
+    _call("dg_linear_forward", ctypes.byref(op), _ptr(ws), _nbytes(ws), _stream(stream))
+
+
+def swiglu(g, u, h, stream=None):
+    """h = silu(g) * u elementwise (fp16)."""
+    _call("dg_swiglu", _ptr(g), _ptr(u), _ptr(h), g.numel(), _stream(stream))
+
+
+def residual_add(a, b, out, stream=None):
+    """out = a + b elementwise (fp16)."""
+    _call("dg_residual_add", _ptr(a), _ptr(b), _ptr(out), a.numel(), _stream(stream))
+
+
+def causal_conv1d_update(x, state, w, y, bias=None, act=ACT_SILU, stream=None):
+    """One causal-conv1d decode step: x [M][C], state [M][C][W-1] (updated in
+    place), w [C][W], bias [C] or None, y [M][C]; all fp16."""
+    C, width = w.shape
+    M = x.numel() // C
+    _call("dg_causal_conv1d_update", _ptr(x), _ptr(state), _ptr(w), _ptr(bias), _ptr(y), M, C,
+          width, act, _stream(stream))
+
+
+def quantize_weights_i8(W, Wq, w_scale, stream=None):
+    """fp16 W [N][K] -> int8 Wq [N][K] + fp32 per-row scales (load-time packer)."""
+    N, K = W.shape
+    _call("dg_quantize_weights_i8", _ptr(W), _ptr(Wq), _ptr(w_scale), N, K, _stream(stream))
+
+
+def quantize_weights_w4(W, Wq, scales, group_size=32, stream=None):
+    """fp16 W [N][K] -> packed int4 Wq [N][K/2] + fp16 scales [N][K/group] (load-time packer)."""
+    N, K = W.shape
+    _call("dg_quantize_weights_w4", _ptr(W), _ptr(Wq), _ptr(scales), N, K, group_size,
+          _stream(stream))
 
 
 def lm_head_argmax(head, ws, stream=None):

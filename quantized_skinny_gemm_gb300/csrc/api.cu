@@ -265,6 +265,22 @@ dg_status validate(const dg_linear& op, bool allow_quant_input) {
             if (!al2(op.w_scale)) return DG_ERR_MISALIGNED;
             break;
     }
+    if (op.reserved) return DG_ERR_INVALID_ARG;
+    switch (op.epilogue) {
+        case DG_EPI_NONE: break;
+        case DG_EPI_RESIDUAL:
+            if (head || op.acc_out || !op.y || !op.residual) return DG_ERR_INVALID_ARG;
+            if (!al2(op.residual)) return DG_ERR_MISALIGNED;
+            break;
+        case DG_EPI_SWIGLU:
+            if (head || op.acc_out || !op.y || !op.W2) return DG_ERR_INVALID_ARG;
+            if (op.kind == DG_LINEAR_W8A8) return DG_ERR_UNSUPPORTED;
+            if ((op.kind == DG_LINEAR_W4A16 || op.kind == DG_LINEAR_W4A8) && !op.w2_scale)
+                return DG_ERR_INVALID_ARG;
+            if (!al16(op.W2) || (op.w2_scale && !al2(op.w2_scale))) return DG_ERR_MISALIGNED;
+            break;
+        default: return DG_ERR_INVALID_ARG;
+    }
     if (quantized_act(op.kind)) {
         if (!op.x_i8 || !op.x_scale) return DG_ERR_INVALID_ARG;
         if (!al16(op.x_i8) || !al4(op.x_scale)) return DG_ERR_MISALIGNED;
@@ -296,7 +312,8 @@ static void fill_common(GemvParams& p, const dg_linear& op) {
 
 // Whether W8A8 with this many tokens runs on the tensor-core kernel.
 static bool use_i8_mma(const dg_linear& op) {
-    if (op.kind != DG_LINEAR_W8A8 || op.M < 8 || op.K % 64 || tune().MMA == 0) return false;
+    if (op.kind != DG_LINEAR_W8A8 || op.M < 8 || op.K % 64 || tune().MMA == 0 || op.epilogue)
+        return false;
     return gemv_i8_mma_smem(op.K) <= smem_optin_limit();
 }
 
@@ -361,7 +378,7 @@ static int pick_kparts(const GemvLaunch& L, int N, int K) {
 // Workspace a per-op launch may use for split-K partials: 8 ranges of M x N
 // 4-byte sums, for launches small enough to split (device-independent).
 static size_t split_ws_bytes(const dg_linear& op) {
-    if (op.token) return 0;
+    if (op.token || op.epilogue) return 0;
     const size_t outs = (size_t)op.M * (size_t)op.N;
     if (outs > 65536) return 0;
     return (8 * outs * 4 + 255) & ~(size_t)255;
@@ -370,7 +387,7 @@ static size_t split_ws_bytes(const dg_linear& op) {
 // Whether fp16 / bf16 with this many tokens runs on the tensor-core tile.
 static bool use_fp_mma(const dg_linear& op) {
     if ((op.kind != DG_LINEAR_F16 && op.kind != DG_LINEAR_BF16) || op.M < 8 || op.K % 32 ||
-        tune().MMA == 0)
+        tune().MMA == 0 || op.epilogue)
         return false;
     return gemv_fp_mma_smem(op.K) <= smem_optin_limit();
 }
@@ -416,6 +433,7 @@ static dg_status launch_group(const dg_linear* ops, int n, cudaStream_t s, void*
                               size_t ws_bytes = 0) {
     GemvParams p;
     fill_common(p, ops[0]);
+    const bool pair = ops[0].epilogue == DG_EPI_SWIGLU;  // (such an op is alone: n == 1)
     int rows = 0;
     for (int i = 0; i < n; ++i) {
         Segment& g = p.t.seg[i];
@@ -429,12 +447,26 @@ static dg_status launch_group(const dg_linear* ops, int n, cudaStream_t s, void*
     }
     p.t.nseg = n;
     p.t.N = rows;
+    if (pair) {  // gate and up rows interleaved: 2N rows, y = silu(gate) * up
+        Segment& u = p.t.seg[1];
+        u.W = ops[0].W2;
+        u.scale = ops[0].w2_scale;
+        u.y = nullptr;
+        u.acc_out = nullptr;
+        u.row_begin = 0;
+        u.rows = ops[0].N;
+        p.t.nseg = 2;
+        p.t.N = 2 * ops[0].N;
+        p.t.pair = 1;
+    }
+    if (ops[0].epilogue == DG_EPI_RESIDUAL) p.t.res = ops[0].residual;
     if (use_i8_mma(ops[0])) return launch_i8_mma(p, s);
     if (use_fp_mma(ops[0])) return launch_fp_mma(p, ops[0].kind == DG_LINEAR_BF16, s);
     GemvLaunch L{fmt_of(ops[0].kind), pick_mt(ops[0].M), 0, false, ops[0].K, p.group, 0};
     L.R = pick_r(L.fmt, L.MT, L.K);
+    if (pair && (L.R & 1)) L.R = 2;  // a row group holds whole pairs
     configure(L, p);
-    if (ws && al16(ws)) {
+    if (ws && al16(ws) && !ops[0].epilogue) {
         const int S = pick_kparts(L, p.t.N, p.a.K);
         if (S > 1 && ws_bytes >= (size_t)S * p.a.M * p.t.N * 4) {
             p.kparts = S;
@@ -486,7 +518,7 @@ constexpr size_t kStepHeader = 256;
 // ---- the persistent decode-step path -----------------------------------------------
 
 static bool same_group(const dg_linear& a, const dg_linear& b) {
-    return !b.token && b.kind == a.kind && b.M == a.M && b.K == a.K && b.x == a.x &&
+    return !b.token && !a.epilogue && !b.epilogue && b.kind == a.kind && b.M == a.M && b.K == a.K && b.x == a.x &&
            b.x_i8 == a.x_i8 && b.x_scale == a.x_scale && b.group_size == a.group_size;
 }
 
@@ -540,6 +572,7 @@ static void op_ranges(const dg_linear& op, std::vector<Range>& rd, std::vector<R
     } else {
         add_range(rd, op.x, M * K * act_elem_bytes(op.kind));
     }
+    if (op.epilogue == DG_EPI_RESIDUAL) add_range(rd, op.residual, M * N * 2);
     add_range(wr, op.y, M * N * 2);
     add_range(wr, op.logits, N * 4);
     add_range(wr, op.token, 4);
@@ -566,6 +599,13 @@ static void weight_ranges(const dg_linear& op, std::vector<Range>& v) {
             add_range(v, op.W, N * K / 2);
             if (op.group_size > 0) add_range(v, op.w_scale, N * (K / (size_t)op.group_size) * 2);
             break;
+    }
+    if (op.epilogue == DG_EPI_SWIGLU) {  // the up projection, same format and shape
+        dg_linear up = op;
+        up.W = op.W2;
+        up.w_scale = op.w2_scale;
+        up.epilogue = DG_EPI_NONE;
+        weight_ranges(up, v);
     }
 }
 
@@ -653,6 +693,18 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
             }
             ph.nseg = j - i;
             ph.N = rows;
+            if (a.epilogue == DG_EPI_SWIGLU) {  // gate and up rows interleaved (j == i + 1)
+                StepSeg& u = ph.seg[1];
+                u.W = a.W2;
+                u.scale = a.w2_scale;
+                u.y = nullptr;
+                u.rows = a.N;
+                u.row_begin = 0;
+                ph.nseg = 2;
+                ph.N = 2 * a.N;
+                ph.pair = 1;
+            }
+            if (a.epilogue == DG_EPI_RESIDUAL) ph.res = a.residual;
             ph.K = a.K;
             ph.group = a.group_size >= 32 ? a.group_size : 32;
             ph.ks = pick_ks(f, a.K);
@@ -717,9 +769,16 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
         // sub-partition: 883 -> 863 us for the 32-layer step) when no phase
         // splits K, since the split barriers' id ranges are disjoint only up
         // to 16 warps
-        bool split = false;
-        for (int q = 0; q < sp.nphase; ++q) split = split || sp.ph[q].ks > 1;
-        const int nw = split ? 16 : tune().SNW > 0 ? tune().SNW : f == F_W4A8 ? 20 : 16;
+        bool split = false, pairs = false;
+        for (int q = 0; q < sp.nphase; ++q) {
+            split = split || sp.ph[q].ks > 1;
+            pairs = pairs || sp.ph[q].pair;
+        }
+        // (SwiGLU pair phases need an even number of rows per slot: the
+        // formats' defaults give that; a tuned warp count might not)
+        const int nw = split ? 16
+                             : (tune().SNW > 0 && !pairs) ? tune().SNW
+                                                          : f == F_W4A8 ? 20 : 16;
         const int occ = step_occupancy(f, max_k, smem, nw);
         if (occ < 1) return DG_ERR_UNSUPPORTED;
         const int grid = sm_count() * occ;
@@ -820,6 +879,14 @@ dg_status dg_gemv_w4(const uint8_t* Wq, const void* scales, int group_size, cons
     return launch_group(&op, 1, stream, ws, ws_bytes);
 }
 
+dg_status dg_linear_forward(const dg_linear* op, void* ws, size_t ws_bytes, dg_stream stream) {
+    if (!op || op->token) return DG_ERR_INVALID_ARG;
+    dg_status st = validate(*op, false);
+    if (st != DG_OK) return st;
+    if ((st = check_smem(*op)) != DG_OK) return st;
+    return launch_group(op, 1, stream, ws, ws_bytes);
+}
+
 dg_status dg_quantize_act_i8(const void* x, int8_t* xq, float* x_scale, int M, int K,
                              dg_stream stream) {
     if (!x || !xq || !x_scale || M < 1 || K < 1) return DG_ERR_INVALID_ARG;
@@ -901,6 +968,50 @@ dg_status dg_selftest_wait_timeout(unsigned spin_limit, dg_stream stream) {
     int* w = device_error_word();
     if (!w) return DG_ERR_CUDA;
     return to_status(launch_wait_selftest(spin_limit, w, stream));
+}
+
+static bool ranges_overlap(const void* a, size_t an, const void* b, size_t bn) {
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return x < y + bn && y < x + an;
+}
+
+dg_status dg_swiglu(const void* g, const void* u, void* h, int n, dg_stream stream) {
+    if (!g || !u || !h || n < 1) return DG_ERR_INVALID_ARG;
+    if (n % 8 || !al16(g) || !al16(u) || !al16(h)) return DG_ERR_MISALIGNED;
+    return to_status(launch_swiglu(g, u, h, n, stream));
+}
+
+dg_status dg_residual_add(const void* a, const void* b, void* out, int n, dg_stream stream) {
+    if (!a || !b || !out || n < 1) return DG_ERR_INVALID_ARG;
+    if (n % 8 || !al16(a) || !al16(b) || !al16(out)) return DG_ERR_MISALIGNED;
+    return to_status(launch_residual_add(a, b, out, n, stream));
+}
+
+dg_status dg_causal_conv1d_update(const void* x, void* state, const void* w, const void* bias,
+                                  void* y, int M, int C, int width, int act, dg_stream stream) {
+    if (!x || !state || !w || !y || M < 1 || C < 1) return DG_ERR_INVALID_ARG;
+    if (act != DG_ACT_NONE && act != DG_ACT_SILU) return DG_ERR_INVALID_ARG;
+    if (width < 2 || width > 8) return DG_ERR_UNSUPPORTED;
+    if (C % 8 || !al16(x) || !al16(state) || !al16(w) || !al16(y) || (bias && !al16(bias)))
+        return DG_ERR_MISALIGNED;
+    const size_t sb = (size_t)M * C * (width - 1) * 2;
+    if (ranges_overlap(y, (size_t)M * C * 2, state, sb)) return DG_ERR_INVALID_ARG;
+    return to_status(launch_conv1d_update(x, state, w, bias, y, M, C, width, act, stream));
+}
+
+dg_status dg_quantize_weights_i8(const void* W, int8_t* Wq, float* w_scale, int N, int K,
+                                 dg_stream stream) {
+    if (!W || !Wq || !w_scale || N < 1 || K < 1) return DG_ERR_INVALID_ARG;
+    if (K % 16 || !al16(W) || !al16(Wq) || !al4(w_scale)) return DG_ERR_MISALIGNED;
+    return to_status(launch_quant_w8(W, Wq, w_scale, N, K, stream));
+}
+
+dg_status dg_quantize_weights_w4(const void* W, uint8_t* Wq, void* scales, int N, int K,
+                                 int group_size, dg_stream stream) {
+    if (!W || !Wq || !scales || N < 1 || K < 1) return DG_ERR_INVALID_ARG;
+    if (group_size < 32 || group_size % 32 || K % group_size) return DG_ERR_UNSUPPORTED;
+    if (!al16(W) || !al16(Wq) || !al2(scales)) return DG_ERR_MISALIGNED;
+    return to_status(launch_quant_w4(W, Wq, scales, N, K, group_size, stream));
 }
 
 dg_status dg_probe_copy(const void* src, void* dst, size_t bytes, dg_stream stream) {

@@ -31,10 +31,16 @@ struct Segment {
 };
 
 // The matrices of one fused launch (same activations, K and format).
+// Epilogues: `res` adds a residual [M][rows] to the op's result (a launch with
+// a residual holds that one op); `pair` marks a SwiGLU op, whose two segments
+// (gate, up) are walked row by row in pairs: global row 2i is gate row i,
+// 2i + 1 up row i, and y[i] = silu(gate) * up lands in segment 0's y.
 struct SegTable {
     Segment seg[kMaxSeg];
     int nseg;
     int N;               // rows over all segments
+    int pair;
+    const void* res;
 };
 
 // Activations of a launch or phase.
@@ -99,8 +105,10 @@ struct StepPhase {
     float* logits;        // lm_head
     int32_t* token;       // lm_head
     unsigned char* xlay;  // kPhaseXLaid: the activations in the format's layout (workspace)
+    const void* res;      // residual [1][N] added before rounding (a one-op phase)
     int32_t K, N, nseg, flags, ks;
     int32_t group;        // int4 scale group along K (the ops of a phase share it)
+    int32_t pair;         // SwiGLU: segments 0 (gate) and 1 (up) interleaved by row
 };
 
 struct StepParams {
@@ -227,6 +235,11 @@ __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) {
     return *reinterpret_cast<__half2*>(&u);
 }
 
+// silu(v) = v / (1 + e^-v) in fp32: the library exp and IEEE operations (a
+// few fp32 roundings).  For v below about -88, e^-v overflows to infinity and
+// the result is -0, next to the true value (whose magnitude is below 1e-36).
+__device__ __forceinline__ float silu_f32(float v) { return v / (1.f + expf(-v)); }
+
 // Total order of the greedy argmax: larger value first, then lower index; a
 // NaN value is never better.
 __device__ __forceinline__ bool arg_better(float v, int i, float bv, int bi) {
@@ -316,6 +329,14 @@ cudaError_t launch_argmax_pass2(const ArgPart* part, int nparts, int32_t* token,
 cudaError_t launch_quant_act(const __half* x, int8_t* xq, float* s, int M, int K,
                              cudaStream_t st);
 cudaError_t launch_probe_copy(const void* src, void* dst, size_t bytes, cudaStream_t s);
+// aux_kernels.cu
+cudaError_t launch_swiglu(const void* g, const void* u, void* h, int n, cudaStream_t s);
+cudaError_t launch_residual_add(const void* a, const void* b, void* out, int n, cudaStream_t s);
+cudaError_t launch_conv1d_update(const void* x, void* state, const void* w, const void* bias,
+                                 void* y, int M, int C, int width, int silu, cudaStream_t s);
+cudaError_t launch_quant_w8(const void* W, int8_t* Wq, float* s, int N, int K, cudaStream_t st);
+cudaError_t launch_quant_w4(const void* W, uint8_t* Wq, void* scales, int N, int K, int G,
+                            cudaStream_t st);
 cudaError_t launch_probe_read(const void* src, size_t bytes, uint32_t* sink, cudaStream_t s);
 
 }  // namespace dg

@@ -40,17 +40,28 @@ struct RowRef {
     bool valid;
 };
 
+// Segment of global row r and the row's index inside it: by position, or for
+// a SwiGLU pair table by parity (row 2i is gate row i, 2i + 1 up row i).
+__device__ __forceinline__ int seg_of_row(const SegTable& t, int r, int* local) {
+    if (t.pair) {
+        *local = r >> 1;
+        return r & 1;
+    }
+    int s = 0;
+#pragma unroll
+    for (int i = 1; i < kMaxSeg; ++i)
+        if (i < t.nseg && r >= t.seg[i].row_begin) s = i;
+    *local = r - t.seg[s].row_begin;
+    return s;
+}
+
 __device__ __forceinline__ RowRef locate(const SegTable& t, int r, size_t row_bytes,
                                          const RowRef& fallback) {
     RowRef rr = fallback;
     rr.valid = false;
     if (r >= t.N) return rr;
-    int s = 0;
-#pragma unroll
-    for (int i = 1; i < kMaxSeg; ++i)
-        if (i < t.nseg && r >= t.seg[i].row_begin) s = i;
+    const int s = seg_of_row(t, r, &rr.local);
     const Segment& sg = t.seg[s];
-    rr.local = r - sg.row_begin;
     rr.w = static_cast<const unsigned char*>(sg.W) + (size_t)rr.local * row_bytes;
     rr.scale = sg.scale;
     rr.y = sg.y;
@@ -74,6 +85,22 @@ __device__ __forceinline__ float from_bits<float>(int v) { return __int_as_float
 template <>
 __device__ __forceinline__ int from_bits<int>(int v) { return v; }
 
+// Writes an op's final fp32 value for token m of row r into its output, as
+// fp16 (bf16 for the bf16 format), round to nearest even.
+template <bool BF16>
+__device__ __forceinline__ void write_out(const RowRef& r, int m, float v) {
+    const size_t o = (size_t)m * r.seg_rows + r.local;
+    if (BF16)
+        static_cast<__nv_bfloat16*>(r.y)[o] = __float2bfloat16_rn(v);
+    else
+        static_cast<__half*>(r.y)[o] = __float2half_rn(v);
+}
+template <bool BF16>
+__device__ __forceinline__ float read_res(const void* res, size_t o) {
+    return BF16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(res)[o])
+                : __half2float(static_cast<const __half*>(res)[o]);
+}
+
 // ---- format policies ------------------------------------------------------------
 // stage_x fills the CTA's activation area from `a`; the int8 policies read
 // their codes from `a.xq`, which may point to global or shared memory.
@@ -93,6 +120,7 @@ __device__ __forceinline__ float2 unpack2_f32(uint32_t w) {
 // shared memory.
 template <bool BF16>
 struct PolicyFP {
+    static constexpr bool kBF16 = BF16;
     static constexpr int kElems = 8;
     static constexpr bool kMacRows = false;  // one row per mac() call
     static constexpr bool kIntAct = false;
@@ -164,6 +192,7 @@ struct PolicyFP {
 
 // int8 weights x int8 activations, exact int32 sums; 16 elements per chunk.
 struct PolicyI8 {
+    static constexpr bool kBF16 = false;
     static constexpr int kElems = 16;
     static constexpr bool kMacRows = false;  // one row per mac() call
     static constexpr bool kIntAct = true;
@@ -266,6 +295,7 @@ __device__ __forceinline__ unsigned int4_x_piece(int c, int i, int pieces) {
 // before the group scale is applied.  All rows of a slot go through one call,
 // so each activation piece is loaded once for all of them.
 struct PolicyW4A16 {
+    static constexpr bool kBF16 = false;
     static constexpr int kElems = 32;
     static constexpr bool kIntAct = false;
     static constexpr bool kDirectX = false;
@@ -353,6 +383,7 @@ struct PolicyW4A16 {
 // x0 x2 x4 x6 | x1 x3 x5 x7 (even codes sit in low nibbles), followed by the
 // int32 sum of each 32-chunk.
 struct PolicyW4A8 {
+    static constexpr bool kBF16 = false;
     static constexpr int kElems = 32;
     static constexpr bool kMacRows = false;  // one row per mac() call
     static constexpr bool kIntAct = true;
@@ -443,6 +474,23 @@ struct PolicyW4A8 {
         static_cast<__half*>(r.y)[(size_t)m * r.seg_rows + r.local] = __float2half_rn(sx * a);
     }
 };
+
+// Stores token m of row r: the plain store, or with an epilogue the fp32
+// result plus the residual (res, [M][rows] of the output type), or for a
+// SwiGLU pair silu(gate) * up with `up` the pair's second row.
+template <class P>
+__device__ __forceinline__ void store_row(const RowRef& r, int m, typename P::Acc a, float sx,
+                                          const void* res, bool pair, const RowRef& up,
+                                          typename P::Acc au) {
+    if (!res && !pair) {
+        P::store(r, m, a, sx);
+        return;
+    }
+    float v = P::finish(r, a, sx);
+    if (res) v += read_res<P::kBF16>(res, (size_t)m * r.seg_rows + r.local);
+    if (pair) v = silu_f32(v) * P::finish(up, au, sx);
+    write_out<P::kBF16>(r, m, v);
+}
 
 // Named barrier of warp `warp`'s slot when ks = 2, 4 or 8 warps share a row.
 // In a persistent kernel warps move through phases independently, so phases
@@ -760,6 +808,7 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvP
                         }
                     }
                 } else {
+                    if (p.t.pair && (r & 1)) continue;  // stored with its gate row
 #pragma unroll
                     for (int m = 0; m < MT; ++m)
                         if (m < p.a.M && lane == ((r * MT + m) & 31)) {
@@ -768,7 +817,9 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvP
                                                            rows[r].global] = to_bits(acc[r][m]);
                             } else {
                                 const float sx = p.a.x_scale ? __ldg(p.a.x_scale + m) : 1.f;
-                                P::store(rows[r], m, acc[r][m], sx);
+                                const int ru = r + 1 < R ? r + 1 : r;  // (pairs: R is even)
+                                store_row<P>(rows[r], m, acc[r][m], sx, p.t.res, p.t.pair != 0,
+                                             rows[ru], acc[ru][m]);
                             }
                         }
                 }
@@ -876,6 +927,8 @@ cudaError_t run_family_main(const GemvLaunch& L, const GemvParams* p, cudaStream
         case 16:
             if constexpr (P::kElems == 16) {
                 if (L.R == 4) return run_one<P, 16, 4, false>(p, L.grid, smem, s, occ);
+            } else {
+                if (L.R == 2) return run_one<P, 16, 2, false>(p, L.grid, smem, s, occ);  // SwiGLU pairs
             }
             return run_one<P, 16, 1, false>(p, L.grid, smem, s, occ);
         default: return cudaErrorInvalidValue;

@@ -6,15 +6,22 @@
 
 namespace dg {
 
-// Row r (global over the phase's segments) of phase ph.
+// Row r (global over the phase's segments) of phase ph; a SwiGLU phase
+// (ph.pair) interleaves its gate and up rows: row 2i is gate row i, 2i + 1 up
+// row i.
 __device__ __forceinline__ RowRef locate_step(const StepPhase& ph, int r, size_t rb) {
     RowRef rr{};
     int s = 0;
+    if (ph.pair) {
+        s = r & 1;
+        rr.local = r >> 1;
+    } else {
 #pragma unroll
-    for (int i = 1; i < kMaxSeg; ++i)
-        if (i < ph.nseg && r >= ph.seg[i].row_begin) s = i;
+        for (int i = 1; i < kMaxSeg; ++i)
+            if (i < ph.nseg && r >= ph.seg[i].row_begin) s = i;
+        rr.local = r - ph.seg[s].row_begin;
+    }
     const StepSeg& sg = ph.seg[s];
-    rr.local = r - sg.row_begin;
     rr.w = static_cast<const unsigned char*>(sg.W) + (size_t)rr.local * rb;
     rr.scale = sg.scale;
     rr.y = sg.y;
@@ -76,7 +83,9 @@ __device__ void plan_phases(const StepParams& sp, PhaseSlice* table, int b, int 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     for (int p = warp; p < sp.nphase; p += nw) {
         const StepPhase& ph = sp.ph[p];
-        const int r0 = slice_begin(ph.N, b, G), r1 = slice_begin(ph.N, b + 1, G);
+        // a SwiGLU phase is sliced by pairs, so a pair never straddles CTAs
+        const int f = ph.pair ? 2 : 1, Nu = ph.N / f;
+        const int r0 = f * slice_begin(Nu, b, G), r1 = f * slice_begin(Nu, b + 1, G);
         if (lane == 0) {
             table[p].r0 = r0;
             table[p].n = r1 - r0;

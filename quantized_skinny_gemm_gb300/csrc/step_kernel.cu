@@ -347,8 +347,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
                                 best_i = rows[r].global;
                             }
                         }
-                    } else if (lane == r) {
-                        P::store(rows[r], 0, acc[r][0], sx);
+                    } else if (lane == r && !(ph.pair && (r & 1))) {
+                        const int ru = r + 1 < R ? r + 1 : r;  // (pairs: R is even)
+                        store_row<P>(rows[r], 0, acc[r][0], sx, ph.res, ph.pair != 0, rows[ru],
+                                     acc[ru][0]);
                     }
                 }
             }

@@ -15,7 +15,8 @@ from typing import Dict, List, Optional
 
 import torch
 
-from . import LINEAR_F16, LINEAR_W4A16, LINEAR_W4A8, LINEAR_W8A8, StepPlan, linear
+from . import (EPI_RESIDUAL, EPI_SWIGLU, LINEAR_F16, LINEAR_W4A16, LINEAR_W4A8, LINEAR_W8A8,
+               StepPlan, decode_step_weights, linear, residual_add, swiglu)
 
 
 class Arena:
@@ -70,6 +71,7 @@ def count_launches(ops, persistent=True):
     """Kernel launches (memsets excluded) dg_decode_step_weights issues for
     these ops: with the persistent kernel, one per run of single-token ops of
     one kind (per 144 fused groups); otherwise one per fused group (same kind,
+    no epilogue,
     M, K, group and activation pointers, up to 4 ops, an lm_head alone), plus
     the lm_head's argmax pass and one quantization launch per fused group with
     fp16 inputs to an int8-activation kind."""
@@ -78,10 +80,11 @@ def count_launches(ops, persistent=True):
         while i < hi:
             a = ops[i]
             j = i + 1
-            if not a.token:
+            if not a.token and not a.epilogue:
                 while j < hi and j - i < 4:
                     b = ops[j]
-                    if (b.token or b.kind != a.kind or b.M != a.M or b.K != a.K or b.x != a.x
+                    if (b.token or b.epilogue or b.kind != a.kind or b.M != a.M or b.K != a.K
+                            or b.x != a.x
                             or b.x_i8 != a.x_i8 or b.x_scale != a.x_scale
                             or b.group_size != a.group_size):
                         break
@@ -190,7 +193,16 @@ def int4_decode_step(layers, head, x_head, device, act="a16", M=1, group=32) -> 
         outs.append(ys)
     logits = token = xh = None
     hcodes = None
-    if head is not None:
+    if head is not None and head.scales is None:
+        # an fp16 lm_head after the int4 layers (a second persistent launch)
+        W = head.W.to(device)
+        xh = in_views[head_ids[0]]
+        xh.copy_(x_head)
+        logits, token = out_views[head_ids[1]], out_views[head_ids[2]]
+        ops.append(linear(LINEAR_F16, W, 1, head.N, head.K, x=xh, logits=logits, token=token))
+        keep.append(W)
+        wbytes += _nbytes(W)
+    elif head is not None:
         W, S = head.W.to(device), head.scales.to(device)
         xh = in_views[head_ids[0]]
         xh.copy_(x_head)
@@ -206,3 +218,95 @@ def int4_decode_step(layers, head, x_head, device, act="a16", M=1, group=32) -> 
     ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=device)
     return DeviceStep(plan, ws, ins, outs, ain.buf, aout.buf, wbytes, count_launches(ops),
                       logits, token, xh, keep=keep, act_codes=codes, head_codes=hcodes)
+
+
+@dataclass
+class BlockStep:
+    """A decoder-block step with its epilogues: fused (one dg_decode_step_weights
+    call, residual and SwiGLU in the stream's epilogues) or unfused (the
+    GEMVs, then separate elementwise launches).  run() enqueues one step."""
+    run: object
+    inputs: List[Dict[str, torch.Tensor]]      # per layer: x_attn, x_o, x_mlp, h
+    outputs: List[Dict[str, torch.Tensor]]     # per layer: q, k, v, h1, act, h2
+    in_arena: torch.Tensor
+    out_arena: torch.Tensor
+    weight_bytes: int
+    n_launches: int
+    plan: Optional[StepPlan] = None
+    ws: Optional[torch.Tensor] = None
+    keep: list = field(default_factory=list)
+
+
+def fp16_block_step(layers, hs, device, fused=True) -> BlockStep:
+    """The 1536-wide fp16 decoder as decoder blocks (synth.decode_fp16_workload
+    layers, synth.residual_stream inputs hs).  Per layer: q, k, v = W x_attn;
+    h1 = h + W_o x_o; act = silu(W_gate x_mlp) * (W_up x_mlp); h2 = h1 +
+    W_down act.  The attention and the norms between them are not part of the
+    weight stream: x_attn, x_o and x_mlp are synthetic inputs.  Fused: the
+    residual adds and SwiGLU are epilogues of one persistent launch (down
+    waits for act and h1 inside it).  Unfused: per layer the GEMVs of q, k, v,
+    o, gate and up in one launch, then h1 = h + o, act = swiglu(gate, up),
+    the down GEMV and h2 = h1 + down as launches of their own."""
+    ain, aout = Arena(), Arena()
+    M = 1
+    names_in = ("x_attn", "x_o", "x_mlp")
+    in_ids, out_ids = [], []
+    for L, h in zip(layers, hs):
+        hidden = h.shape[1]
+        inter = next(l.N for l in L.linears if l.name == "gate")
+        ids = {k: ain.reserve(L.inputs[k].shape, torch.float16) for k in names_in}
+        ids["h"] = ain.reserve(h.shape, torch.float16)
+        in_ids.append(ids)
+        o = {n: aout.reserve((M, l.N), torch.float16) for l in L.linears for n in (l.name,)
+             if n in ("q", "k", "v")}
+        o["h1"] = aout.reserve((M, hidden), torch.float16)
+        o["act"] = aout.reserve((M, inter), torch.float16)
+        o["h2"] = aout.reserve((M, hidden), torch.float16)
+        if not fused:  # the unfused GEMV outputs
+            for n, width in (("o", hidden), ("gate", inter), ("up", inter), ("down", hidden)):
+                o["y_" + n] = aout.reserve((M, width), torch.float16)
+        out_ids.append(o)
+    in_views, out_views = ain.build(device), aout.build(device)
+    keep, ins, outs, wbytes = [ain.buf, aout.buf], [], [], 0
+    fused_ops, per_layer = [], []
+    for L, h, iid, oid in zip(layers, hs, in_ids, out_ids):
+        xin = {k: in_views[iid[k]] for k in iid}
+        for k in names_in:
+            xin[k].copy_(L.inputs[k])
+        xin["h"].copy_(h)
+        ys = {k: out_views[oid[k]] for k in oid}
+        W = {l.name: l.W.to(device) for l in L.linears}
+        keep += list(W.values())
+        wbytes += sum(_nbytes(w) for w in W.values())
+        lin = {l.name: l for l in L.linears}
+        mk = lambda n, x, y, **kw: linear(LINEAR_F16, W[n], M, lin[n].N, lin[n].K, x=x, y=y, **kw)
+        qkv = [mk(n, xin["x_attn"], ys[n]) for n in ("q", "k", "v")]
+        if fused:
+            fused_ops += qkv + [
+                mk("o", xin["x_o"], ys["h1"], epilogue=EPI_RESIDUAL, residual=xin["h"]),
+                mk("gate", xin["x_mlp"], ys["act"], epilogue=EPI_SWIGLU, W2=W["up"]),
+                mk("down", ys["act"], ys["h2"], epilogue=EPI_RESIDUAL, residual=ys["h1"])]
+        else:
+            head = qkv + [mk("o", xin["x_o"], ys["y_o"]), mk("gate", xin["x_mlp"], ys["y_gate"]),
+                          mk("up", xin["x_mlp"], ys["y_up"])]
+            down = [mk("down", ys["act"], ys["y_down"])]
+            per_layer.append((StepPlan(head), StepPlan(down), xin, ys))
+        ins.append(xin)
+        outs.append(ys)
+    if fused:
+        plan = StepPlan(fused_ops, keep)
+        ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=device)
+        run = lambda stream=None: decode_step_weights(plan, ws, stream=stream)
+        return BlockStep(run, ins, outs, ain.buf, aout.buf, wbytes, 1, plan, ws, keep)
+    wsb = max(max(a.workspace_bytes(), b.workspace_bytes()) for a, b, _, _ in per_layer)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=device)
+
+    def run(stream=None):
+        for head, down, xin, ys in per_layer:
+            decode_step_weights(head, ws, stream=stream)
+            residual_add(xin["h"], ys["y_o"], ys["h1"], stream=stream)
+            swiglu(ys["y_gate"], ys["y_up"], ys["act"], stream=stream)
+            decode_step_weights(down, ws, stream=stream)
+            residual_add(ys["h1"], ys["y_down"], ys["h2"], stream=stream)
+    keep.append(per_layer)
+    return BlockStep(run, ins, outs, ain.buf, aout.buf, wbytes, 5 * len(per_layer), None, ws, keep)

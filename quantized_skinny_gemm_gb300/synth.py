@@ -184,3 +184,18 @@ def weight_bytes(linears) -> int:
         if l.scales is not None:
             tot += l.scales.numel() * l.scales.element_size()
     return tot
+
+
+def residual_stream(layers, hidden, seed=0, M=1):
+    """Per layer, the residual-stream input h [M][hidden] ~N(0, 1) of a decoder
+    block whose o and down projections add into it (drawn from their own
+    generator, so the decoder workloads above are unchanged)."""
+    g = generator(seed + 7919)
+    return [normal((M, hidden), 1.0, g) for _ in range(layers)]
+
+
+def fp16_head(vocab, hidden, seed=0):
+    """An fp16 lm_head [vocab][hidden] ~N(0, 0.02) for the int4 decoder (its own
+    generator, so the int4 workload's draws are unchanged)."""
+    g = generator(seed + 104729)
+    return Linear("lm_head", vocab, hidden, normal((vocab, hidden), W_STD, g), None, "x_head")

@@ -45,9 +45,12 @@ def test_status_strings(lib):
 
 
 def test_linear_struct_layout_matches_header():
-    # 5 int32 then 9 pointers: 20 bytes + 4 bytes padding + 72
-    assert ctypes.sizeof(dg.Linear) == 96
+    # 5 int32, 4 bytes padding, 9 pointers (to 96), epilogue + reserved int32, 3 pointers
+    assert ctypes.sizeof(dg.Linear) == 128
     assert dg.Linear.W.offset == 24
+    assert dg.Linear.epilogue.offset == 96
+    assert dg.Linear.residual.offset == 104
+    assert dg.Linear.W2.offset == 112 and dg.Linear.w2_scale.offset == 120
 
 
 def test_gemv_f16_validation(lib):
@@ -191,3 +194,51 @@ def test_selftest_validation(lib):
 def test_probe_validation(lib):
     assert lib.dg_probe_copy(A, B, 24, None) == MISALIGNED
     assert lib.dg_probe_read(None, 16, A, None) == INVALID
+
+
+def _op(**kw):
+    d = dict(kind=dg.LINEAR_F16, M=1, N=8, K=64, group_size=32, W=A, x=A, y=B)
+    d.update(kw)
+    return dg.Linear(**d)
+
+
+def test_linear_forward_and_epilogue_validation(lib):
+    f = lib.dg_linear_forward
+    assert f(None, None, 0, None) == INVALID
+    assert f(ctypes.byref(_head()), None, 0, None) == INVALID           # lm_heads go elsewhere
+    assert f(ctypes.byref(_op(epilogue=7)), None, 0, None) == INVALID
+    assert f(ctypes.byref(_op(reserved=1)), None, 0, None) == INVALID
+    assert f(ctypes.byref(_op(epilogue=dg.EPI_RESIDUAL)), None, 0, None) == INVALID  # no residual
+    assert f(ctypes.byref(_op(epilogue=dg.EPI_RESIDUAL, residual=B + 1)), None, 0,
+             None) == MISALIGNED
+    assert f(ctypes.byref(_op(epilogue=dg.EPI_SWIGLU)), None, 0, None) == INVALID    # no W2
+    assert f(ctypes.byref(_op(epilogue=dg.EPI_SWIGLU, W2=ODD)), None, 0, None) == MISALIGNED
+    assert f(ctypes.byref(_op(kind=dg.LINEAR_W4A16, w_scale=A, epilogue=dg.EPI_SWIGLU, W2=A)),
+             None, 0, None) == INVALID                                    # no w2_scale
+    assert f(ctypes.byref(_op(kind=dg.LINEAR_W8A8, w_scale=A, x=None, x_i8=A, x_scale=A,
+                              epilogue=dg.EPI_SWIGLU, W2=A)), None, 0, None) == UNSUPPORTED
+    assert f(ctypes.byref(_op(kind=dg.LINEAR_W8A8, w_scale=A, x=None, x_i8=A, x_scale=A,
+                              acc_out=B, epilogue=dg.EPI_RESIDUAL, residual=A)), None, 0,
+             None) == INVALID
+    head = _head(epilogue=dg.EPI_RESIDUAL, residual=A)
+    arr = (dg.Linear * 1)(head)
+    assert lib.dg_decode_step_weights(ctypes.cast(arr, ctypes.c_void_p), 1, A, 1 << 20,
+                                      None) == INVALID
+    # epilogue ops never split K: no split-K workspace is asked for them
+    assert dg.workspace_bytes([_op(N=256, epilogue=dg.EPI_RESIDUAL, residual=A)]) == 256
+
+
+def test_elementwise_conv1d_and_packer_validation(lib):
+    assert lib.dg_swiglu(None, A, B, 8, None) == INVALID
+    assert lib.dg_swiglu(A, A, B, 12, None) == MISALIGNED
+    assert lib.dg_residual_add(A, ODD, B, 8, None) == MISALIGNED
+    c = lib.dg_causal_conv1d_update
+    assert c(None, B, A, None, 0x300000, 1, 16, 4, 1, None) == INVALID
+    assert c(A, B, A, None, 0x300000, 1, 16, 4, 5, None) == INVALID     # act
+    assert c(A, B, A, None, 0x300000, 1, 16, 9, 1, None) == UNSUPPORTED  # width
+    assert c(A, B, A, None, 0x300000, 1, 12, 4, 1, None) == MISALIGNED   # C % 8
+    assert c(A, B, A, ODD, 0x300000, 1, 16, 4, 1, None) == MISALIGNED    # bias
+    assert c(A, B, A, None, B + 16, 1, 16, 4, 1, None) == INVALID        # y overlaps state
+    assert lib.dg_quantize_weights_i8(A, B, A, 8, 24, None) == MISALIGNED
+    assert lib.dg_quantize_weights_w4(A, B, A, 8, 96, 64, None) == UNSUPPORTED
+    assert lib.dg_quantize_weights_w4(A, B, A + 1, 8, 64, 32, None) == MISALIGNED
