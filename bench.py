@@ -156,6 +156,17 @@ class Workload:
     config = {}
 
 
+_INT4_DATA = {}
+
+
+def int4_decoder_data(synth):
+    """The 32-layer int4 decoder's host data (seed 0), drawn once per process:
+    its W4A16, W4A8 and fp16-head variants stream the same layers."""
+    if "d" not in _INT4_DATA:
+        _INT4_DATA["d"] = synth.decode_int4_workload(seed=0)
+    return _INT4_DATA["d"]
+
+
 def build_workload(name, dev, torch):
     import quantized_skinny_gemm_gb300 as dg
     from quantized_skinny_gemm_gb300 import plans, synth
@@ -183,7 +194,7 @@ def build_workload(name, dev, torch):
         act = name[-3:]
         small = "_4l_" in name
         layers, head, xh = (synth.decode_int4_workload(seed=0, layers=4, vocab=0) if small
-                            else synth.decode_int4_workload(seed=0))
+                            else int4_decoder_data(synth))
         st = plans.int4_decode_step(layers, head, xh, dev, act=act)
         w.host = (layers, head, xh)
         w.in_arena, w.out_arena = st.in_arena, st.out_arena
@@ -282,6 +293,115 @@ def build_workload(name, dev, torch):
         assert w.config["weight_bytes_per_step"] == st.weight_bytes
         w.dominant = ("decode step (persistent kernel)", w.run, 1, st.weight_bytes)
         w.cpu_sample = ("fp", layers)
+    elif name in ("block_fp16_fused", "block_fp16_unfused"):
+        # the 28-layer 1536-wide decoder as decoder blocks with their epilogues
+        layers = synth.decode_fp16_workload(seed=0)
+        hs = synth.residual_stream(len(layers), 1536, seed=0)
+        st = plans.fp16_block_step(layers, hs, dev, fused=name.endswith("_fused"))
+        w.host = (layers, hs)
+        w.in_arena, w.out_arena = st.in_arena, st.out_arena
+        w.unit_bytes = st.weight_bytes
+        w.launches = st.n_launches
+        w.run = lambda: st.run(stream=s)
+        w.config = workload_config(name)
+        assert w.config["weight_bytes_per_step"] == st.weight_bytes
+        w.dominant = ("decoder-block step (%s)" % name[10:], w.run, 1, st.weight_bytes)
+        w.cpu_sample = ("fp", layers)
+        w.keep = st
+    elif name == "decode_int4_a16_f16head":
+        layers, _, xh = int4_decoder_data(synth)
+        head = synth.fp16_head(128256, 4096, seed=0)
+        st = plans.int4_decode_step(layers, head, xh, dev, act="a16")
+        w.host = (layers, head, xh)
+        w.in_arena, w.out_arena = st.in_arena, st.out_arena
+        w.unit_bytes = st.weight_bytes
+        w.launches = st.n_launches
+        w.run = lambda: dg.decode_step_weights(st.plan, st.ws, stream=s)
+        w.config = workload_config(name)
+        assert w.config["weight_bytes_per_step"] == st.weight_bytes
+        w.dominant = ("int4 decode step + fp16 lm_head (two persistent launches)", w.run, 1,
+                      st.weight_bytes)
+        w.cpu_sample = ("w4a16", (layers, None, None))
+        w.dtype = "int4xf16"
+    elif name == "conv1d":
+        # one decode step of 24 depthwise causal-conv1d layers, 8192 channels,
+        # 4 taps, SiLU (one launch per layer, in layer order)
+        L, C, Wd = 24, 8192, 4
+        g = synth.generator(0)
+        xs = [synth.normal((1, C), 1.0, g).to(dev) for _ in range(L)]
+        sts = [synth.normal((1, C, Wd - 1), 1.0, g).to(dev) for _ in range(L)]
+        wts = [synth.normal((C, Wd), 0.5, g).to(dev) for _ in range(L)]
+        bs = [synth.normal((C,), 0.1, g).to(dev) for _ in range(L)]
+        ys = [torch.empty(1, C, dtype=torch.float16, device=dev) for _ in range(L)]
+        w.host = None
+        w.in_arena = torch.cat([t.view(-1) for t in xs]).view(torch.uint8)
+        w.out_arena = torch.cat([t.view(-1) for t in ys]).view(torch.uint8)
+        per = C * (2 * Wd + 2 * 2 * (Wd - 1) + 2 + 2 + 2)   # taps, window in+out, x, y, bias
+        w.unit_bytes = L * per
+        w.launches = L
+        w.run = lambda: [dg.causal_conv1d_update(xs[i], sts[i], wts[i], ys[i], bias=bs[i], stream=s)
+                         for i in range(L)]
+        w.config = workload_config(name)
+        w.dominant = ("causal-conv1d step, 8192 channels, 4 taps", w.run, L, per)
+        w.cpu_sample = ("conv", (C, Wd))
+        w.keep = (xs, sts, wts, bs, ys)
+    elif name in ("quant_w4", "quant_w8"):
+        # the load-time packers on a 14336x4096 fp16 matrix (rotating copies > 2x L2)
+        N, K = 14336, 4096
+        per = N * K * 2
+        C = -(-2 * L2_BYTES // per)
+        Ws = [synth.normal((N, K), synth.W_STD, synth.generator(i)).to(dev) for i in range(C)]
+        if name == "quant_w4":
+            outs = [(torch.empty(N, K // 2, dtype=torch.uint8, device=dev),
+                     torch.empty(N, K // 32, dtype=torch.float16, device=dev)) for _ in range(C)]
+            calls = [lambda Wd=Wd, o=o: dg.quantize_weights_w4(Wd, o[0], o[1], stream=s)
+                     for Wd, o in zip(Ws, outs)]
+        else:
+            outs = [(torch.empty(N, K, dtype=torch.int8, device=dev),
+                     torch.empty(N, dtype=torch.float32, device=dev)) for _ in range(C)]
+            calls = [lambda Wd=Wd, o=o: dg.quantize_weights_i8(Wd, o[0], o[1], stream=s)
+                     for Wd, o in zip(Ws, outs)]
+        w.host = None
+        w.in_arena = w.out_arena = None
+        w.unit_bytes = C * per
+        w.launches = C
+        w.run = lambda: [c() for c in calls]
+        w.config = workload_config(name)
+        w.dominant = ("%s packer, 14336x4096 fp16 in" % name[-2:], w.run, C, per)
+        w.cpu_sample = None
+        w.keep = (Ws, outs)
+        w.dtype = "f16->" + ("int4" if name == "quant_w4" else "i8")
+    elif name in ("int4_m8", "int4_m16", "int4_a8_m16"):
+        # one int4 matrix at 8 / 16 tokens (verify block), rotating copies > 2x L2
+        M = int(name.split("_m")[1])
+        Wq, sc, x = synth.w4_case(14336, 4096, M, seed=0)
+        per = Wq.numel() + sc.numel() * 2
+        C = -(-2 * L2_BYTES // per)
+        xd = x.to(dev)
+        copies = [(Wq.to(dev), sc.to(dev)) for _ in range(C)]
+        ys = [torch.empty(M, 14336, dtype=torch.float16, device=dev) for _ in range(C)]
+        if name == "int4_a8_m16":
+            xq = torch.empty(M, 4096, dtype=torch.int8, device=dev)
+            xs_ = torch.empty(M, dtype=torch.float32, device=dev)
+            dg.quantize_act_i8(xd, xq, xs_, stream=s)
+            calls = [lambda c=c, y=y: dg.gemv_w4(c[0], c[1], y, x_i8=xq, x_scale=xs_, stream=s)
+                     for c, y in zip(copies, ys)]
+            w.dtype = "int4xi8"
+        else:
+            calls = [lambda c=c, y=y: dg.gemv_w4(c[0], c[1], y, x_f16=xd, stream=s)
+                     for c, y in zip(copies, ys)]
+            w.dtype = "int4xf16"
+        w.host = (Wq, x)
+        w.in_arena = xd.view(torch.uint8).view(-1)
+        w.out_arena = torch.cat([y.view(-1) for y in ys]).view(torch.uint8)
+        w.unit_bytes = C * per
+        w.launches = C
+        w.run = lambda: [c() for c in calls]
+        w.config = workload_config(name)
+        w.dominant = ("int4 14336x4096 verify tile, M=%d" % M, w.run, C, per)
+        w.cpu_sample = ("w4a16", ([synth.Layer([synth.Linear("m", 14336, 4096, Wq, sc, "x")],
+                                               {"x": x})], None, None))
+        w.keep = (copies, ys)
     elif name == "gemv_f16_2048" or name.startswith("w8a8_m") or name.startswith("fp16_m"):
         # one matrix called repeatedly; C rotating copies (> 2x L2 in total) keep
         # every call cold.  A step is one call on each copy.
@@ -324,6 +444,7 @@ def build_workload(name, dev, torch):
         w.in_arena, w.out_arena = ain.buf, aout.buf
         w.unit_bytes = C * per
         w.launches = C
+        w.calls = calls
         w.run = lambda: [c() for c in calls]
         w.config = workload_config(name)
         assert (w.config["bytes_per_call"], w.config["calls_per_step"]) == (per, C)
@@ -350,6 +471,12 @@ def workload_config(name):
                             "decoder, 28 matrices, M=1",
                 "weight_bytes_per_step": 4 * fp16_layer,
                 "l2": "inputs 374 MB > 126 MB L2 (no flush)"}
+    if name == "decode_int4_a16_f16head":
+        nbytes = int4_bytes(32 * int4_layer) + 128256 * 4096 * 2
+        return {"workload": "decode-step weight stream, 32-layer 4096-wide int4 g32 decoder "
+                            "(Llama-3.1-8B shape) + fp16 128256-row lm_head with argmax, W4A16, M=1",
+                "weight_bytes_per_step": nbytes,
+                "l2": "inputs %.2f GB > 126 MB L2 (no flush)" % (nbytes / 1e9)}
     if name.startswith("decode_int4"):
         act = name[-3:]
         small = "_4l_" in name
@@ -375,6 +502,33 @@ def workload_config(name):
                             % name[-3:][1:].upper(),
                 "weight_bytes_per_step": int4_bytes(2 * 28672 * 4096),
                 "l2": "inputs 132 MB > 126 MB L2 (no flush)"}
+    if name in ("block_fp16_fused", "block_fp16_unfused"):
+        return {"workload": "decoder-block step of the 28-layer 1536-wide fp16 decoder: "
+                            "q/k/v, o + residual, gate|up -> SwiGLU, down + residual, M=1, %s"
+                            % ("epilogues fused into one persistent launch" if name.endswith("_fused")
+                               else "epilogues as separate launches"),
+                "weight_bytes_per_step": 28 * fp16_layer,
+                "l2": "inputs 2.62 GB > 126 MB L2 (no flush)"}
+    if name == "conv1d":
+        return {"workload": "causal-conv1d decode step, 24 layers x 8192 channels x 4 taps, "
+                            "SiLU, M=1 (one launch per layer)",
+                "bytes_per_step": 24 * 8192 * (8 + 12 + 6),
+                "l2": "5.0 MB per step: L2-resident (the op is launch-bound)"}
+    if name in ("quant_w4", "quant_w8"):
+        per = 14336 * 4096 * 2
+        C = -(-2 * L2_BYTES // per)
+        return {"workload": "load-time %s packer, 14336x4096 fp16 weights" %
+                            ("int4 g32" if name == "quant_w4" else "int8 per-channel"),
+                "bytes_per_call": per, "calls_per_step": C,
+                "l2": "%d rotating copies, %.0f MB > 2x L2" % (C, C * per / 1e6)}
+    if name in ("int4_m8", "int4_m16", "int4_a8_m16"):
+        per = int4_bytes(14336 * 4096)
+        C = -(-2 * L2_BYTES // per)
+        M = int(name.split("_m")[1])
+        return {"workload": "int4 g32 14336x4096 verify tile, W4%s, M=%d"
+                            % ("A8" if "a8" in name else "A16", M),
+                "bytes_per_call": per, "calls_per_step": C,
+                "l2": "%d rotating weight copies, %.0f MB > 2x L2" % (C, C * per / 1e6)}
     if name == "gemv_f16_2048" or name.startswith("w8a8_m") or name.startswith("fp16_m"):
         if name == "gemv_f16_2048":
             per, desc = 2048 * 2048 * 2, "fp16 GEMV 2048x2048, M=1"
@@ -474,6 +628,22 @@ def oracle_sample(w, budget_s, nthreads=0):
             if time.perf_counter() - t0 > budget_s:
                 break
         desc = "%d whole int4 matrices of the decoder in layer order" % mats
+    elif kind == "conv":
+        C, Wd = data
+        g = __import__("torch").Generator().manual_seed(0)
+        T = __import__("torch")
+        x = (T.randn(1, C, generator=g)).half().numpy()
+        st = (T.randn(1, C, Wd - 1, generator=g)).half().numpy()
+        wt = (T.randn(C, Wd, generator=g) * 0.5).half().numpy()
+        b = (T.randn(C, generator=g) * 0.1).half().numpy()
+        per = C * (2 * Wd + 2 * 2 * (Wd - 1) + 2 + 2 + 2)
+        while True:
+            oracle.causal_conv1d_update(x, st, wt, b)
+            done += per
+            mats += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        desc = "%d causal-conv1d steps of 8192 channels" % mats
     elif kind == "w8":
         import oracle as orc
         W, s_w, x = data
@@ -523,8 +693,14 @@ def main():
                              "decode_int4_4l_a16", "decode_int4_4l_a8", "lm_head",
                              "gateup_fp16", "gateup_w4a16", "gateup_w4a8", "decode_fp16_4l",
                              "gemv_f16_2048", "w8a8_m1",
-                             "w8a8_m4", "w8a8_m16", "fp16_m8", "fp16_m16"])
+                             "w8a8_m4", "w8a8_m16", "fp16_m8", "fp16_m16", "block_fp16_fused",
+                             "block_fp16_unfused", "decode_int4_a16_f16head", "conv1d",
+                             "quant_w4", "quant_w8", "int4_m8", "int4_m16", "int4_a8_m16"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip the per-configuration measurements (the `configs` object)")
+    ap.add_argument("--config-cpu-budget", type=float, default=2.0,
+                    help="seconds of oracle time per configuration's cpu_baseline")
     ap.add_argument("--quick", action="store_true",
                     help="time the step only (no dominant-kernel, e2e, probe or CPU legs); "
                          "for configuration sweeps")
@@ -634,10 +810,96 @@ def main():
                 d1, c1, desc1 = oracle_sample(w, args.cpu_budget / 3, nthreads=1)
                 out["cpu_baseline"]["one_core"] = {"value": round(d1 / c1 / 1e9, 4),
                                                    "sample": desc1 + " (%.1f s)" % c1}
+        if world == 1 and args.configs:
+            out["configs"] = measure_configs(args, torch, dg, dev, peak, local)
         print(json.dumps(out), flush=True)
     if dist:
         dist.destroy_process_group()
     return 0
+
+
+# Every configuration the library is measured on, beside the headline step:
+# (row of the hot-path table it exercises, workload).
+CONFIG_WORKLOADS = [
+    ("config 1", "gemv_f16_2048"), ("config 3", "lm_head"), ("config 4", "w8a8_m1"),
+    ("config 4", "w8a8_m4"), ("config 4", "w8a8_m16"), ("config 5", "decode_int4_a16"),
+    ("config 5", "decode_int4_a8"), ("NEXT-1", "int4_m16"), ("NEXT-1", "int4_a8_m16"),
+    ("NEXT-1", "fp16_m16"), ("NEXT-2", "block_fp16_fused"), ("NEXT-2", "block_fp16_unfused"),
+    ("NEXT-3", "decode_int4_a16_f16head"), ("NEXT-3", "quant_w4"), ("NEXT-4", "conv1d"),
+]
+
+
+def measure_config(name, row, torch, dg, dev, peak, local, cpu_budget):
+    """One configuration: its step replayed from a CUDA graph for about half a
+    second (inputs already resident), with the clocks sampled meanwhile, the
+    per-launch time of its dominant kernel, and the oracle on a bounded sample."""
+    t_build = time.perf_counter()
+    w = build_workload(name, dev, torch)
+    t_build = time.perf_counter() - t_build
+    s = w.stream
+    g = graph_of(w.run, s, torch)
+    for _ in range(3):
+        with torch.cuda.stream(s):
+            g.replay()
+    torch.cuda.synchronize()
+    est = time_graph(g, s, 3, torch) / 3
+    steps = int(max(10, min(3000, 0.5 / max(est, 1e-7))))
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.25)
+    secs = time_graph(g, s, steps, torch)
+    clk = clocks.stop()
+    dname, _, dlaunch, dbytes = w.dominant
+    gbs = w.unit_bytes * steps / secs / 1e9
+    d_launch_s = secs / steps / dlaunch
+    res = {"row": row, "workload": w.config.get("workload", name),
+           "us_per_step": round(secs / steps * 1e6, 3), "steps": steps,
+           "value": round(gbs, 1), "unit": "GB/s", "frac": round(gbs / peak, 4),
+           "launches_per_step": w.launches,
+           "kernel": {"name": dname, "us_per_launch": round(d_launch_s * 1e6, 3),
+                      "bytes_per_launch": dbytes,
+                      "frac": round(dbytes / d_launch_s / 1e9 / peak, 4)},
+           "clocks": clk, "dtype": w.dtype, "build_s": round(t_build, 1)}
+    if getattr(w, "calls", None):
+        # one call per replay, rotating over the copies: the cold single-launch
+        # time (graph launch included) beside the graph-amortised one above
+        gs = [graph_of(c, s, torch) for c in w.calls]
+        n = 40 * len(gs)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for i in range(n):
+                gs[i % len(gs)].replay()
+            e1.record(s)
+        e1.synchronize()
+        res["single_launch_us"] = round(e0.elapsed_time(e1) * 1e3 / n, 3)
+        res["graph_amortised_us_per_call"] = round(d_launch_s * 1e6, 3)
+    if w.cpu_sample and cpu_budget > 0:
+        done, cs, desc = oracle_sample(w, cpu_budget)
+        res["cpu_baseline"] = {"value": round(done / cs / 1e9, 4), "unit": "GB/s",
+                               "cores": os.cpu_count(), "kind": "oracle",
+                               "sample": desc + " (%.1f s)" % cs}
+    del w, g
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_configs(args, torch, dg, dev, peak, local):
+    out = {}
+    t0 = time.perf_counter()
+    for row, name in CONFIG_WORKLOADS:
+        log("config", row, name)
+        try:
+            out[name] = measure_config(name, row, torch, dg, dev, peak, local, args.config_cpu_budget)
+        except Exception as e:  # report, and go on with the others
+            out[name] = {"row": row, "error": repr(e)[:300]}
+    fu, un = out.get("block_fp16_fused"), out.get("block_fp16_unfused")
+    if fu and un and "us_per_step" in fu and "us_per_step" in un:
+        out["epilogue_fusion_saves_us_per_step"] = round(un["us_per_step"] - fu["us_per_step"], 3)
+    out["total_s"] = round(time.perf_counter() - t0, 1)
+    return out
 
 
 def measure_e2e(w, args, torch, dg, g):

@@ -427,6 +427,41 @@ static dg_status launch_fp_mma(GemvParams& p, bool bf16, cudaStream_t s) {
     return to_status(gemv_fp_mma(&p, bf16, p.a.K, need < maxg ? need : maxg, s, nullptr));
 }
 
+// Whether int4 with this many tokens runs on the tensor-core tile: 8..16
+// tokens whose staged activations fit one CTA (K up to about 6900); longer
+// rows stay on the CUDA-core tile.
+static bool use_w4_mma(const dg_linear& op) {
+    if ((op.kind != DG_LINEAR_W4A16 && op.kind != DG_LINEAR_W4A8) || op.M < 8 || op.K % 32 ||
+        tune().MMA == 0 || op.epilogue)
+        return false;
+    return gemv_w4_mma_smem(op.K) <= smem_optin_limit();
+}
+
+static dg_status launch_w4_mma(GemvParams& p, bool a8, cudaStream_t s) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int occ = 0;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = cache.find({dev, p.a.K, (int)a8});
+        if (it != cache.end()) occ = it->second;
+    }
+    if (!occ) {
+        if (gemv_w4_mma(nullptr, a8, p.a.K, 0, nullptr, &occ) != cudaSuccess || occ < 1) occ = 1;
+        std::lock_guard<std::mutex> g(mu);
+        cache[{dev, p.a.K, (int)a8}] = occ;
+    }
+    p.ksplit = fp_mma_ks(p.a.K);  // the same rule on K alone: 32-wide blocks per warp
+    const int tiles = (p.t.N + 15) / 16;
+    const int per_cta = kW4MmaWarps / p.ksplit;
+    const int need = (tiles + per_cta - 1) / per_cta;
+    int maxg = sm_count() * occ;
+    if (maxg < 1) maxg = 1;
+    return to_status(gemv_w4_mma(&p, a8, p.a.K, need < maxg ? need : maxg, s, nullptr));
+}
+
 // Launches ops[0..n) (same kind, same activations) as one kernel (two with
 // split-K, when ws holds the partials).
 static dg_status launch_group(const dg_linear* ops, int n, cudaStream_t s, void* ws = nullptr,
@@ -462,6 +497,7 @@ static dg_status launch_group(const dg_linear* ops, int n, cudaStream_t s, void*
     if (ops[0].epilogue == DG_EPI_RESIDUAL) p.t.res = ops[0].residual;
     if (use_i8_mma(ops[0])) return launch_i8_mma(p, s);
     if (use_fp_mma(ops[0])) return launch_fp_mma(p, ops[0].kind == DG_LINEAR_BF16, s);
+    if (use_w4_mma(ops[0])) return launch_w4_mma(p, ops[0].kind == DG_LINEAR_W4A8, s);
     GemvLaunch L{fmt_of(ops[0].kind), pick_mt(ops[0].M), 0, false, ops[0].K, p.group, 0};
     L.R = pick_r(L.fmt, L.MT, L.K);
     if (pair && (L.R & 1)) L.R = 2;  // a row group holds whole pairs
@@ -526,12 +562,12 @@ static bool same_group(const dg_linear& a, const dg_linear& b) {
 static bool step_eligible(const dg_linear& op) { return op.M == 1 && !op.acc_out; }
 
 // CTAs of the step kernel per SM.
-static int step_occupancy(Fmt f, int max_k, size_t smem, int nw) {
+static int step_occupancy(Fmt f, int max_k, size_t smem, int nw, bool epi) {
     static std::mutex mu;
-    static std::map<std::tuple<int, int, int, size_t, int>, int> cache;
+    static std::map<std::tuple<int, int, int, size_t, int, int>, int> cache;
     int dev = 0;
     cudaGetDevice(&dev);
-    const auto key = std::make_tuple(dev, (int)f, max_k, smem, nw);
+    const auto key = std::make_tuple(dev, (int)f, max_k, smem, nw, (int)epi);
     {
         std::lock_guard<std::mutex> g(mu);
         auto it = cache.find(key);
@@ -539,7 +575,7 @@ static int step_occupancy(Fmt f, int max_k, size_t smem, int nw) {
     }
     StepParams* none = nullptr;
     int occ = 0;
-    const cudaError_t e = step_launch(f, none, 0, smem, nullptr, &occ, nw);
+    const cudaError_t e = step_launch(f, none, 0, smem, nullptr, &occ, nw, epi);
     if (e != cudaSuccess) occ = 0;
     std::lock_guard<std::mutex> g(mu);
     cache[key] = occ;
@@ -769,22 +805,23 @@ static dg_status launch_step_run(const dg_linear* ops, int n, void* ws, cudaStre
         // sub-partition: 883 -> 863 us for the 32-layer step) when no phase
         // splits K, since the split barriers' id ranges are disjoint only up
         // to 16 warps
-        bool split = false, pairs = false;
+        bool split = false, pairs = false, epi = false;
         for (int q = 0; q < sp.nphase; ++q) {
             split = split || sp.ph[q].ks > 1;
             pairs = pairs || sp.ph[q].pair;
+            epi = epi || sp.ph[q].pair || sp.ph[q].res;
         }
         // (SwiGLU pair phases need an even number of rows per slot: the
         // formats' defaults give that; a tuned warp count might not)
         const int nw = split ? 16
                              : (tune().SNW > 0 && !pairs) ? tune().SNW
                                                           : f == F_W4A8 ? 20 : 16;
-        const int occ = step_occupancy(f, max_k, smem, nw);
+        const int occ = step_occupancy(f, max_k, smem, nw, epi);
         if (occ < 1) return DG_ERR_UNSUPPORTED;
         const int grid = sm_count() * occ;
         if (grid > kMaxArgCtas) return DG_ERR_UNSUPPORTED;
         if (cudaMemsetAsync(ws, 0, 2 * sizeof(unsigned), s) != cudaSuccess) return DG_ERR_CUDA;
-        const cudaError_t e = step_launch(f, &sp, grid, smem, s, nullptr, nw);
+        const cudaError_t e = step_launch(f, &sp, grid, smem, s, nullptr, nw, epi);
         if (e != cudaSuccess) return DG_ERR_CUDA;
     }
     return DG_OK;

@@ -307,6 +307,11 @@ size_t gemv_smem(Fmt f, int MT, int K, int group);
 // W8A8 for 8..16 tokens on the tensor cores (mma.sync s8, exact int32).
 cudaError_t gemv_i8_mma(const GemvParams* p, int K, int grid, cudaStream_t s, int* occ, bool f16);
 size_t gemv_i8_mma_smem(int K);
+// Groupwise int4 for 8..16 tokens on the tensor cores (gemv_w4_mma.cu), CTAs
+// of kW4MmaWarps warps.
+constexpr int kW4MmaWarps = 16;
+cudaError_t gemv_w4_mma(const GemvParams* p, bool a8, int K, int grid, cudaStream_t s, int* occ);
+size_t gemv_w4_mma_smem(int K);
 // fp16 / bf16 for 8..16 tokens on the tensor cores (gemv_fp_mma.cu).
 cudaError_t gemv_fp_mma(const GemvParams* p, bool bf16, int K, int grid, cudaStream_t s, int* occ);
 size_t gemv_fp_mma_smem(int K);
@@ -319,9 +324,10 @@ int head_grid(const dg_linear& op);
 
 // Persistent decode-step kernel (step_kernel.cu): one cooperative launch over
 // sp.nphase phases of format f, with nw warps per CTA (16, or 0 for the
-// format's default).  occ != nullptr: report CTAs per SM instead.
+// format's default); epi: some phase carries an epilogue (residual, SwiGLU).
+// occ != nullptr: report CTAs per SM instead.
 cudaError_t step_launch(Fmt f, const StepParams* sp, int grid, size_t smem, cudaStream_t s,
-                        int* occ, int nw);
+                        int* occ, int nw, bool epi);
 size_t step_smem(Fmt f, int max_k);
 cudaError_t launch_wait_selftest(unsigned limit, int* err, cudaStream_t s);
 

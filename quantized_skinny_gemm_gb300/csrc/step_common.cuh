@@ -8,11 +8,12 @@ namespace dg {
 
 // Row r (global over the phase's segments) of phase ph; a SwiGLU phase
 // (ph.pair) interleaves its gate and up rows: row 2i is gate row i, 2i + 1 up
-// row i.
+// row i (PAIRS = false: the launch has no such phase).
+template <bool PAIRS = true>
 __device__ __forceinline__ RowRef locate_step(const StepPhase& ph, int r, size_t rb) {
     RowRef rr{};
     int s = 0;
-    if (ph.pair) {
+    if (PAIRS && ph.pair) {
         s = r & 1;
         rr.local = r >> 1;
     } else {

@@ -191,7 +191,9 @@ __host__ __device__ size_t step_smem_for(int max_k) {
            (P::kDirectX ? 0 : (size_t)max_k + 16);
 }
 
-template <class P, int NW>
+// EPI: the launch has epilogue phases (residual adds, SwiGLU pairs); the
+// variant without them carries none of that code.
+template <class P, int NW, bool EPI>
 __global__ void __launch_bounds__(NW * 32, 1)
     k_step(const __grid_constant__ StepParams sp, int max_k) {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -319,12 +321,12 @@ __global__ void __launch_bounds__(NW * 32, 1)
             RowRef rows[R];
             {
                 const int first = r0 + rg * R;
-                const RowRef f = active ? locate_step(ph, first, g.rb) : RowRef{};
+                const RowRef f = active ? locate_step<EPI>(ph, first, g.rb) : RowRef{};
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     const int gr = first + r;
                     if (active && gr < r1) {
-                        rows[r] = locate_step(ph, gr, g.rb);
+                        rows[r] = locate_step<EPI>(ph, gr, g.rb);
                     } else {
                         rows[r] = f;
                         rows[r].valid = false;
@@ -347,10 +349,14 @@ __global__ void __launch_bounds__(NW * 32, 1)
                                 best_i = rows[r].global;
                             }
                         }
-                    } else if (lane == r && !(ph.pair && (r & 1))) {
-                        const int ru = r + 1 < R ? r + 1 : r;  // (pairs: R is even)
-                        store_row<P>(rows[r], 0, acc[r][0], sx, ph.res, ph.pair != 0, rows[ru],
-                                     acc[ru][0]);
+                    } else if constexpr (EPI) {
+                        if (lane == r && !(ph.pair && (r & 1))) {
+                            const int ru = r + 1 < R ? r + 1 : r;  // (pairs: R is even)
+                            store_row<P>(rows[r], 0, acc[r][0], sx, ph.res, ph.pair != 0,
+                                         rows[ru], acc[ru][0]);
+                        }
+                    } else if (lane == r) {
+                        P::store(rows[r], 0, acc[r][0], sx);
                     }
                 }
             }
@@ -386,10 +392,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
 }
 
 
-template <class P, int NW>
+template <class P, int NW, bool EPI>
 cudaError_t step_run_nw(const StepParams* sp, int grid, size_t smem, cudaStream_t s, int* occ,
                         int max_k) {
-    auto fn = k_step<P, NW>;
+    auto fn = k_step<P, NW, EPI>;
     constexpr int threads = NW * 32;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -411,14 +417,21 @@ cudaError_t step_run_nw(const StepParams* sp, int grid, size_t smem, cudaStream_
     return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(fn), args);
 }
 
+template <class P, int NW>
+cudaError_t step_run_epi(const StepParams* sp, int grid, size_t smem, cudaStream_t s, int* occ,
+                         int max_k, bool epi) {
+    return epi ? step_run_nw<P, NW, true>(sp, grid, smem, s, occ, max_k)
+               : step_run_nw<P, NW, false>(sp, grid, smem, s, occ, max_k);
+}
+
 template <class P>
 cudaError_t step_run(const StepParams* sp, int grid, size_t smem, cudaStream_t s, int* occ,
-                     int max_k, int nw) {
+                     int max_k, int nw, bool epi) {
     // W4A8 may run 20 warps (the host picks it only when no phase splits K:
     // the split barriers' id ranges are disjoint up to 16 warps)
     if constexpr (std::is_same<P, PolicyW4A8>::value)
-        if (nw == 20) return step_run_nw<P, 20>(sp, grid, smem, s, occ, max_k);
-    return step_run_nw<P, StepCfg<P>::kWarps>(sp, grid, smem, s, occ, max_k);
+        if (nw == 20) return step_run_epi<P, 20>(sp, grid, smem, s, occ, max_k, epi);
+    return step_run_epi<P, StepCfg<P>::kWarps>(sp, grid, smem, s, occ, max_k, epi);
 }
 
 size_t step_smem(Fmt f, int max_k) {
@@ -433,17 +446,17 @@ size_t step_smem(Fmt f, int max_k) {
 }
 
 cudaError_t step_launch(Fmt f, const StepParams* sp, int grid, size_t smem, cudaStream_t s,
-                        int* occ, int nw) {
+                        int* occ, int nw, bool epi) {
     int max_k = 0;
     if (sp)
         for (int p = 0; p < sp->nphase; ++p)
             if (sp->ph[p].K > max_k) max_k = sp->ph[p].K;
     switch (f) {
-        case F_F16: return step_run<PolicyFP<false>>(sp, grid, smem, s, occ, max_k, nw);
-        case F_BF16: return step_run<PolicyFP<true>>(sp, grid, smem, s, occ, max_k, nw);
-        case F_I8: return step_run<PolicyI8>(sp, grid, smem, s, occ, max_k, nw);
-        case F_W4A16: return step_run<PolicyW4A16>(sp, grid, smem, s, occ, max_k, nw);
-        case F_W4A8: return step_run<PolicyW4A8>(sp, grid, smem, s, occ, max_k, nw);
+        case F_F16: return step_run<PolicyFP<false>>(sp, grid, smem, s, occ, max_k, nw, epi);
+        case F_BF16: return step_run<PolicyFP<true>>(sp, grid, smem, s, occ, max_k, nw, epi);
+        case F_I8: return step_run<PolicyI8>(sp, grid, smem, s, occ, max_k, nw, epi);
+        case F_W4A16: return step_run<PolicyW4A16>(sp, grid, smem, s, occ, max_k, nw, epi);
+        case F_W4A8: return step_run<PolicyW4A8>(sp, grid, smem, s, occ, max_k, nw, epi);
     }
     return cudaErrorInvalidValue;
 }
