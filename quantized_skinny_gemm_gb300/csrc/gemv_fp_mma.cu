@@ -4,7 +4,9 @@
 // operands as they are and accumulates in fp32.
 //
 // One warp owns a tile of 16 weight rows and all 16 (zero-padded) tokens:
-// D[16 rows][16 tokens] = W[16][K] x[16][K]^T as two n8 halves.  Thread
+// D[16 rows][16 tokens] = W[16][K] x[16][K]^T as two n8 halves; the tokens'
+// values are read from global memory through L1 (no staging, so two CTAs fit
+// an SM and K is unbounded).  Thread
 // (g = lane/4, t = lane%4) loads 16 bytes (8 values) of rows g and g+8 at
 // k0 + 8t of each 32-wide k block; k16 step s (s = 0, 1) takes values
 // 8t + 4s .. 8t + 4s + 3: logical k 2t, 2t+1 <- +0, +1 and 2t+8, 2t+9 <- +2,
@@ -54,20 +56,10 @@ __global__ void __launch_bounds__(kThreads) k_fp_mma(const __grid_constant__ Gem
     griddep_launch_dependents();
     griddep_wait();
 
-    // activations: 16 tokens x K values (tokens >= M zero), rows padded by 64
-    // bytes so the 8 quads of a warp read from different banks
-    const size_t xstride = (size_t)K * 2 + 64;
-    {
-        const int per_row = K / 8;
-        const uint4* src = static_cast<const uint4*>(p.a.x);
-        for (int i = threadIdx.x; i < 16 * per_row; i += blockDim.x) {
-            const int m = i / per_row, c = i - m * per_row;
-            *reinterpret_cast<uint4*>(smem + (size_t)m * xstride + 16 * c) =
-                m < M ? src[i] : make_uint4(0, 0, 0, 0);
-        }
-    }
-    float* part = reinterpret_cast<float*>(smem + 16 * xstride);  // [warp][8][32]
-    __syncthreads();
+    // activations are read from global memory through L1 (every warp of an
+    // SM reads the same 16 x K values); tokens >= M read as zeros
+    float* part = reinterpret_cast<float*>(smem);  // [warp][8][32]
+    const unsigned char* xg = static_cast<const unsigned char*>(p.a.x);
 
     const int n_tiles = (p.t.N + 15) / 16;
     const int nblk = K / 32 / ks;  // 32-wide k blocks per warp
@@ -83,23 +75,25 @@ __global__ void __launch_bounds__(kThreads) k_fp_mma(const __grid_constant__ Gem
         const size_t k0 = ((size_t)kw * nblk * 32 + 8 * t) * 2;  // bytes
         const unsigned char* wlo = (rlo.valid ? rlo.w : first.w) + k0;
         const unsigned char* whi = (rhi.valid ? rhi.w : first.w) + k0;
-        const unsigned char* xlo = smem + (size_t)g * xstride + k0;
-        const unsigned char* xhi = smem + (size_t)(g + 8) * xstride + k0;
+        const unsigned char* xlo = xg + (size_t)g * K * 2 + k0;        // token g
+        const unsigned char* xhi = xg + (size_t)(g + 8) * K * 2 + k0;  // token g + 8
+        const bool has_lo = g < M, has_hi = g + 8 < M;
         float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};  // tokens 0..7, 8..15
 
         for (int kb = 0; active && kb < nblk; kb += kFpMmaUnroll) {
-            uint4 alo[kFpMmaUnroll], ahi[kFpMmaUnroll];
+            uint4 alo[kFpMmaUnroll], ahi[kFpMmaUnroll], blv[kFpMmaUnroll], bhv[kFpMmaUnroll];
 #pragma unroll
             for (int u = 0; u < kFpMmaUnroll; ++u)
                 if (kb + u < nblk) {
                     alo[u] = ld_stream16(wlo + (size_t)(kb + u) * 64);
                     ahi[u] = ld_stream16(whi + (size_t)(kb + u) * 64);
+                    blv[u] = has_lo ? ld_nc16(xlo + (size_t)(kb + u) * 64) : make_uint4(0, 0, 0, 0);
+                    bhv[u] = has_hi ? ld_nc16(xhi + (size_t)(kb + u) * 64) : make_uint4(0, 0, 0, 0);
                 }
 #pragma unroll
             for (int u = 0; u < kFpMmaUnroll; ++u)
                 if (kb + u < nblk) {
-                    const uint4 bl = *reinterpret_cast<const uint4*>(xlo + (size_t)(kb + u) * 64);
-                    const uint4 bh = *reinterpret_cast<const uint4*>(xhi + (size_t)(kb + u) * 64);
+                    const uint4 bl = blv[u], bh = bhv[u];
                     // step 0: values +0..+3 (words x, y); step 1: +4..+7 (z, w)
                     mma_16816<BF16>(d0, alo[u].x, ahi[u].x, alo[u].y, ahi[u].y, bl.x, bl.y);
                     mma_16816<BF16>(d1, alo[u].x, ahi[u].x, alo[u].y, ahi[u].y, bh.x, bh.y);
@@ -143,7 +137,7 @@ __global__ void __launch_bounds__(kThreads) k_fp_mma(const __grid_constant__ Gem
     }
 }
 
-size_t gemv_fp_mma_smem(int K) { return (size_t)16 * ((size_t)K * 2 + 64) + (size_t)kWarps * 8 * 32 * 4; }
+size_t gemv_fp_mma_smem(int) { return (size_t)kWarps * 8 * 32 * 4; }
 
 cudaError_t gemv_fp_mma(const GemvParams* p, bool bf16, int K, int grid, cudaStream_t s, int* occ) {
     const size_t smem = gemv_fp_mma_smem(K);

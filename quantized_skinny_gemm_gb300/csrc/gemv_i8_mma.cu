@@ -47,20 +47,10 @@ __global__ void __launch_bounds__(kThreads) k_w8a8_mma(const __grid_constant__ G
     griddep_launch_dependents();
     griddep_wait();
 
-    // activations: 16 tokens x K int8 (tokens >= M zero), rows padded by 64
-    // bytes so the 8 quads of a warp read from different banks
-    const int xstride = K + 64;
-    {
-        const int per_row = K / 16;
-        const uint4* src = reinterpret_cast<const uint4*>(p.a.xq);
-        for (int i = threadIdx.x; i < 16 * per_row; i += blockDim.x) {
-            const int m = i / per_row, c = i - m * per_row;
-            *reinterpret_cast<uint4*>(smem + (size_t)m * xstride + 16 * c) =
-                m < M ? src[i] : make_uint4(0, 0, 0, 0);
-        }
-    }
-    int* part = reinterpret_cast<int*>(smem + (size_t)16 * xstride);  // [warp][8][32]
-    __syncthreads();
+    // activations are read from global memory through L1 (every warp of an
+    // SM reads the same 16 x K codes); tokens >= M read as zeros
+    int* part = reinterpret_cast<int*>(smem);  // [warp][8][32]
+    const unsigned char* xg = reinterpret_cast<const unsigned char*>(p.a.xq);
 
     const int n_tiles = (p.t.N + 15) / 16;
     const int nblk = K / 64 / ks;  // 64-wide k blocks per warp
@@ -76,23 +66,25 @@ __global__ void __launch_bounds__(kThreads) k_w8a8_mma(const __grid_constant__ G
         const size_t k0 = (size_t)kw * nblk * 64 + 16 * t;
         const unsigned char* wlo = (rlo.valid ? rlo.w : first.w) + k0;
         const unsigned char* whi = (rhi.valid ? rhi.w : first.w) + k0;
-        const unsigned char* xlo = smem + (size_t)g * xstride + k0;        // token g
-        const unsigned char* xhi = smem + (size_t)(g + 8) * xstride + k0;  // token g + 8
+        const unsigned char* xlo = xg + (size_t)g * K + k0;        // token g
+        const unsigned char* xhi = xg + (size_t)(g + 8) * K + k0;  // token g + 8
+        const bool has_lo = g < M, has_hi = g + 8 < M;
         int d0[4] = {0, 0, 0, 0}, d1[4] = {0, 0, 0, 0};  // tokens 0..7, 8..15
 
         for (int kb = 0; active && kb < nblk; kb += kMmaUnroll) {
-            uint4 alo[kMmaUnroll], ahi[kMmaUnroll];
+            uint4 alo[kMmaUnroll], ahi[kMmaUnroll], blv[kMmaUnroll], bhv[kMmaUnroll];
 #pragma unroll
             for (int u = 0; u < kMmaUnroll; ++u)
                 if (kb + u < nblk) {
                     alo[u] = ld_stream16(wlo + (size_t)(kb + u) * 64);
                     ahi[u] = ld_stream16(whi + (size_t)(kb + u) * 64);
+                    blv[u] = has_lo ? ld_nc16(xlo + (size_t)(kb + u) * 64) : make_uint4(0, 0, 0, 0);
+                    bhv[u] = has_hi ? ld_nc16(xhi + (size_t)(kb + u) * 64) : make_uint4(0, 0, 0, 0);
                 }
 #pragma unroll
             for (int u = 0; u < kMmaUnroll; ++u)
                 if (kb + u < nblk) {
-                    const uint4 bl = *reinterpret_cast<const uint4*>(xlo + (size_t)(kb + u) * 64);
-                    const uint4 bh = *reinterpret_cast<const uint4*>(xhi + (size_t)(kb + u) * 64);
+                    const uint4 bl = blv[u], bh = bhv[u];
                     mma_s8_16816_32(d0, alo[u].x, ahi[u].x, alo[u].y, ahi[u].y, bl.x, bl.y);
                     mma_s8_16816_32(d1, alo[u].x, ahi[u].x, alo[u].y, ahi[u].y, bh.x, bh.y);
                     mma_s8_16816_32(d0, alo[u].z, ahi[u].z, alo[u].w, ahi[u].w, bl.z, bl.w);
@@ -177,18 +169,10 @@ __global__ void __launch_bounds__(kThreads) k_w8a8_mma_f16(const __grid_constant
     griddep_launch_dependents();
     griddep_wait();
 
-    const int xstride = K + 64;
-    {
-        const int per_row = K / 16;
-        const uint4* src = reinterpret_cast<const uint4*>(p.a.xq);
-        for (int i = threadIdx.x; i < 16 * per_row; i += blockDim.x) {
-            const int m = i / per_row, c = i - m * per_row;
-            *reinterpret_cast<uint4*>(smem + (size_t)m * xstride + 16 * c) =
-                m < M ? src[i] : make_uint4(0, 0, 0, 0);
-        }
-    }
-    int* part = reinterpret_cast<int*>(smem + (size_t)16 * xstride);  // [warp][8][32]
-    __syncthreads();
+    // activations are read from global memory through L1 (every warp of an
+    // SM reads the same 16 x K codes); tokens >= M read as zeros
+    int* part = reinterpret_cast<int*>(smem);  // [warp][8][32]
+    const unsigned char* xg = reinterpret_cast<const unsigned char*>(p.a.xq);
 
     const int n_tiles = (p.t.N + 15) / 16;
     const int nblk = K / 64 / ks;
@@ -204,26 +188,28 @@ __global__ void __launch_bounds__(kThreads) k_w8a8_mma_f16(const __grid_constant
         const size_t k0 = (size_t)kw * nblk * 64 + 16 * t;
         const unsigned char* wlo = (rlo.valid ? rlo.w : first.w) + k0;
         const unsigned char* whi = (rhi.valid ? rhi.w : first.w) + k0;
-        const unsigned char* xlo = smem + (size_t)g * xstride + k0;
-        const unsigned char* xhi = smem + (size_t)(g + 8) * xstride + k0;
+        const unsigned char* xlo = xg + (size_t)g * K + k0;
+        const unsigned char* xhi = xg + (size_t)(g + 8) * K + k0;
+        const bool has_lo = g < M, has_hi = g + 8 < M;
         int i0[4] = {0, 0, 0, 0}, i1[4] = {0, 0, 0, 0};  // tokens 0..7, 8..15
 
         for (int kb0 = 0; active && kb0 < nblk; kb0 += kF16FlushBlocks) {
             float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
             const int kb1 = min(nblk, kb0 + kF16FlushBlocks);
             for (int kb = kb0; kb < kb1; kb += kMmaUnroll) {
-                uint4 alo[kMmaUnroll], ahi[kMmaUnroll];
+                uint4 alo[kMmaUnroll], ahi[kMmaUnroll], blv[kMmaUnroll], bhv[kMmaUnroll];
 #pragma unroll
                 for (int u = 0; u < kMmaUnroll; ++u)
                     if (kb + u < kb1) {
                         alo[u] = ld_stream16(wlo + (size_t)(kb + u) * 64);
                         ahi[u] = ld_stream16(whi + (size_t)(kb + u) * 64);
+                        blv[u] = has_lo ? ld_nc16(xlo + (size_t)(kb + u) * 64) : make_uint4(0, 0, 0, 0);
+                        bhv[u] = has_hi ? ld_nc16(xhi + (size_t)(kb + u) * 64) : make_uint4(0, 0, 0, 0);
                     }
 #pragma unroll
                 for (int u = 0; u < kMmaUnroll; ++u)
                     if (kb + u < kb1) {
-                        const uint4 bl = *reinterpret_cast<const uint4*>(xlo + (size_t)(kb + u) * 64);
-                        const uint4 bh = *reinterpret_cast<const uint4*>(xhi + (size_t)(kb + u) * 64);
+                        const uint4 bl = blv[u], bh = bhv[u];
                         const uint32_t wl[4] = {alo[u].x, alo[u].y, alo[u].z, alo[u].w};
                         const uint32_t wh[4] = {ahi[u].x, ahi[u].y, ahi[u].z, ahi[u].w};
                         const uint32_t xl[4] = {bl.x, bl.y, bl.z, bl.w};
@@ -283,7 +269,7 @@ __global__ void __launch_bounds__(kThreads) k_w8a8_mma_f16(const __grid_constant
     }
 }
 
-size_t gemv_i8_mma_smem(int K) { return (size_t)16 * (K + 64) + (size_t)kWarps * 8 * 32 * 4; }
+size_t gemv_i8_mma_smem(int) { return (size_t)kWarps * 8 * 32 * 4; }
 
 // f16: the fp16 tensor path (exact as above); else the int8 one.
 cudaError_t gemv_i8_mma(const GemvParams* p, int K, int grid, cudaStream_t s, int* occ, bool f16) {

@@ -118,21 +118,42 @@ __global__ void __launch_bounds__(kW4MmaWarps * 32) k_w4_mma(const __grid_consta
         const uint16_t* shi = static_cast<const uint16_t*>(ahi_row.scale) + (size_t)ahi_row.local * gk;
         const unsigned char* xlo = smem + (size_t)g * xstride + ((size_t)kb0 * 4 + t) * 16;
         const unsigned char* xhi = smem + (size_t)(g + 8) * xstride + ((size_t)kb0 * 4 + t) * 16;
+        // one scale per block (groups of 32) and 16-byte aligned runs of eight:
+        // scales arrive as one vector per row and batch
+        const bool vec_scales = cpg == 1 && (gk % 8) == 0 && (kb0 % 8) == 0 &&
+                                ((reinterpret_cast<uintptr_t>(alo_row.scale) |
+                                  reinterpret_cast<uintptr_t>(ahi_row.scale)) & 15) == 0;
         // y[row g / g+8][token 2t, 2t+1, 8+2t, 9+2t]
         float ylo[4] = {0.f, 0.f, 0.f, 0.f}, yhi[4] = {0.f, 0.f, 0.f, 0.f};
 
         for (int kb = 0; active && kb < nblk; kb += kW4MmaUnroll) {
             uint32_t wl[kW4MmaUnroll], wh[kW4MmaUnroll];
-            float sl[kW4MmaUnroll], sh[kW4MmaUnroll];
+            uint16_t sl16[kW4MmaUnroll], sh16[kW4MmaUnroll];
 #pragma unroll
             for (int u = 0; u < kW4MmaUnroll; ++u)
                 if (kb + u < nblk) {
                     wl[u] = ld_word(wlo + (size_t)(kb + u) * 16);
                     wh[u] = ld_word(whi + (size_t)(kb + u) * 16);
-                    const int sg = group_of_chunk(kb0 + kb + u, cpg, cps);
-                    sl[u] = __half2float(__ushort_as_half(ld_stream_u16(slo + sg)));
-                    sh[u] = __half2float(__ushort_as_half(ld_stream_u16(shi + sg)));
                 }
+            if (vec_scales && kb + kW4MmaUnroll <= nblk) {
+                // one scale per block, eight consecutive ones: one 16-byte load per row
+                const uint4 a = *reinterpret_cast<const uint4*>(slo + kb0 + kb);
+                const uint4 b = *reinterpret_cast<const uint4*>(shi + kb0 + kb);
+                const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                for (int u = 0; u < kW4MmaUnroll; ++u) {
+                    sl16[u] = (u & 1) ? hi16(aw[u >> 1]) : lo16(aw[u >> 1]);
+                    sh16[u] = (u & 1) ? hi16(bw[u >> 1]) : lo16(bw[u >> 1]);
+                }
+            } else {
+#pragma unroll
+                for (int u = 0; u < kW4MmaUnroll; ++u)
+                    if (kb + u < nblk) {
+                        const int sg = group_of_chunk(kb0 + kb + u, cpg, cps);
+                        sl16[u] = ld_stream_u16(slo + sg);
+                        sh16[u] = ld_stream_u16(shi + sg);
+                    }
+            }
 #pragma unroll
             for (int u = 0; u < kW4MmaUnroll; ++u)
                 if (kb + u < nblk) {
@@ -146,14 +167,16 @@ __global__ void __launch_bounds__(kW4MmaWarps * 32) k_w4_mma(const __grid_consta
                     mma_f16_zero(d1, ql[0], qh[0], ql[1], qh[1], bh.x, bh.y);
                     mma_f16_acc(d0, ql[2], qh[2], ql[3], qh[3], bl.z, bl.w);
                     mma_f16_acc(d1, ql[2], qh[2], ql[3], qh[3], bh.z, bh.w);
-                    ylo[0] = fmaf(d0[0], sl[u], ylo[0]);
-                    ylo[1] = fmaf(d0[1], sl[u], ylo[1]);
-                    ylo[2] = fmaf(d1[0], sl[u], ylo[2]);
-                    ylo[3] = fmaf(d1[1], sl[u], ylo[3]);
-                    yhi[0] = fmaf(d0[2], sh[u], yhi[0]);
-                    yhi[1] = fmaf(d0[3], sh[u], yhi[1]);
-                    yhi[2] = fmaf(d1[2], sh[u], yhi[2]);
-                    yhi[3] = fmaf(d1[3], sh[u], yhi[3]);
+                    const float sl = __half2float(__ushort_as_half(sl16[u]));
+                    const float sh = __half2float(__ushort_as_half(sh16[u]));
+                    ylo[0] = fmaf(d0[0], sl, ylo[0]);
+                    ylo[1] = fmaf(d0[1], sl, ylo[1]);
+                    ylo[2] = fmaf(d1[0], sl, ylo[2]);
+                    ylo[3] = fmaf(d1[1], sl, ylo[3]);
+                    yhi[0] = fmaf(d0[2], sh, yhi[0]);
+                    yhi[1] = fmaf(d0[3], sh, yhi[1]);
+                    yhi[2] = fmaf(d1[2], sh, yhi[2]);
+                    yhi[3] = fmaf(d1[3], sh, yhi[3]);
                 }
         }
         if (ks > 1) {  // slices 1..ks-1 hand their sums to slice 0 of the slot
