@@ -1024,7 +1024,10 @@ def run_reference(args, world):
            "ms_per_step": round(secs / min(args.steps, 50) * 1e3, 3), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": dict(main_cfg, parallelism="single GPU box, host cores",
-                          sample="about 1 s of whole-matrix oracle calls per step (" + cfg + ")"),
+                          sample=("each step: about 1 s of whole-matrix oracle calls over the "
+                                  "same sample (%s): %s; the sample's weights are re-read every "
+                                  "step, so the host caches may hold part of them, unlike the "
+                                  "GPU arm's full workload" % (cfg, desc))),
            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": os.cpu_count(),
                             "kind": "oracle", "sample": desc},
            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
