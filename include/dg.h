@@ -38,18 +38,26 @@
  *    than half the SMs) that is given workspace splits K across CTAs (split-K:
  *    S fixed K ranges, partial sums in ws, a second kernel adding them in range
  *    order); its order then also depends on N, M and the SM count, and is still
- *    the same on every call.  Integer (W8A8) sums are exact either way.  fp16 /
- *    bf16 calls with 8 <= M <= 16 run on the tensor cores (fp32 accumulate, K
- *    split by a rule on K alone): their order differs from the M < 8 path's
- *    and, within that path, still depends only on K.
+ *    the same on every call.  Integer (W8A8) sums are exact either way.  The
+ *    second exception: fp16 / bf16 calls with 8 <= M <= 16 and no epilogue run
+ *    on the tcgen05 tensor cores with the work split stream-K over all SMs (the
+ *    launch's 128-row x 64-k weight blocks cut into one equal range per SM; a
+ *    row tile cut between CTAs is summed in fp32 piece by piece in CTA order),
+ *    so their order depends on K, on the rows of the whole launch and on the
+ *    SM count, and is still the same on every call.  Such a call keeps a small
+ *    fixup scratch per (device, stream) (about 4.3 MB, allocated on the
+ *    stream's first such call); a stream first used inside graph capture runs
+ *    the mma.sync tile instead (K split by a rule on K alone).
  *  - Alignment.  W, x, xq and y must be 16-byte aligned; K must be a multiple
  *    of 8 (fp16/bf16), 16 (int8) or 32 (int4).
  *  - Tuning.  The environment variable DG_TUNE (comma-separated KEY=value,
  *    read once per process) overrides launch choices for configuration
  *    sweeps; unset, the defaults above hold.  Every setting stays within the
- *    parity bound; KS (warps per row), KP (split-K ranges) and MMA
- *    (tensor-core tiles off / int8 tile) change a row's summation order, the
- *    others only the schedule.
+ *    parity bound; KS (warps per row), KP (split-K ranges), MMA (tensor-core
+ *    tiles off / int8 tile), TC (fewest tokens on the tcgen05 tile, 0 = off)
+ *    and TG (its CTA count) change a row's summation order, the others (TS:
+ *    its ring stages 6 / 8 / 12; TP: weight boxes it prefetches to L2 before
+ *    the dependency wait) only the schedule.
  */
 #ifndef DG_H_
 #define DG_H_

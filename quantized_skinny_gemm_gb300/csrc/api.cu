@@ -66,7 +66,7 @@ int* device_error_word() {
 }
 
 // ---- tuning knobs ------------------------------------------------------------------
-// DG_TUNE="R=2,KS=1,CPS=4,PF=32768,PDL=1,STEP=1,SPIN=20000000,SNW=16,MMA=1"
+// DG_TUNE="R=2,KS=1,CPS=4,PF=32768,PDL=1,STEP=1,SPIN=20000000,SNW=16,MMA=1,TC=8"
 // overrides the launch heuristic (for configuration sweeps); an unset key
 // keeps the heuristic's choice.  STEP=0 runs decode steps as one launch per
 // fused group instead of the persistent step kernel; STEP=2 puts a grid
@@ -74,6 +74,10 @@ int* device_error_word() {
 struct Tune {
     int R = 0, KS = 0, CPS = 0, PF = -1, PDL = -1, STEP = -1, SPIN = -1, SNW = 0, MMA = -1;
     int KP = 0;                                // split-K ranges of a per-op launch (1 = off)
+    int TC = -1;                               // fewest tokens on the tcgen05 tile (0 = off)
+    int TG = 0;                                // CTAs of the tcgen05 tile (0 = one per SM)
+    int TS = 0;                                // TMA ring stages of the tcgen05 tile (6, 8, 12)
+    int TP = -1;                               // weight boxes the tcgen05 tile prefetches early
 };
 
 static Tune read_tune() {
@@ -95,6 +99,10 @@ static Tune read_tune() {
         else if (std::sscanf(tok, "SNW=%d", &v) == 1) t.SNW = v;
         else if (std::sscanf(tok, "MMA=%d", &v) == 1) t.MMA = v;
         else if (std::sscanf(tok, "KP=%d", &v) == 1) t.KP = v;
+        else if (std::sscanf(tok, "TC=%d", &v) == 1) t.TC = v;
+        else if (std::sscanf(tok, "TG=%d", &v) == 1) t.TG = v;
+        else if (std::sscanf(tok, "TS=%d", &v) == 1) t.TS = v;
+        else if (std::sscanf(tok, "TP=%d", &v) == 1) t.TP = v;
     }
     return t;
 }
@@ -294,6 +302,11 @@ dg_status validate(const dg_linear& op, bool allow_quant_input) {
 }
 
 dg_status check_smem(const dg_linear& op) {
+    // fp16 / bf16 at 8+ tokens runs on a tensor-core tile (tcgen05, or its
+    // mma.sync fallback), neither of which stages the activations
+    if ((op.kind == DG_LINEAR_F16 || op.kind == DG_LINEAR_BF16) && op.M >= 8 && !op.epilogue &&
+        op.K % 32 == 0 && tune().MMA != 0)
+        return DG_OK;
     const size_t need = gemv_smem(fmt_of(op.kind), pick_mt(op.M), op.K, op.group_size);
     const size_t lim = smem_optin_limit();
     if (lim == 0) return DG_ERR_CUDA;
@@ -390,6 +403,29 @@ static bool use_fp_mma(const dg_linear& op) {
         tune().MMA == 0 || op.epilogue)
         return false;
     return gemv_fp_mma_smem(op.K) <= smem_optin_limit();
+}
+
+// Whether fp16 / bf16 with this many tokens runs on the tcgen05 + TMA tile
+// (the mma.sync tile and the CUDA-core tiles remain for epilogues and for
+// what the TMA tile cannot address).
+static constexpr int kTcMinTokens = 8;
+
+static bool use_tc(const dg_linear& op) {
+    const int min_m = tune().TC >= 0 ? tune().TC : kTcMinTokens;
+    return (op.kind == DG_LINEAR_F16 || op.kind == DG_LINEAR_BF16) && min_m > 0 &&
+           op.M >= min_m && !op.epilogue && op.K % 8 == 0;
+}
+
+static dg_status launch_tc(const GemvParams& p, bool bf16, cudaStream_t s, bool* launched) {
+    *launched = false;
+    if (!gemv_tc_supported(p)) return DG_OK;
+    const unsigned spin = tune().SPIN > 0 ? (unsigned)tune().SPIN : 4000000u;
+    // L2 prefetch of the first weight boxes pays off while the previous launch's
+    // tail leaves DRAM idle, for launches short enough that the tail matters
+    size_t bytes = 0;
+    for (int g = 0; g < p.t.nseg; ++g) bytes += (size_t)p.t.seg[g].rows * p.a.K * 2;
+    const int prefetch = tune().TP >= 0 ? tune().TP : bytes <= ((size_t)64 << 20) ? 6 : 0;
+    return to_status(gemv_tc(p, bf16, spin, tune().TG, tune().TS, prefetch, s, launched));
 }
 
 // K split of the fp16 / bf16 tile, from K alone (so a row's result does not
@@ -496,6 +532,11 @@ static dg_status launch_group(const dg_linear* ops, int n, cudaStream_t s, void*
     }
     if (ops[0].epilogue == DG_EPI_RESIDUAL) p.t.res = ops[0].residual;
     if (use_i8_mma(ops[0])) return launch_i8_mma(p, s);
+    if (use_tc(ops[0])) {
+        bool launched = false;
+        const dg_status st = launch_tc(p, ops[0].kind == DG_LINEAR_BF16, s, &launched);
+        if (st != DG_OK || launched) return st;
+    }
     if (use_fp_mma(ops[0])) return launch_fp_mma(p, ops[0].kind == DG_LINEAR_BF16, s);
     if (use_w4_mma(ops[0])) return launch_w4_mma(p, ops[0].kind == DG_LINEAR_W4A8, s);
     GemvLaunch L{fmt_of(ops[0].kind), pick_mt(ops[0].M), 0, false, ops[0].K, p.group, 0};

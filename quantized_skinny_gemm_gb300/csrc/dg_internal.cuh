@@ -315,6 +315,14 @@ size_t gemv_w4_mma_smem(int K);
 // fp16 / bf16 for 8..16 tokens on the tensor cores (gemv_fp_mma.cu).
 cudaError_t gemv_fp_mma(const GemvParams* p, bool bf16, int K, int grid, cudaStream_t s, int* occ);
 size_t gemv_fp_mma_smem(int K);
+// fp16 / bf16, 1..16 tokens, on tcgen05 with TMA-fed operands (stream-K over
+// all SMs).  gemv_tc leaves *launched false (and returns cudaSuccess) when it
+// cannot take the launch: no tensor-map encoder, or no fixup scratch for this
+// stream yet while the stream is being captured.
+bool gemv_tc_supported(const GemvParams& p);
+cudaError_t gemv_tc(const GemvParams& p, bool bf16, unsigned spin, int grid, int stages, int prefetch,
+                    cudaStream_t s, bool* launched);
+size_t gemv_tc_smem();
 
 // Host helpers of api.cu shared with the static-scratch lm_head entry point.
 dg_status validate(const dg_linear& op, bool allow_quant_input);

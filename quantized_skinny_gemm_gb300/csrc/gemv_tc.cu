@@ -1,0 +1,574 @@
+// fp16 / bf16 weights for 2..16 tokens on the 5th-generation tensor cores
+// (tcgen05), the weight stream moved by the Tensor Memory Accelerator.
+//
+// With several tokens the skinny product is a dense contraction, so each
+// weight byte is read once by TMA and multiplied against all tokens by one
+// tcgen05.mma:  D[128 weight rows][16 tokens] += W[128][64 k] x[16][64 k]^T,
+// the 128 x 16 fp32 accumulator living in tensor memory (TMEM).  Tokens past
+// M, rows past a matrix's end and k past K are read as zeros by TMA.
+//
+// Work split (stream-K): the (row tile, 64-wide k block) pairs of the launch,
+// tile-major, are cut into gridDim.x equal contiguous ranges, one per CTA, so
+// every SM streams the same number of weight bytes whatever N and K are.  A
+// CTA runs one continuous TMA -> MMA pipeline over its range; a tile that its
+// range covers whole is rounded and stored by the CTA itself; a tile cut
+// between CTAs is finished by whichever of its CTAs arrives last, which adds
+// the pieces' fp32 partial sums in CTA order (so the result does not depend on
+// arrival order).  No CTA ever waits for another one.
+//
+// CTA roles (6 warps): warp 0 lane 0 issues TMA loads into a 6-stage ring
+// (16 KB of weights + 2 KB of tokens per stage, 128-byte swizzle); warp 1 owns
+// the TMEM allocation and its lane 0 issues the MMAs; warps 2-5 drain the two
+// TMEM accumulators (double-buffered, so a tile's epilogue overlaps the next
+// tile's MMAs), each warp reading the 32 TMEM lanes (weight rows) its warp
+// index may access.  Every wait is bounded; on a timeout the kernel records
+// the library's timeout error, lets its copies and MMAs land, frees TMEM and
+// returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "dg_internal.cuh"
+
+namespace dg {
+
+namespace {
+
+constexpr int kTcRows = 128;                       // MMA M: weight rows per tile
+constexpr int kTcTok = 16;                         // MMA N: tokens (zero-padded)
+constexpr int kTcBK = 64;                          // k per stage (one 128-byte swizzle row)
+constexpr int kTcABytes = kTcRows * kTcBK * 2;     // 16 KB
+constexpr int kTcBBytes = kTcTok * kTcBK * 2;      // 2 KB
+constexpr int kTcThreads = 192;
+constexpr int kTcPiece = kTcRows * kTcTok;         // floats of one partial tile
+constexpr int kTcMaxCtas = 256;
+constexpr int kTcMaxTiles = 65536;
+constexpr size_t tc_smem(int stages) { return (size_t)stages * (kTcABytes + kTcBBytes) + 1024 + 256; }
+
+struct TcParams {
+    CUtensorMap wmap[kMaxSeg];   // per matrix: {K, rows} fp16 / bf16, box {64, 128}
+    CUtensorMap xmap;            // tokens: {K, M}, box {64, 16}
+    void* y[kMaxSeg];            // [M][rows]
+    int rows[kMaxSeg];
+    int tile_begin[kMaxSeg + 1]; // first tile of each matrix (tiles never straddle two)
+    int nseg, nkb, M;
+    long long total;             // tiles * nkb
+    float* part;                 // [2 * gridDim.x][kTcPiece] partial tiles
+    unsigned* count;             // [tiles] pieces arrived; zero between launches
+    int* err;
+    unsigned spin;               // bound on every mbarrier wait (polls)
+    int prefetch;                // weight boxes prefetched to L2 before the dependency wait
+};
+
+// Instruction descriptor of tcgen05.mma .kind::f16: fp32 accumulator, A and B
+// K-major fp16 (or bf16), N = 16, M = 128.
+template <bool BF16>
+constexpr uint32_t tc_idesc() {
+    return (1u << 4) | (BF16 ? (1u << 7) | (1u << 10) : 0u) | ((uint32_t)(kTcTok >> 3) << 17) |
+           ((uint32_t)(kTcRows >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase of `bar` with this parity to complete, at most `limit`
+// polls; false (and the timeout recorded) if it did not.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned limit,
+                                          int* err) {
+    for (unsigned n = 0; n < limit; ++n)
+        if (mbar_try(bar, parity)) return true;
+    atomicExch(err, kErrTimeout);
+    return false;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, rows of 128 bytes
+// in groups of 8 rows 1024 bytes apart (the layout TMA writes with
+// CU_TENSOR_MAP_SWIZZLE_128B).  The 16-wide k step s of a stage starts 32 * s
+// bytes into the swizzle row.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+    return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)1 << 16) |
+           ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives on `bar` once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ long long range_begin(long long c, long long total, long long G) {
+    return c * total / G;
+}
+
+// The CTA whose range holds block `blk`.
+__device__ __forceinline__ int cta_of_block(long long blk, long long total, long long G) {
+    long long c = blk * G / total;
+    while (c > 0 && range_begin(c, total, G) > blk) --c;
+    while (c + 1 < G && range_begin(c + 1, total, G) <= blk) ++c;
+    return (int)c;
+}
+
+__device__ __forceinline__ int seg_of_tile(const TcParams& p, int tile) {
+    int g = 0;
+    while (g + 1 < p.nseg && tile >= p.tile_begin[g + 1]) ++g;
+    return g;
+}
+
+template <bool BF16>
+__device__ __forceinline__ void store_tokens(const TcParams& p, int g, int row, const float (&a)[16]) {
+    if (row >= p.rows[g]) return;
+    const size_t rows = (size_t)p.rows[g];
+    if (BF16) {
+        __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y[g]);
+#pragma unroll
+        for (int m = 0; m < kTcTok; ++m)
+            if (m < p.M) y[(size_t)m * rows + row] = __float2bfloat16_rn(a[m]);
+    } else {
+        __half* y = static_cast<__half*>(p.y[g]);
+#pragma unroll
+        for (int m = 0; m < kTcTok; ++m)
+            if (m < p.M) y[(size_t)m * rows + row] = __float2half_rn(a[m]);
+    }
+}
+
+}  // namespace
+
+template <bool BF16, int kTcStages>
+__global__ void __launch_bounds__(kTcThreads, 1) k_gemv_tc(const __grid_constant__ TcParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char* sA = smem;                                   // [stage][128 rows][128 B]
+    unsigned char* sB = smem + kTcStages * kTcABytes;           // [stage][16 tokens][128 B]
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + kTcStages * kTcBBytes);
+    uint64_t* empty = full + kTcStages;
+    uint64_t* acc_full = empty + kTcStages;                     // [2]
+    uint64_t* acc_empty = acc_full + 2;                         // [2]
+    uint64_t* mma_done = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    int* last_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long G = gridDim.x, c = blockIdx.x;
+    const long long b0 = range_begin(c, p.total, G), b1 = range_begin(c + 1, p.total, G);
+    const int nkb = p.nkb;
+
+    griddep_launch_dependents();
+    if (threadIdx.x == 0) {
+        for (int g = 0; g < p.nseg; ++g)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.wmap[g]))
+                         : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.xmap))
+                     : "memory");
+        for (int i = 0; i < kTcStages; ++i) {
+            mbar_init(smem_addr(&full[i]), 1);
+            mbar_init(smem_addr(&empty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_addr(&acc_full[i]), 1);
+            mbar_init(smem_addr(&acc_empty[i]), 128);
+        }
+        mbar_init(smem_addr(mma_done), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        // warm L2 with this CTA's first weight boxes while the previous launch
+        // drains (a prefetch never changes what a later load returns)
+        if (p.prefetch) {
+            const int nb = (int)(b1 - b0) < p.prefetch ? (int)(b1 - b0) : p.prefetch;
+            int tile = (int)(b0 / nkb), kb = (int)(b0 % nkb), g = seg_of_tile(p, tile);
+            for (int n = 0; n < nb; ++n) {
+                asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
+                                 reinterpret_cast<uint64_t>(&p.wmap[g])),
+                             "r"(kb * kTcBK), "r"((tile - p.tile_begin[g]) * kTcRows)
+                             : "memory");
+                if (++kb == nkb) {
+                    kb = 0;
+                    ++tile;
+                    if (g + 1 < p.nseg && tile >= p.tile_begin[g + 1]) ++g;
+                }
+            }
+        }
+    }
+    if (warp == 1) {
+        asm volatile(
+            "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 32;" ::"r"(
+                smem_addr(tmem_slot))
+            : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    griddep_wait();  // the tokens (and the outputs) belong to the previous launch until here
+
+    const int nblk = (int)(b1 - b0);          // k blocks of this CTA
+    const int t0 = (int)(b0 / nkb), kb_first = (int)(b0 % nkb);
+    if (warp == 0 && lane == 0) {
+        // ---- TMA producer ----
+        int tile = t0, kb = kb_first, g = seg_of_tile(p, t0), s = 0, issued = 0;
+        uint32_t ph = 0;  // parity of the ring's current lap
+        for (int n = 0; n < nblk; ++n) {
+            if (n >= kTcStages && !mbar_wait(smem_addr(&empty[s]), ph ^ 1u, p.spin, p.err)) break;
+            mbar_expect_tx(smem_addr(&full[s]), kTcABytes + kTcBBytes);
+            tma_load_2d(smem_addr(sA + s * kTcABytes), &p.wmap[g], kb * kTcBK,
+                        (tile - p.tile_begin[g]) * kTcRows, smem_addr(&full[s]));
+            tma_load_2d(smem_addr(sB + s * kTcBBytes), &p.xmap, kb * kTcBK, 0, smem_addr(&full[s]));
+            issued = n + 1;
+            if (++kb == nkb) {
+                kb = 0;
+                ++tile;
+                if (g + 1 < p.nseg && tile >= p.tile_begin[g + 1]) ++g;
+            }
+            if (++s == kTcStages) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
+        // the copies still in flight land before the CTA can leave
+        for (int j = issued > kTcStages ? issued - kTcStages : 0; j < issued; ++j)
+            mbar_wait(smem_addr(&full[j % kTcStages]), (uint32_t)((j / kTcStages) & 1), p.spin, p.err);
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer ----
+        constexpr uint32_t idesc = tc_idesc<BF16>();
+        int kb = kb_first, s = 0, seg_i = 0;  // seg_i: tiles started by this CTA
+        uint32_t ph = 0;
+        for (int n = 0; n < nblk; ++n) {
+            const bool first = n == 0 || kb == 0;
+            const bool last = n == nblk - 1 || kb == nkb - 1;
+            const int buf = seg_i & 1;
+            if (first && seg_i >= 2 &&
+                !mbar_wait(smem_addr(&acc_empty[buf]), (uint32_t)((seg_i / 2 - 1) & 1), p.spin, p.err))
+                break;
+            if (!mbar_wait(smem_addr(&full[s]), ph, p.spin, p.err)) break;
+            tc_fence_after();
+            const uint32_t a0 = smem_addr(sA + s * kTcABytes), bb0 = smem_addr(sB + s * kTcBBytes);
+#pragma unroll
+            for (int kk = 0; kk < kTcBK / 16; ++kk)
+                tc_mma(tmem + (uint32_t)(buf * kTcTok), sw128_desc(a0 + kk * 32),
+                       sw128_desc(bb0 + kk * 32), idesc, (first && kk == 0) ? 0u : 1u);
+            tc_commit(smem_addr(&empty[s]));
+            if (last) {
+                tc_commit(smem_addr(&acc_full[buf]));
+                ++seg_i;
+            }
+            if (++kb == nkb) kb = 0;
+            if (++s == kTcStages) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
+        tc_commit(smem_addr(mma_done));
+        mbar_wait(smem_addr(mma_done), 0, p.spin, p.err);
+    } else if (warp >= 2) {
+        // ---- epilogue: 128 threads, thread <-> weight row of the tile ----
+        const int q = warp & 3;                 // TMEM lanes 32q .. 32q + 31
+        const int rl = 32 * q + lane;           // row within the tile
+        const int t1 = (int)((b1 - 1) / nkb);
+        for (int tile = t0; tile <= t1; ++tile) {
+            const int si = tile - t0, buf = si & 1;
+            float a[16];
+            if (mbar_wait(smem_addr(&acc_full[buf]), (uint32_t)((si / 2) & 1), p.spin, p.err)) {
+                tc_fence_after();
+                tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * kTcTok), a);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) a[j] = 0.f;
+            }
+            tc_fence_before();
+            mbar_arrive(smem_addr(&acc_empty[buf]));
+            const int g = seg_of_tile(p, tile);
+            const int row = (tile - p.tile_begin[g]) * kTcRows + rl;
+            const long long tb = (long long)tile * nkb, te = tb + nkb;
+            if (b0 <= tb && b1 >= te) {  // the whole tile is this CTA's
+                store_tokens<BF16>(p, g, row, a);
+                continue;
+            }
+            // a piece of a tile shared with other CTAs: publish it (one release
+            // by one thread after the epilogue's barrier covers the 128 threads'
+            // stores), and the last of the tile's CTAs to arrive sums the pieces
+            // in CTA order
+            float4* dst = reinterpret_cast<float4*>(
+                p.part + ((size_t)(2 * c + (si == 0 ? 0 : 1)) * kTcPiece + (size_t)rl * kTcTok));
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                __stcg(dst + j, make_float4(a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3]));
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            const int fc = cta_of_block(tb, p.total, G), lc = cta_of_block(te - 1, p.total, G);
+            if (threadIdx.x == 64) {
+                unsigned old;
+                asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
+                             : "=r"(old)
+                             : "l"(p.count + tile)
+                             : "memory");
+                *last_flag = old == (unsigned)(lc - fc) ? 1 : 0;
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (*last_flag) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) a[j] = 0.f;
+                for (int c0 = fc; c0 <= lc; c0 += 4) {  // four pieces in flight at a time
+                    float4 v[4][4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int cc = c0 + u;
+                        if (cc > lc) break;
+                        const int first_tile = (int)(range_begin(cc, p.total, G) / nkb);
+                        const float4* src = reinterpret_cast<const float4*>(
+                            p.part + ((size_t)(2 * cc + (tile == first_tile ? 0 : 1)) * kTcPiece +
+                                      (size_t)rl * kTcTok));
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) v[u][j] = __ldcg(src + j);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        if (c0 + u > lc) break;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            a[4 * j] += v[u][j].x;
+                            a[4 * j + 1] += v[u][j].y;
+                            a[4 * j + 2] += v[u][j].z;
+                            a[4 * j + 3] += v[u][j].w;
+                        }
+                    }
+                }
+                store_tokens<BF16>(p, g, row, a);
+                if (threadIdx.x == 64) p.count[tile] = 0u;  // ready for the next launch
+            }
+        }
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 32;" ::"r"(tmem) : "memory");
+}
+
+// ---- host side ---------------------------------------------------------------------
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// 2-D row-major map of a [outer][inner] fp16 / bf16 array, 128-byte swizzle.
+bool encode_2d(CUtensorMap* m, const void* base, bool bf16, int inner, int outer, int box_inner,
+               int box_outer) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    const cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct TcScratch {
+    float* part = nullptr;
+    unsigned* count = nullptr;
+};
+
+// The fixup scratch of one (device, stream): launches on one stream run one
+// after another, so they can share it; launches on different streams never do.
+// Allocated on first use (outside stream capture), counters zeroed on that
+// stream; every launch leaves them zero.
+bool tc_scratch(cudaStream_t s, TcScratch* out) {
+    static std::mutex mu;
+    static std::map<std::pair<int, cudaStream_t>, TcScratch> table;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> g(mu);
+    auto it = table.find({dev, s});
+    if (it != table.end()) {
+        *out = it->second;
+        return true;
+    }
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+        cudaGetLastError();
+        return false;
+    }
+    TcScratch t;
+    if (cudaMalloc(&t.part, (size_t)2 * kTcMaxCtas * kTcPiece * sizeof(float)) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (cudaMalloc(&t.count, (size_t)kTcMaxTiles * sizeof(unsigned)) != cudaSuccess ||
+        cudaMemsetAsync(t.count, 0, (size_t)kTcMaxTiles * sizeof(unsigned), s) != cudaSuccess) {
+        cudaFree(t.part);
+        if (t.count) cudaFree(t.count);
+        cudaGetLastError();
+        return false;
+    }
+    table[{dev, s}] = t;
+    *out = t;
+    return true;
+}
+
+// The dynamic shared memory opt-in, set once per device and instantiation.
+cudaError_t smem_attr_once(const void* fn, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void*>, bool> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> g(mu);
+    if (done.count({dev, fn})) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) done[{dev, fn}] = true;
+    return e;
+}
+
+template <bool BF16>
+const void* tc_kernel(int stages) {
+    switch (stages) {
+        case 8: return reinterpret_cast<const void*>(k_gemv_tc<BF16, 8>);
+        case 12: return reinterpret_cast<const void*>(k_gemv_tc<BF16, 12>);
+        default: return reinterpret_cast<const void*>(k_gemv_tc<BF16, 6>);
+    }
+}
+
+}  // namespace
+
+bool gemv_tc_supported(const GemvParams& p) {
+    if (p.a.M < 1 || p.a.M > kTcTok || p.a.K % 8 || !encode_fn()) return false;
+    if (reinterpret_cast<uintptr_t>(p.a.x) & 15) return false;
+    int tiles = 0;
+    for (int g = 0; g < p.t.nseg; ++g) {
+        if (reinterpret_cast<uintptr_t>(p.t.seg[g].W) & 15) return false;
+        tiles += (p.t.seg[g].rows + kTcRows - 1) / kTcRows;
+    }
+    return tiles <= kTcMaxTiles && p.t.nseg <= kMaxSeg && !p.t.pair && !p.t.res;
+}
+
+size_t gemv_tc_smem() { return tc_smem(6); }
+
+cudaError_t gemv_tc(const GemvParams& gp, bool bf16, unsigned spin, int grid_req, int stages,
+                    int prefetch, cudaStream_t s, bool* launched) {
+    *launched = false;
+    TcScratch scratch;
+    if (!tc_scratch(s, &scratch)) return cudaSuccess;
+    TcParams p;
+    memset(&p, 0, sizeof p);
+    const int K = gp.a.K;
+    p.nseg = gp.t.nseg;
+    p.M = gp.a.M;
+    p.nkb = (K + kTcBK - 1) / kTcBK;
+    int tiles = 0;
+    for (int g = 0; g < p.nseg; ++g) {
+        const Segment& sg = gp.t.seg[g];
+        if (!encode_2d(&p.wmap[g], sg.W, bf16, K, sg.rows, kTcBK, kTcRows)) return cudaSuccess;
+        p.y[g] = sg.y;
+        p.rows[g] = sg.rows;
+        p.tile_begin[g] = tiles;
+        tiles += (sg.rows + kTcRows - 1) / kTcRows;
+    }
+    p.tile_begin[p.nseg] = tiles;
+    if (!encode_2d(&p.xmap, gp.a.x, bf16, K, gp.a.M, kTcBK, kTcTok)) return cudaSuccess;
+    p.total = (long long)tiles * p.nkb;
+    p.part = scratch.part;
+    p.count = scratch.count;
+    p.err = device_error_word();
+    p.spin = spin;
+    p.prefetch = prefetch;
+    if (!p.err) return cudaSuccess;
+    long long grid = grid_req > 0 ? grid_req : sm_count();
+    if (grid > kTcMaxCtas) grid = kTcMaxCtas;
+    if (grid > p.total) grid = p.total;
+    if (grid < 1) grid = 1;
+    if (stages != 8 && stages != 12) stages = 6;
+    const void* fn = bf16 ? tc_kernel<true>(stages) : tc_kernel<false>(stages);
+    const size_t smem = tc_smem(stages);
+    cudaError_t e = smem_attr_once(fn, smem);
+    if (e != cudaSuccess) return e;
+    void* args[] = {&p};
+    e = launch_pdl(fn, dim3((unsigned)grid), dim3(kTcThreads), smem, s, args);
+    if (e == cudaSuccess) *launched = true;
+    return e;
+}
+
+}  // namespace dg
