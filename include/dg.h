@@ -44,7 +44,10 @@
  *    launch's 128-row x 64-k weight blocks cut into one equal range per SM; a
  *    row tile cut between CTAs is summed in fp32 piece by piece in CTA order),
  *    so their order depends on K, on the rows of the whole launch and on the
- *    SM count, and is still the same on every call.  Such a call keeps a small
+ *    SM count, and is still the same on every call.  The same holds for int4
+ *    calls on the int8 / int4 tcgen05 tile (by default 8+ tokens with K >
+ *    8192; one fp32 accumulator per group, scaled as in the scalar
+ *    definition); W8A8 there keeps exact int32 sums.  Such a call keeps a small
  *    fixup scratch per (device, stream) (about 4.3 MB, allocated on the
  *    stream's first such call); a stream first used inside graph capture runs
  *    the mma.sync tile instead (K split by a rule on K alone).
@@ -54,10 +57,12 @@
  *    read once per process) overrides launch choices for configuration
  *    sweeps; unset, the defaults above hold.  Every setting stays within the
  *    parity bound; KS (warps per row), KP (split-K ranges), MMA (tensor-core
- *    tiles off / int8 tile), TC (fewest tokens on the tcgen05 tile, 0 = off)
- *    and TG (its CTA count) change a row's summation order, the others (TS:
- *    its ring stages 6 / 8 / 12; TP: weight boxes it prefetches to L2 before
- *    the dependency wait) only the schedule.
+ *    tiles off / int8 tile), TC (fewest tokens on the fp16 / bf16 tcgen05
+ *    tile, 0 = off), TQ (fewest tokens on the int8 / int4 tcgen05 tile, 0 =
+ *    off; by default only int4 with 8+ tokens and K > 8192 goes there) and TG
+ *    (the tcgen05 tiles' CTA count) change a row's summation order, the others
+ *    (TS: the fp16 tile's ring stages 6 / 8 / 12; TP: weight boxes it
+ *    prefetches to L2 before the dependency wait) only the schedule.
  */
 #ifndef DG_H_
 #define DG_H_

@@ -78,6 +78,7 @@ struct Tune {
     int TG = 0;                                // CTAs of the tcgen05 tile (0 = one per SM)
     int TS = 0;                                // TMA ring stages of the tcgen05 tile (6, 8, 12)
     int TP = -1;                               // weight boxes the tcgen05 tile prefetches early
+    int TQ = -1;                               // fewest tokens on the int8 / int4 tcgen05 tile (0 = off)
 };
 
 static Tune read_tune() {
@@ -103,6 +104,7 @@ static Tune read_tune() {
         else if (std::sscanf(tok, "TG=%d", &v) == 1) t.TG = v;
         else if (std::sscanf(tok, "TS=%d", &v) == 1) t.TS = v;
         else if (std::sscanf(tok, "TP=%d", &v) == 1) t.TP = v;
+        else if (std::sscanf(tok, "TQ=%d", &v) == 1) t.TQ = v;
     }
     return t;
 }
@@ -428,6 +430,25 @@ static dg_status launch_tc(const GemvParams& p, bool bf16, cudaStream_t s, bool*
     return to_status(gemv_tc(p, bf16, spin, tune().TG, tune().TS, prefetch, s, launched));
 }
 
+// Whether int8 / int4 with this many tokens runs on the tcgen05 tile.  By
+// default only where it measured faster than the mma.sync / CUDA-core tiles:
+// int4 at 8+ tokens with rows longer than 8192 k (44 us against 57-69 us for
+// 4096 x 14336 at 8 tokens); DG_TUNE TQ=m sends every int8 / int4 launch of
+// m or more tokens to it.
+static bool use_tcq(const dg_linear& op) {
+    const bool int4 = op.kind == DG_LINEAR_W4A16 || op.kind == DG_LINEAR_W4A8;
+    if (op.epilogue || (!int4 && op.kind != DG_LINEAR_W8A8)) return false;
+    if (tune().TQ >= 0) return tune().TQ > 0 && op.M >= tune().TQ;
+    return int4 && op.M >= 8 && op.K > 8192;
+}
+
+static dg_status launch_tcq(const GemvParams& p, Fmt f, cudaStream_t s, bool* launched) {
+    *launched = false;
+    if (!gemv_tcq_supported(p, f)) return DG_OK;
+    const unsigned spin = tune().SPIN > 0 ? (unsigned)tune().SPIN : 4000000u;
+    return to_status(gemv_tcq(p, f, spin, tune().TG, s, launched));
+}
+
 // K split of the fp16 / bf16 tile, from K alone (so a row's result does not
 // depend on N): the most warps (4, 2, 1) that divide the 32-wide k blocks and
 // leave each at least 16 of them.
@@ -531,6 +552,11 @@ static dg_status launch_group(const dg_linear* ops, int n, cudaStream_t s, void*
         p.t.pair = 1;
     }
     if (ops[0].epilogue == DG_EPI_RESIDUAL) p.t.res = ops[0].residual;
+    if (use_tcq(ops[0])) {
+        bool launched = false;
+        const dg_status st = launch_tcq(p, fmt_of(ops[0].kind), s, &launched);
+        if (st != DG_OK || launched) return st;
+    }
     if (use_i8_mma(ops[0])) return launch_i8_mma(p, s);
     if (use_tc(ops[0])) {
         bool launched = false;

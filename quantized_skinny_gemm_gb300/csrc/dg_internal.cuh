@@ -323,6 +323,12 @@ bool gemv_tc_supported(const GemvParams& p);
 cudaError_t gemv_tc(const GemvParams& p, bool bf16, unsigned spin, int grid, int stages, int prefetch,
                     cudaStream_t s, bool* launched);
 size_t gemv_tc_smem();
+// int8 / int4 weights (W8A8, W4A16, W4A8), 1..16 tokens, on tcgen05: codes
+// widened to fp16 into TMEM, group scales applied per accumulator run
+// (gemv_tcq.cu).  Same launch contract as gemv_tc.
+bool gemv_tcq_supported(const GemvParams& p, Fmt f);
+cudaError_t gemv_tcq(const GemvParams& p, Fmt f, unsigned spin, int grid, cudaStream_t s,
+                     bool* launched);
 
 // Host helpers of api.cu shared with the static-scratch lm_head entry point.
 dg_status validate(const dg_linear& op, bool allow_quant_input);

@@ -24,28 +24,26 @@
 // index may access.  Every wait is bounded; on a timeout the kernel records
 // the library's timeout error, lets its copies and MMAs land, frees TMEM and
 // returns.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <map>
 #include <mutex>
 #include <utility>
 
-#include "dg_internal.cuh"
+#include "tc_common.cuh"
 
 namespace dg {
 
+using namespace tc;
+
 namespace {
 
-constexpr int kTcRows = 128;                       // MMA M: weight rows per tile
-constexpr int kTcTok = 16;                         // MMA N: tokens (zero-padded)
+constexpr int kTcRows = kRows;
+constexpr int kTcTok = kTok;
 constexpr int kTcBK = 64;                          // k per stage (one 128-byte swizzle row)
 constexpr int kTcABytes = kTcRows * kTcBK * 2;     // 16 KB
 constexpr int kTcBBytes = kTcTok * kTcBK * 2;      // 2 KB
 constexpr int kTcThreads = 192;
-constexpr int kTcPiece = kTcRows * kTcTok;         // floats of one partial tile
-constexpr int kTcMaxCtas = 256;
-constexpr int kTcMaxTiles = 65536;
+constexpr int kTcPiece = kPiece;
+constexpr int kTcMaxCtas = kMaxCtas;
 constexpr size_t tc_smem(int stages) { return (size_t)stages * (kTcABytes + kTcBBytes) + 1024 + 256; }
 
 struct TcParams {
@@ -63,120 +61,6 @@ struct TcParams {
     int prefetch;                // weight boxes prefetched to L2 before the dependency wait
 };
 
-// Instruction descriptor of tcgen05.mma .kind::f16: fp32 accumulator, A and B
-// K-major fp16 (or bf16), N = 16, M = 128.
-template <bool BF16>
-constexpr uint32_t tc_idesc() {
-    return (1u << 4) | (BF16 ? (1u << 7) | (1u << 10) : 0u) | ((uint32_t)(kTcTok >> 3) << 17) |
-           ((uint32_t)(kTcRows >> 4) << 24);
-}
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Waits for the phase of `bar` with this parity to complete, at most `limit`
-// polls; false (and the timeout recorded) if it did not.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned limit,
-                                          int* err) {
-    for (unsigned n = 0; n < limit; ++n)
-        if (mbar_try(bar, parity)) return true;
-    atomicExch(err, kErrTimeout);
-    return false;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, rows of 128 bytes
-// in groups of 8 rows 1024 bytes apart (the layout TMA writes with
-// CU_TENSOR_MAP_SWIZZLE_128B).  The 16-wide k step s of a stage starts 32 * s
-// bytes into the swizzle row.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
-    return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)1 << 16) |
-           ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrives on `bar` once every MMA this thread issued so far has completed.
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// 16 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-}
-
-__device__ __forceinline__ long long range_begin(long long c, long long total, long long G) {
-    return c * total / G;
-}
-
-// The CTA whose range holds block `blk`.
-__device__ __forceinline__ int cta_of_block(long long blk, long long total, long long G) {
-    long long c = blk * G / total;
-    while (c > 0 && range_begin(c, total, G) > blk) --c;
-    while (c + 1 < G && range_begin(c + 1, total, G) <= blk) ++c;
-    return (int)c;
-}
 
 __device__ __forceinline__ int seg_of_tile(const TcParams& p, int tile) {
     int g = 0;
@@ -300,7 +184,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemv_tc(const __grid_constant
             mbar_wait(smem_addr(&full[j % kTcStages]), (uint32_t)((j / kTcStages) & 1), p.spin, p.err);
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer ----
-        constexpr uint32_t idesc = tc_idesc<BF16>();
+        constexpr uint32_t idesc = idesc_f16<BF16>();
         int kb = kb_first, s = 0, seg_i = 0;  // seg_i: tiles started by this CTA
         uint32_t ph = 0;
         for (int n = 0; n < nblk; ++n) {
@@ -417,9 +301,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemv_tc(const __grid_constant
 
 // ---- host side ---------------------------------------------------------------------
 
-namespace {
+namespace tc {
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void* f = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -432,33 +316,27 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D row-major map of a [outer][inner] fp16 / bf16 array, 128-byte swizzle.
-bool encode_2d(CUtensorMap* m, const void* base, bool bf16, int inner, int outer, int box_inner,
-               int box_outer) {
+bool have_encoder() { return encode_fn() != nullptr; }
+
+bool encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType type, int elem_bytes,
+               long long inner, long long outer, int box_inner, int box_outer,
+               CUtensorMapSwizzle swizzle) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
-    const cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+    const cuuint64_t strides[1] = {(cuuint64_t)inner * (cuuint64_t)elem_bytes};
     const cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return fn(m, type, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-struct TcScratch {
-    float* part = nullptr;
-    unsigned* count = nullptr;
-};
-
-// The fixup scratch of one (device, stream): launches on one stream run one
-// after another, so they can share it; launches on different streams never do.
-// Allocated on first use (outside stream capture), counters zeroed on that
-// stream; every launch leaves them zero.
-bool tc_scratch(cudaStream_t s, TcScratch* out) {
+// Allocated on a stream's first use (outside stream capture), counters zeroed
+// on that stream; every launch leaves them zero.
+bool scratch(cudaStream_t s, Scratch* out) {
     static std::mutex mu;
-    static std::map<std::pair<int, cudaStream_t>, TcScratch> table;
+    static std::map<std::pair<int, cudaStream_t>, Scratch> table;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     std::lock_guard<std::mutex> g(mu);
@@ -472,13 +350,13 @@ bool tc_scratch(cudaStream_t s, TcScratch* out) {
         cudaGetLastError();
         return false;
     }
-    TcScratch t;
-    if (cudaMalloc(&t.part, (size_t)2 * kTcMaxCtas * kTcPiece * sizeof(float)) != cudaSuccess) {
+    Scratch t;
+    if (cudaMalloc(&t.part, (size_t)2 * kMaxCtas * kPiece * sizeof(float)) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
-    if (cudaMalloc(&t.count, (size_t)kTcMaxTiles * sizeof(unsigned)) != cudaSuccess ||
-        cudaMemsetAsync(t.count, 0, (size_t)kTcMaxTiles * sizeof(unsigned), s) != cudaSuccess) {
+    if (cudaMalloc(&t.count, (size_t)kMaxTiles * sizeof(unsigned)) != cudaSuccess ||
+        cudaMemsetAsync(t.count, 0, (size_t)kMaxTiles * sizeof(unsigned), s) != cudaSuccess) {
         cudaFree(t.part);
         if (t.count) cudaFree(t.count);
         cudaGetLastError();
@@ -489,7 +367,6 @@ bool tc_scratch(cudaStream_t s, TcScratch* out) {
     return true;
 }
 
-// The dynamic shared memory opt-in, set once per device and instantiation.
 cudaError_t smem_attr_once(const void* fn, size_t smem) {
     static std::mutex mu;
     static std::map<std::pair<int, const void*>, bool> done;
@@ -503,6 +380,10 @@ cudaError_t smem_attr_once(const void* fn, size_t smem) {
     return e;
 }
 
+}  // namespace tc
+
+namespace {
+
 template <bool BF16>
 const void* tc_kernel(int stages) {
     switch (stages) {
@@ -515,14 +396,14 @@ const void* tc_kernel(int stages) {
 }  // namespace
 
 bool gemv_tc_supported(const GemvParams& p) {
-    if (p.a.M < 1 || p.a.M > kTcTok || p.a.K % 8 || !encode_fn()) return false;
+    if (p.a.M < 1 || p.a.M > kTcTok || p.a.K % 8 || !have_encoder()) return false;
     if (reinterpret_cast<uintptr_t>(p.a.x) & 15) return false;
     int tiles = 0;
     for (int g = 0; g < p.t.nseg; ++g) {
         if (reinterpret_cast<uintptr_t>(p.t.seg[g].W) & 15) return false;
         tiles += (p.t.seg[g].rows + kTcRows - 1) / kTcRows;
     }
-    return tiles <= kTcMaxTiles && p.t.nseg <= kMaxSeg && !p.t.pair && !p.t.res;
+    return tiles <= kMaxTiles && p.t.nseg <= kMaxSeg && !p.t.pair && !p.t.res;
 }
 
 size_t gemv_tc_smem() { return tc_smem(6); }
@@ -530,28 +411,31 @@ size_t gemv_tc_smem() { return tc_smem(6); }
 cudaError_t gemv_tc(const GemvParams& gp, bool bf16, unsigned spin, int grid_req, int stages,
                     int prefetch, cudaStream_t s, bool* launched) {
     *launched = false;
-    TcScratch scratch;
-    if (!tc_scratch(s, &scratch)) return cudaSuccess;
+    Scratch scr;
+    if (!scratch(s, &scr)) return cudaSuccess;
     TcParams p;
     memset(&p, 0, sizeof p);
     const int K = gp.a.K;
     p.nseg = gp.t.nseg;
     p.M = gp.a.M;
     p.nkb = (K + kTcBK - 1) / kTcBK;
+    const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     int tiles = 0;
     for (int g = 0; g < p.nseg; ++g) {
         const Segment& sg = gp.t.seg[g];
-        if (!encode_2d(&p.wmap[g], sg.W, bf16, K, sg.rows, kTcBK, kTcRows)) return cudaSuccess;
+        if (!encode_2d(&p.wmap[g], sg.W, dt, 2, K, sg.rows, kTcBK, kTcRows, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaSuccess;
         p.y[g] = sg.y;
         p.rows[g] = sg.rows;
         p.tile_begin[g] = tiles;
         tiles += (sg.rows + kTcRows - 1) / kTcRows;
     }
     p.tile_begin[p.nseg] = tiles;
-    if (!encode_2d(&p.xmap, gp.a.x, bf16, K, gp.a.M, kTcBK, kTcTok)) return cudaSuccess;
+    if (!encode_2d(&p.xmap, gp.a.x, dt, 2, K, gp.a.M, kTcBK, kTcTok, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaSuccess;
     p.total = (long long)tiles * p.nkb;
-    p.part = scratch.part;
-    p.count = scratch.count;
+    p.part = scr.part;
+    p.count = scr.count;
     p.err = device_error_word();
     p.spin = spin;
     p.prefetch = prefetch;
