@@ -371,17 +371,19 @@ def build_workload(name, dev, torch):
         w.cpu_sample = None
         w.keep = (Ws, outs)
         w.dtype = "f16->" + ("int4" if name == "quant_w4" else "i8")
-    elif name in ("int4_m8", "int4_m16", "int4_a8_m16"):
-        # one int4 matrix at 8 / 16 tokens (verify block), rotating copies > 2x L2
+    elif name in ("int4_m8", "int4_m16", "int4_a8_m16", "int4_down_m8"):
+        # one int4 matrix at 8 / 16 tokens (verify block), rotating copies > 2x L2:
+        # the 14336x4096 up projection, or the 4096x14336 down projection
         M = int(name.split("_m")[1])
-        Wq, sc, x = synth.w4_case(14336, 4096, M, seed=0)
+        NW, KW = (4096, 14336) if "down" in name else (14336, 4096)
+        Wq, sc, x = synth.w4_case(NW, KW, M, seed=0)
         per = Wq.numel() + sc.numel() * 2
         C = -(-2 * L2_BYTES // per)
         xd = x.to(dev)
         copies = [(Wq.to(dev), sc.to(dev)) for _ in range(C)]
-        ys = [torch.empty(M, 14336, dtype=torch.float16, device=dev) for _ in range(C)]
+        ys = [torch.empty(M, NW, dtype=torch.float16, device=dev) for _ in range(C)]
         if name == "int4_a8_m16":
-            xq = torch.empty(M, 4096, dtype=torch.int8, device=dev)
+            xq = torch.empty(M, KW, dtype=torch.int8, device=dev)
             xs_ = torch.empty(M, dtype=torch.float32, device=dev)
             dg.quantize_act_i8(xd, xq, xs_, stream=s)
             calls = [lambda c=c, y=y: dg.gemv_w4(c[0], c[1], y, x_i8=xq, x_scale=xs_, stream=s)
@@ -398,8 +400,8 @@ def build_workload(name, dev, torch):
         w.launches = C
         w.run = lambda: [c() for c in calls]
         w.config = workload_config(name)
-        w.dominant = ("int4 14336x4096 verify tile, M=%d" % M, w.run, C, per)
-        w.cpu_sample = ("w4a16", ([synth.Layer([synth.Linear("m", 14336, 4096, Wq, sc, "x")],
+        w.dominant = ("int4 %dx%d verify tile, M=%d" % (NW, KW, M), w.run, C, per)
+        w.cpu_sample = ("w4a16", ([synth.Layer([synth.Linear("m", NW, KW, Wq, sc, "x")],
                                                {"x": x})], None, None))
         w.keep = (copies, ys)
     elif name == "gemv_f16_2048" or name.startswith("w8a8_m") or name.startswith("fp16_m"):
@@ -521,12 +523,13 @@ def workload_config(name):
                             ("int4 g32" if name == "quant_w4" else "int8 per-channel"),
                 "bytes_per_call": per, "calls_per_step": C,
                 "l2": "%d rotating copies, %.0f MB > 2x L2" % (C, C * per / 1e6)}
-    if name in ("int4_m8", "int4_m16", "int4_a8_m16"):
+    if name in ("int4_m8", "int4_m16", "int4_a8_m16", "int4_down_m8"):
         per = int4_bytes(14336 * 4096)
         C = -(-2 * L2_BYTES // per)
         M = int(name.split("_m")[1])
-        return {"workload": "int4 g32 14336x4096 verify tile, W4%s, M=%d"
-                            % ("A8" if "a8" in name else "A16", M),
+        return {"workload": "int4 g32 %s verify tile, W4%s, M=%d"
+                            % ("4096x14336" if "down" in name else "14336x4096",
+                               "A8" if "a8" in name else "A16", M),
                 "bytes_per_call": per, "calls_per_step": C,
                 "l2": "%d rotating weight copies, %.0f MB > 2x L2" % (C, C * per / 1e6)}
     if name == "gemv_f16_2048" or name.startswith("w8a8_m") or name.startswith("fp16_m"):
@@ -695,7 +698,8 @@ def main():
                              "gemv_f16_2048", "w8a8_m1",
                              "w8a8_m4", "w8a8_m16", "fp16_m8", "fp16_m16", "block_fp16_fused",
                              "block_fp16_unfused", "decode_int4_a16_f16head", "conv1d",
-                             "quant_w4", "quant_w8", "int4_m8", "int4_m16", "int4_a8_m16"])
+                             "quant_w4", "quant_w8", "int4_m8", "int4_m16", "int4_a8_m16",
+                             "int4_down_m8"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-configs", dest="configs", action="store_false",
                     help="skip the per-configuration measurements (the `configs` object)")
@@ -824,6 +828,7 @@ CONFIG_WORKLOADS = [
     ("config 1", "gemv_f16_2048"), ("config 3", "lm_head"), ("config 4", "w8a8_m1"),
     ("config 4", "w8a8_m4"), ("config 4", "w8a8_m16"), ("config 5", "decode_int4_a16"),
     ("config 5", "decode_int4_a8"), ("NEXT-1", "int4_m16"), ("NEXT-1", "int4_a8_m16"),
+    ("NEXT-1", "int4_down_m8"),
     ("NEXT-1", "fp16_m16"), ("NEXT-2", "block_fp16_fused"), ("NEXT-2", "block_fp16_unfused"),
     ("NEXT-3", "decode_int4_a16_f16head"), ("NEXT-3", "quant_w4"), ("NEXT-4", "conv1d"),
 ]
