@@ -61,8 +61,9 @@
  *    tile, 0 = off), TQ (fewest tokens on the int8 / int4 tcgen05 tile, 0 =
  *    off; by default only int4 with 8+ tokens and K > 8192 goes there) and TG
  *    (the tcgen05 tiles' CTA count) change a row's summation order, the others
- *    (TS: the fp16 tile's ring stages 6 / 8 / 12; TP: weight boxes it
- *    prefetches to L2 before the dependency wait) only the schedule.
+ *    (TK: 64-k boxes per stage of the fp16 tile, 1 or 2; TS: its ring stages,
+ *    6 / 8 / 12 with one box, 3 / 4 / 6 with two; TP: stages it prefetches to
+ *    L2 before the dependency wait) only the schedule.
  */
 #ifndef DG_H_
 #define DG_H_

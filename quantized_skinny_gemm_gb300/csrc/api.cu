@@ -79,6 +79,7 @@ struct Tune {
     int TS = 0;                                // TMA ring stages of the tcgen05 tile (6, 8, 12)
     int TP = -1;                               // weight boxes the tcgen05 tile prefetches early
     int TQ = -1;                               // fewest tokens on the int8 / int4 tcgen05 tile (0 = off)
+    int TK = 0;                                // 64-k boxes per stage of the fp16 tcgen05 tile (1, 2; 0 = 2)
 };
 
 static Tune read_tune() {
@@ -105,6 +106,7 @@ static Tune read_tune() {
         else if (std::sscanf(tok, "TS=%d", &v) == 1) t.TS = v;
         else if (std::sscanf(tok, "TP=%d", &v) == 1) t.TP = v;
         else if (std::sscanf(tok, "TQ=%d", &v) == 1) t.TQ = v;
+        else if (std::sscanf(tok, "TK=%d", &v) == 1) t.TK = v;
     }
     return t;
 }
@@ -427,7 +429,10 @@ static dg_status launch_tc(const GemvParams& p, bool bf16, cudaStream_t s, bool*
     size_t bytes = 0;
     for (int g = 0; g < p.t.nseg; ++g) bytes += (size_t)p.t.seg[g].rows * p.a.K * 2;
     const int prefetch = tune().TP >= 0 ? tune().TP : bytes <= ((size_t)64 << 20) ? 6 : 0;
-    return to_status(gemv_tc(p, bf16, spin, tune().TG, tune().TS, prefetch, s, launched));
+    // two 64-k boxes per stage, four stages (measured best of 6x1, 8x1, 12x1, 3x2, 4x2, 6x2)
+    const int nb = tune().TK == 1 ? 1 : 2;
+    const int stages = tune().TS > 0 ? tune().TS : nb == 2 ? 4 : 6;
+    return to_status(gemv_tc(p, bf16, spin, tune().TG, stages, nb, prefetch, s, launched));
 }
 
 // Whether int8 / int4 with this many tokens runs on the tcgen05 tile.  By

@@ -320,8 +320,8 @@ size_t gemv_fp_mma_smem(int K);
 // cannot take the launch: no tensor-map encoder, or no fixup scratch for this
 // stream yet while the stream is being captured.
 bool gemv_tc_supported(const GemvParams& p);
-cudaError_t gemv_tc(const GemvParams& p, bool bf16, unsigned spin, int grid, int stages, int prefetch,
-                    cudaStream_t s, bool* launched);
+cudaError_t gemv_tc(const GemvParams& p, bool bf16, unsigned spin, int grid, int stages, int nb,
+                    int prefetch, cudaStream_t s, bool* launched);
 size_t gemv_tc_smem();
 // int8 / int4 weights (W8A8, W4A16, W4A8), 1..16 tokens, on tcgen05: codes
 // widened to fp16 into TMEM, group scales applied per accumulator run

@@ -16,8 +16,9 @@
 // the pieces' fp32 partial sums in CTA order (so the result does not depend on
 // arrival order).  No CTA ever waits for another one.
 //
-// CTA roles (6 warps): warp 0 lane 0 issues TMA loads into a 6-stage ring
-// (16 KB of weights + 2 KB of tokens per stage, 128-byte swizzle); warp 1 owns
+// CTA roles (6 warps): warp 0 lane 0 issues TMA loads into a ring of stages of
+// NB 64-k boxes (16 KB of weights + 2 KB of tokens per box, 128-byte swizzle;
+// by default 4 stages of 2 boxes, 8 MMAs per stage); warp 1 owns
 // the TMEM allocation and its lane 0 issues the MMAs; warps 2-5 drain the two
 // TMEM accumulators (double-buffered, so a tile's epilogue overlaps the next
 // tile's MMAs), each warp reading the 32 TMEM lanes (weight rows) its warp
@@ -44,7 +45,10 @@ constexpr int kTcBBytes = kTcTok * kTcBK * 2;      // 2 KB
 constexpr int kTcThreads = 192;
 constexpr int kTcPiece = kPiece;
 constexpr int kTcMaxCtas = kMaxCtas;
-constexpr size_t tc_smem(int stages) { return (size_t)stages * (kTcABytes + kTcBBytes) + 1024 + 256; }
+// A stage holds NB 64-k boxes (NB MMAs x 4 per commit).
+constexpr size_t tc_smem(int stages, int nb) {
+    return (size_t)stages * nb * (kTcABytes + kTcBBytes) + 1024 + 256;
+}
 
 struct TcParams {
     CUtensorMap wmap[kMaxSeg];   // per matrix: {K, rows} fp16 / bf16, box {64, 128}
@@ -87,14 +91,15 @@ __device__ __forceinline__ void store_tokens(const TcParams& p, int g, int row, 
 
 }  // namespace
 
-template <bool BF16, int kTcStages>
+template <bool BF16, int kTcStages, int NB>
 __global__ void __launch_bounds__(kTcThreads, 1) k_gemv_tc(const __grid_constant__ TcParams p) {
+    constexpr int kStA = NB * kTcABytes, kStB = NB * kTcBBytes, kBlkK = NB * kTcBK;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     unsigned char* sA = smem;                                   // [stage][128 rows][128 B]
-    unsigned char* sB = smem + kTcStages * kTcABytes;           // [stage][16 tokens][128 B]
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + kTcStages * kTcBBytes);
+    unsigned char* sB = smem + kTcStages * kStA;                // [stage][NB][16 tokens][128 B]
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + kTcStages * kStB);
     uint64_t* empty = full + kTcStages;
     uint64_t* acc_full = empty + kTcStages;                     // [2]
     uint64_t* acc_empty = acc_full + 2;                         // [2]
@@ -131,10 +136,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemv_tc(const __grid_constant
             const int nb = (int)(b1 - b0) < p.prefetch ? (int)(b1 - b0) : p.prefetch;
             int tile = (int)(b0 / nkb), kb = (int)(b0 % nkb), g = seg_of_tile(p, tile);
             for (int n = 0; n < nb; ++n) {
-                asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
-                                 reinterpret_cast<uint64_t>(&p.wmap[g])),
-                             "r"(kb * kTcBK), "r"((tile - p.tile_begin[g]) * kTcRows)
-                             : "memory");
+#pragma unroll
+                for (int b = 0; b < NB; ++b)
+                    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
+                                     reinterpret_cast<uint64_t>(&p.wmap[g])),
+                                 "r"(kb * kBlkK + kTcBK * b), "r"((tile - p.tile_begin[g]) * kTcRows)
+                                 : "memory");
                 if (++kb == nkb) {
                     kb = 0;
                     ++tile;
@@ -164,10 +171,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemv_tc(const __grid_constant
         uint32_t ph = 0;  // parity of the ring's current lap
         for (int n = 0; n < nblk; ++n) {
             if (n >= kTcStages && !mbar_wait(smem_addr(&empty[s]), ph ^ 1u, p.spin, p.err)) break;
-            mbar_expect_tx(smem_addr(&full[s]), kTcABytes + kTcBBytes);
-            tma_load_2d(smem_addr(sA + s * kTcABytes), &p.wmap[g], kb * kTcBK,
-                        (tile - p.tile_begin[g]) * kTcRows, smem_addr(&full[s]));
-            tma_load_2d(smem_addr(sB + s * kTcBBytes), &p.xmap, kb * kTcBK, 0, smem_addr(&full[s]));
+            mbar_expect_tx(smem_addr(&full[s]), kStA + kStB);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                tma_load_2d(smem_addr(sA + s * kStA + b * kTcABytes), &p.wmap[g], kb * kBlkK + kTcBK * b,
+                            (tile - p.tile_begin[g]) * kTcRows, smem_addr(&full[s]));
+                tma_load_2d(smem_addr(sB + s * kStB + b * kTcBBytes), &p.xmap, kb * kBlkK + kTcBK * b, 0,
+                            smem_addr(&full[s]));
+            }
             issued = n + 1;
             if (++kb == nkb) {
                 kb = 0;
@@ -196,11 +207,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemv_tc(const __grid_constant
                 break;
             if (!mbar_wait(smem_addr(&full[s]), ph, p.spin, p.err)) break;
             tc_fence_after();
-            const uint32_t a0 = smem_addr(sA + s * kTcABytes), bb0 = smem_addr(sB + s * kTcBBytes);
+            const uint64_t da = sw128_desc(smem_addr(sA + s * kStA)), db = sw128_desc(smem_addr(sB + s * kStB));
 #pragma unroll
-            for (int kk = 0; kk < kTcBK / 16; ++kk)
-                tc_mma(tmem + (uint32_t)(buf * kTcTok), sw128_desc(a0 + kk * 32),
-                       sw128_desc(bb0 + kk * 32), idesc, (first && kk == 0) ? 0u : 1u);
+            for (int kk = 0; kk < 4 * NB; ++kk)  // box kk / 4, 32 bytes per 16-k step inside it
+                tc_mma(tmem + (uint32_t)(buf * kTcTok),
+                       da + (uint64_t)(((kk >> 2) * kTcABytes + (kk & 3) * 32) >> 4),
+                       db + (uint64_t)(((kk >> 2) * kTcBBytes + (kk & 3) * 32) >> 4), idesc,
+                       (first && kk == 0) ? 0u : 1u);
             tc_commit(smem_addr(&empty[s]));
             if (last) {
                 tc_commit(smem_addr(&acc_full[buf]));
@@ -222,7 +235,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemv_tc(const __grid_constant
         for (int tile = t0; tile <= t1; ++tile) {
             const int si = tile - t0, buf = si & 1;
             float a[16];
-            if (mbar_wait(smem_addr(&acc_full[buf]), (uint32_t)((si / 2) & 1), p.spin, p.err)) {
+            if (mbar_wait_sleep(smem_addr(&acc_full[buf]), (uint32_t)((si / 2) & 1), p.spin, p.err)) {
                 tc_fence_after();
                 tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * kTcTok), a);
             } else {
@@ -385,11 +398,18 @@ cudaError_t smem_attr_once(const void* fn, size_t smem) {
 namespace {
 
 template <bool BF16>
-const void* tc_kernel(int stages) {
+const void* tc_kernel(int stages, int nb) {
+    if (nb == 2) {
+        switch (stages) {
+            case 4: return reinterpret_cast<const void*>(k_gemv_tc<BF16, 4, 2>);
+            case 6: return reinterpret_cast<const void*>(k_gemv_tc<BF16, 6, 2>);
+            default: return reinterpret_cast<const void*>(k_gemv_tc<BF16, 3, 2>);
+        }
+    }
     switch (stages) {
-        case 8: return reinterpret_cast<const void*>(k_gemv_tc<BF16, 8>);
-        case 12: return reinterpret_cast<const void*>(k_gemv_tc<BF16, 12>);
-        default: return reinterpret_cast<const void*>(k_gemv_tc<BF16, 6>);
+        case 8: return reinterpret_cast<const void*>(k_gemv_tc<BF16, 8, 1>);
+        case 12: return reinterpret_cast<const void*>(k_gemv_tc<BF16, 12, 1>);
+        default: return reinterpret_cast<const void*>(k_gemv_tc<BF16, 6, 1>);
     }
 }
 
@@ -406,10 +426,10 @@ bool gemv_tc_supported(const GemvParams& p) {
     return tiles <= kMaxTiles && p.t.nseg <= kMaxSeg && !p.t.pair && !p.t.res;
 }
 
-size_t gemv_tc_smem() { return tc_smem(6); }
+size_t gemv_tc_smem() { return tc_smem(6, 1); }
 
 cudaError_t gemv_tc(const GemvParams& gp, bool bf16, unsigned spin, int grid_req, int stages,
-                    int prefetch, cudaStream_t s, bool* launched) {
+                    int nb, int prefetch, cudaStream_t s, bool* launched) {
     *launched = false;
     Scratch scr;
     if (!scratch(s, &scr)) return cudaSuccess;
@@ -418,7 +438,8 @@ cudaError_t gemv_tc(const GemvParams& gp, bool bf16, unsigned spin, int grid_req
     const int K = gp.a.K;
     p.nseg = gp.t.nseg;
     p.M = gp.a.M;
-    p.nkb = (K + kTcBK - 1) / kTcBK;
+    if (nb != 2) nb = 1;
+    p.nkb = (K + nb * kTcBK - 1) / (nb * kTcBK);
     const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     int tiles = 0;
     for (int g = 0; g < p.nseg; ++g) {
@@ -444,9 +465,9 @@ cudaError_t gemv_tc(const GemvParams& gp, bool bf16, unsigned spin, int grid_req
     if (grid > kTcMaxCtas) grid = kTcMaxCtas;
     if (grid > p.total) grid = p.total;
     if (grid < 1) grid = 1;
-    if (stages != 8 && stages != 12) stages = 6;
-    const void* fn = bf16 ? tc_kernel<true>(stages) : tc_kernel<false>(stages);
-    const size_t smem = tc_smem(stages);
+    if (nb == 2 ? (stages != 4 && stages != 6) : (stages != 8 && stages != 12)) stages = nb == 2 ? 3 : 6;
+    const void* fn = bf16 ? tc_kernel<true>(stages, nb) : tc_kernel<false>(stages, nb);
+    const size_t smem = tc_smem(stages, nb);
     cudaError_t e = smem_attr_once(fn, smem);
     if (e != cudaSuccess) return e;
     void* args[] = {&p};
