@@ -382,14 +382,15 @@ bool scratch(cudaStream_t s, Scratch* out) {
 
 cudaError_t smem_attr_once(const void* fn, size_t smem) {
     static std::mutex mu;
-    static std::map<std::pair<int, const void*>, bool> done;
+    static std::map<std::pair<int, const void*>, size_t> done;  // the largest opt-in set so far
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> g(mu);
-    if (done.count({dev, fn})) return cudaSuccess;
+    auto it = done.find({dev, fn});
+    if (it != done.end() && it->second >= smem) return cudaSuccess;
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) done[{dev, fn}] = true;
+    if (e == cudaSuccess) done[{dev, fn}] = smem;
     return e;
 }
 

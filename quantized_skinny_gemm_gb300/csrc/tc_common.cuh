@@ -168,7 +168,8 @@ struct Scratch {
 };
 bool scratch(cudaStream_t s, Scratch* out);
 
-// The dynamic shared memory opt-in, set once per device and kernel.
+// The dynamic shared memory opt-in of a kernel on this device, raised when a
+// launch needs more than any before.
 cudaError_t smem_attr_once(const void* fn, size_t smem);
 
 }  // namespace tc
