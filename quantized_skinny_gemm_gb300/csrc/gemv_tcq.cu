@@ -17,7 +17,10 @@
 // Sums follow the scalar definitions group by group.  Each group of the int4
 // formats (or each 1024-k run of W8A8, whose fp32 partial sums stay below
 // 2^24 and so are exact integers) accumulates in a TMEM accumulator of its
-// own, from a ring of them; the epilogue warps read it back and apply it:
+// own, from a ring of them; the MMA issuer hands the int4 groups over four
+// at a time (one commit), and the epilogue warps read them back and apply
+// them in ascending k, with the group scales that the TMA producer brought
+// into a shared-memory ring of 8-group windows (128 rows x 16 bytes each):
 //   W4A16:  a = fmaf(P_g, s_g, a),  P_g the fp32 group sum;  y = fp16(a)
 //   W4A8:   a = fmaf(acc_g, s_g, a), acc_g exact;           y = fp16(x_scale * a)
 //   W8A8:   acc += run sum (exact int32);  y = fp16(float(acc) * w_scale * x_scale)
@@ -25,6 +28,13 @@
 // at the granularity of one weight box, and a row tile cut between CTAs is
 // finished by the last of its CTAs to arrive, in CTA order (int32 pieces for
 // W8A8, so the W8A8 sums stay exact whatever the split).
+//
+// Measured: the epilogue used to load its scales from global memory in
+// register windows, whose moves waited on the loads and whose registers
+// spilled; with the shared-memory windows and the batched hand-off a
+// 14336 x 4096 int4 launch at 16 tokens went from 44 to 26 us.  Each 256-k
+// box now moves about 176 KB through shared memory (TMA, converter reads and
+// fp16 writes, MMA operand reads), the bound it works against.
 //
 // CTA roles (14 warps): warp 0 lane 0 TMA producer; warp 1 TMEM owner and (lane
 // 0) MMA issuer; warps 2-5 epilogue (thread <-> weight row, reading TMEM lane
@@ -47,6 +57,10 @@ constexpr int kQEpiWarp0 = 2, kQConvWarp0 = 6;
 constexpr int kQRawA = kRows * 128;     // 16 KB weight box
 constexpr int kQAccSlots = 16;          // TMEM accumulators (16 columns each)
 constexpr int kQRun8 = 1024;            // W8A8: k per exact fp32 run
+constexpr int kQBatch = 4;              // int4: groups per accumulator hand-off, at most
+constexpr int kQScWin = 8;              // int4: groups per scale window (16 bytes of a scale row)
+constexpr int kQScSlots = 8;            // int4: scale windows in the shared-memory ring
+constexpr int kQScBytes = kRows * 2 * kQScWin;  // one window for the 128 rows of a tile: 2 KB
 
 template <int F>
 struct QTraits {
@@ -60,14 +74,16 @@ struct QTraits {
     static constexpr int kStage = kQRawA + kRawB;
     static constexpr int kStages = kInt4 ? 3 : 4;          // raw ring
     static constexpr int kTmemCols = kQAccSlots * kTok;    // accumulators only
+    static constexpr int kScRing = kInt4 ? kQScSlots * kQScBytes : 0;
     static size_t smem() {
-        return (size_t)kStages * kStage + 2 * (size_t)(kWideA + kConvB) + 1024 + 512;
+        return (size_t)kStages * kStage + 2 * (size_t)(kWideA + kConvB) + kScRing + 1024 + 1024;
     }
 };
 
 struct TcqParams {
     CUtensorMap wmap[kMaxSeg];   // per matrix: bytes {K bytes, rows}, box {128, 128}, 128B swizzle
     CUtensorMap xmap;            // W4A16: fp16 {K, M} box {64, 16} swizzled; else int8 {K, M} box {KS, 16}
+    CUtensorMap smap[kMaxSeg];   // int4: fp16 scales {K / group, rows}, box {8 groups, 128 rows}
     void* y[kMaxSeg];            // fp16 [M][rows]
     int32_t* acc_out[kMaxSeg];   // W8A8, optional [M][rows]
     const void* scale[kMaxSeg];  // int4: fp16 [rows][K / group]; W8A8: float [rows]
@@ -129,17 +145,26 @@ __global__ void __launch_bounds__(kQThreads, 1) k_gemv_tcq(const __grid_constant
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     constexpr int kQStages = T::kStages;
+    constexpr int kSteps = T::KS / 16;  // MMAs per weight box
+    // Accumulator batches: the int4 formats hand kB groups (kB adjacent
+    // 16-column accumulators, one commit, one TMEM load) to the epilogue at a
+    // time; W8A8 one 1024-k run.  kNB batches fill the accumulator ring.
+    constexpr int kB = T::kInt4 ? (kSteps / RS < kQBatch ? kSteps / RS : kQBatch) : 1;
+    constexpr int kNB = kQAccSlots / kB;
     unsigned char* wideA = smem;                                 // [2][kAtoms][128 rows][128 B]
     unsigned char* convB = wideA + 2 * T::kWideA;                // [2][kAtoms][16][128 B]
     unsigned char* ring = convB + 2 * T::kConvB;                 // [stage]{A box, B box}
-    uint64_t* full = reinterpret_cast<uint64_t*>(ring + kQStages * T::kStage);
+    unsigned char* scring = ring + kQStages * T::kStage;         // int4: [kQScSlots][128 rows][8 groups] fp16
+    uint64_t* full = reinterpret_cast<uint64_t*>(scring + T::kScRing);
     uint64_t* empty = full + kQStages;
     uint64_t* a_full = empty + kQStages;       // [2]
     uint64_t* a_empty = a_full + 2;            // [2]
     uint64_t* acc_full = a_empty + 2;          // [kQAccSlots]
     uint64_t* acc_empty = acc_full + kQAccSlots;
     uint64_t* mma_done = acc_empty + kQAccSlots;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    uint64_t* sc_full = mma_done + 1;          // [kQScSlots]
+    uint64_t* sc_empty = sc_full + kQScSlots;  // [kQScSlots]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sc_empty + kQScSlots);
     int* last_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -151,9 +176,13 @@ __global__ void __launch_bounds__(kQThreads, 1) k_gemv_tcq(const __grid_constant
 
     griddep_launch_dependents();
     if (threadIdx.x == 0) {
-        for (int g = 0; g < p.nseg; ++g)
+        for (int g = 0; g < p.nseg; ++g) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.wmap[g]))
                          : "memory");
+            if (T::kInt4)
+                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.smap[g]))
+                             : "memory");
+        }
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.xmap))
                      : "memory");
         for (int i = 0; i < kQStages; ++i) {
@@ -169,6 +198,10 @@ __global__ void __launch_bounds__(kQThreads, 1) k_gemv_tcq(const __grid_constant
             mbar_init(smem_addr(&acc_empty[i]), 128);
         }
         mbar_init(smem_addr(mma_done), 1);
+        for (int i = 0; i < kQScSlots; ++i) {
+            mbar_init(smem_addr(&sc_full[i]), 1);
+            mbar_init(smem_addr(&sc_empty[i]), 128);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -189,8 +222,20 @@ __global__ void __launch_bounds__(kQThreads, 1) k_gemv_tcq(const __grid_constant
     if (warp == 0 && lane == 0) {
         // ---- TMA producer ----
         int tile = t0, kb = kb_first, g = q_seg_of_tile(p, t0), s = 0, issued = 0;
+        int sc_u = 0;  // int4: scale windows issued
         uint32_t ph = 0;
         for (int n = 0; n < nblk; ++n) {
+            if (T::kInt4 && (n == 0 || ((kb * (kSteps / RS)) % kQScWin) == 0)) {
+                // the 8-group scale window holding this box's groups, for the epilogue
+                const int sl = sc_u % kQScSlots;
+                if (sc_u >= kQScSlots &&
+                    !mbar_wait(smem_addr(&sc_empty[sl]), (uint32_t)(((sc_u / kQScSlots) & 1) ^ 1), p.spin, p.err))
+                    break;
+                mbar_expect_tx(smem_addr(&sc_full[sl]), kQScBytes);
+                tma_load_2d(smem_addr(scring + sl * kQScBytes), &p.smap[g], (kb * (kSteps / RS)) & ~(kQScWin - 1),
+                            (tile - p.tile_begin[g]) * kRows, smem_addr(&sc_full[sl]));
+                ++sc_u;
+            }
             if (n >= kQStages && !mbar_wait(smem_addr(&empty[s]), ph ^ 1u, p.spin, p.err)) break;
             unsigned char* st = ring + s * T::kStage;
             mbar_expect_tx(smem_addr(&full[s]), kQRawA + T::kRawB);
@@ -217,11 +262,12 @@ __global__ void __launch_bounds__(kQThreads, 1) k_gemv_tcq(const __grid_constant
         }
         for (int j = issued > kQStages ? issued - kQStages : 0; j < issued; ++j)
             mbar_wait(smem_addr(&full[j % kQStages]), (uint32_t)((j / kQStages) & 1), p.spin, p.err);
+        for (int j = sc_u > kQScSlots ? sc_u - kQScSlots : 0; j < sc_u; ++j)
+            mbar_wait(smem_addr(&sc_full[j % kQScSlots]), (uint32_t)((j / kQScSlots) & 1), p.spin, p.err);
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer: A and B from shared memory ----
         constexpr uint32_t idesc = idesc_f16<false>();
-        constexpr int kSteps = T::KS / 16;  // MMAs per weight box
-        int kb = kb_first, s = 0, acc_i = 0;
+        int kb = kb_first, s = 0, acc_i = 0;  // acc_i: accumulator batches issued
         int run_left = 0;  // W8A8: k left in the current run (0: start a new one)
         uint32_t ph = 0;
         bool ok = true;
@@ -236,24 +282,29 @@ __global__ void __launch_bounds__(kQThreads, 1) k_gemv_tcq(const __grid_constant
                                                        : smem_addr(convB + r * T::kConvB));
             // k step j: A at atom j / 4 (16 KB apart), B at atom j / 4 (2 KB apart),
             // 32 bytes per step inside an atom (descriptor addresses count 16 bytes)
-            if (T::kInt4) {  // RS steps per group: every box holds whole groups
+            if (T::kInt4) {  // RS steps per group, kB groups per batch: boxes hold whole batches
 #pragma unroll
-                for (int rr = 0; rr < kSteps / RS; ++rr) {
-                    if (acc_i >= kQAccSlots &&
-                        !mbar_wait(smem_addr(&acc_empty[acc_i % kQAccSlots]),
-                                   (uint32_t)((acc_i / kQAccSlots - 1) & 1), p.spin, p.err)) {
+                for (int bb = 0; bb < kSteps / (RS * kB); ++bb) {
+                    if (acc_i >= kNB &&
+                        !mbar_wait(smem_addr(&acc_empty[acc_i % kNB]), (uint32_t)((acc_i / kNB - 1) & 1),
+                                   p.spin, p.err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d = tmem + (uint32_t)((acc_i % kQAccSlots) * kTok);
+                    const uint32_t d0 = tmem + (uint32_t)((acc_i % kNB) * kB * kTok);
 #pragma unroll
-                    for (int jj = 0; jj < RS; ++jj) {
-                        const int j = rr * RS + jj;
-                        tc_mma(d, da + (uint64_t)(((j >> 2) * (kRows * 128) + (j & 3) * 32) >> 4),
-                               db + (uint64_t)(((j >> 2) * 2048 + (j & 3) * 32) >> 4), idesc, jj ? 1u : 0u);
+                    for (int gg = 0; gg < kB; ++gg) {
+#pragma unroll
+                        for (int jj = 0; jj < RS; ++jj) {
+                            const int j = (bb * kB + gg) * RS + jj;
+                            tc_mma(d0 + (uint32_t)(gg * kTok),
+                                   da + (uint64_t)(((j >> 2) * (kRows * 128) + (j & 3) * 32) >> 4),
+                                   db + (uint64_t)(((j >> 2) * 2048 + (j & 3) * 32) >> 4), idesc,
+                                   jj ? 1u : 0u);
+                        }
                     }
-                    tc_commit(smem_addr(&acc_full[acc_i % kQAccSlots]));
+                    tc_commit(smem_addr(&acc_full[acc_i % kNB]));
                     ++acc_i;
                 }
                 if (!ok) break;
@@ -261,15 +312,15 @@ __global__ void __launch_bounds__(kQThreads, 1) k_gemv_tcq(const __grid_constant
                 if (piece_first) run_left = 0;
                 uint32_t fresh = 0;
                 if (run_left == 0) {
-                    if (acc_i >= kQAccSlots &&
-                        !mbar_wait(smem_addr(&acc_empty[acc_i % kQAccSlots]),
-                                   (uint32_t)((acc_i / kQAccSlots - 1) & 1), p.spin, p.err))
+                    if (acc_i >= kNB &&
+                        !mbar_wait(smem_addr(&acc_empty[acc_i % kNB]), (uint32_t)((acc_i / kNB - 1) & 1),
+                                   p.spin, p.err))
                         break;
                     tc_fence_after();
                     run_left = p.seg_k - ((kb * T::KS) & (p.seg_k - 1));
                     fresh = 1;
                 }
-                const uint32_t d = tmem + (uint32_t)((acc_i % kQAccSlots) * kTok);
+                const uint32_t d = tmem + (uint32_t)((acc_i % kNB) * kTok);
 #pragma unroll
                 for (int j = 0; j < kSteps; ++j)
                     tc_mma(d, da + (uint64_t)(((j >> 2) * (kRows * 128) + (j & 3) * 32) >> 4),
@@ -277,7 +328,7 @@ __global__ void __launch_bounds__(kQThreads, 1) k_gemv_tcq(const __grid_constant
                            (fresh && j == 0) ? 0u : 1u);
                 run_left -= T::KS;
                 if (run_left == 0 || piece_last) {
-                    tc_commit(smem_addr(&acc_full[acc_i % kQAccSlots]));
+                    tc_commit(smem_addr(&acc_full[acc_i % kNB]));
                     ++acc_i;
                     run_left = 0;
                 }
@@ -366,6 +417,9 @@ __global__ void __launch_bounds__(kQThreads, 1) k_gemv_tcq(const __grid_constant
         const int rl = 32 * q + lane;
         const int t1 = (int)((b1 - 1) / nkb);
         int acc_i = 0;
+        // int4 scales: the producer's 8-group windows, in the order it issued them
+        int sc_u = 0;
+        uint4 swin = make_uint4(0, 0, 0, 0);
         for (int tile = t0; tile <= t1; ++tile) {
             const long long tb = (long long)tile * nkb, te = tb + nkb;
             const long long pb = tb > b0 ? tb : b0, pe = te < b1 ? te : b1;  // this CTA's piece
@@ -381,53 +435,67 @@ __global__ void __launch_bounds__(kQThreads, 1) k_gemv_tcq(const __grid_constant
             }
             // the piece's runs, in the MMA issuer's order
             const int k_lo = (int)(pb - tb) * T::KS, k_hi = (int)(pe - tb) * T::KS;
-            // int4 scales: 16-byte windows of 8 groups, four windows in flight
-            const uint16_t* srow = static_cast<const uint16_t*>(p.scale[g]) +
-                                   (size_t)(live ? row : (tile - p.tile_begin[g]) * kRows) * p.ngroups;
-            uint4 win0 = make_uint4(0, 0, 0, 0), win1 = win0, win2 = win0, win3 = win0;
-            int wbase = 0;
-            auto load_win = [&](int w) -> uint4 {
-                return (T::kInt4 && w * 8 < p.ngroups) ? ld_nc16(srow + 8 * w) : make_uint4(0, 0, 0, 0);
-            };
-            if (T::kInt4) {
-                wbase = (k_lo / p.seg_k) >> 3;
-                win0 = load_win(wbase);
-                win1 = load_win(wbase + 1);
-                win2 = load_win(wbase + 2);
-                win3 = load_win(wbase + 3);
-            }
+            // one batch per pass: kB groups (int4; k stays a multiple of kB groups,
+            // as every piece is whole boxes) or one W8A8 run
             for (int k = k_lo; k < k_hi;) {
-                const int k_end = min(k_hi, (k / p.seg_k + 1) * p.seg_k);
-                const int slot = acc_i % kQAccSlots;
-                float v[16];
-                if (mbar_wait_sleep(smem_addr(&acc_full[slot]), (uint32_t)((acc_i / kQAccSlots) & 1), p.spin, p.err)) {
-                    tc_fence_after();
-                    tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(slot * kTok), v);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] = 0.f;
-                }
-                tc_fence_before();
-                mbar_arrive(smem_addr(&acc_empty[slot]));
-                ++acc_i;
+                const int k_end = min(k_hi, (k / p.seg_k + kB) * p.seg_k);
+                const int slot = acc_i % kNB;
+                int gi0 = 0;
                 if (T::kInt4) {
-                    const int gi = k / p.seg_k;
-                    while ((gi >> 3) > wbase) {
-                        win0 = win1;
-                        win1 = win2;
-                        win2 = win3;
-                        win3 = load_win(wbase + 4);
-                        ++wbase;
+                    gi0 = k / p.seg_k;
+                    if (sc_u == 0 || (gi0 & (kQScWin - 1)) == 0) {  // the batch opens a window
+                        if (sc_u > 0) mbar_arrive(smem_addr(&sc_empty[(sc_u - 1) % kQScSlots]));
+                        const int sl = sc_u % kQScSlots;
+                        if (mbar_wait_sleep(smem_addr(&sc_full[sl]), (uint32_t)((sc_u / kQScSlots) & 1), p.spin,
+                                            p.err))
+                            swin = *reinterpret_cast<const uint4*>(scring + sl * kQScBytes + rl * 16);
+                        else
+                            swin = make_uint4(0, 0, 0, 0);
+                        ++sc_u;
                     }
-                    const int e = gi & 7;
-                    const uint32_t wd = (e >> 1) == 0 ? win0.x : (e >> 1) == 1 ? win0.y : (e >> 1) == 2 ? win0.z : win0.w;
-                    const float sg = __half2float(__ushort_as_half((uint16_t)((e & 1) ? wd >> 16 : wd)));
-#pragma unroll
-                    for (int m = 0; m < kTok; ++m) a[m] = fmaf(v[m], sg, a[m]);
-                } else {
-#pragma unroll
-                    for (int m = 0; m < kTok; ++m) ai[m] += __float2int_rn(v[m]);
                 }
+                const bool got =
+                    mbar_wait_sleep(smem_addr(&acc_full[slot]), (uint32_t)((acc_i / kNB) & 1), p.spin, p.err);
+                if (got) tc_fence_after();
+                // kH groups per TMEM read (32 registers at most), the slot released
+                // after the last read
+                constexpr int kH = kB > 2 ? 2 : kB;
+#pragma unroll
+                for (int h = 0; h < kB; h += kH) {
+                    uint32_t v[kH][16];
+                    if (got) {
+#pragma unroll
+                        for (int gg = 0; gg < kH; ++gg)
+                            tmem_ld16_async(tmem + ((uint32_t)(32 * q) << 16) +
+                                                (uint32_t)((slot * kB + h + gg) * kTok),
+                                            v[gg]);
+#pragma unroll
+                        for (int gg = 0; gg < kH; ++gg) tmem_ld_wait(v[gg]);
+                    } else {
+#pragma unroll
+                        for (int gg = 0; gg < kH; ++gg)
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) v[gg][j] = 0u;
+                    }
+                    if (h + kH == kB) {
+                        tc_fence_before();
+                        mbar_arrive(smem_addr(&acc_empty[slot]));
+                    }
+                    if (T::kInt4) {
+#pragma unroll
+                        for (int gg = 0; gg < kH; ++gg) {  // groups in ascending k
+                            const int e = (gi0 + h + gg) & (kQScWin - 1);
+                            const uint32_t wd = (e >> 1) == 0 ? swin.x : (e >> 1) == 1 ? swin.y : (e >> 1) == 2 ? swin.z : swin.w;
+                            const float sg = __half2float(__ushort_as_half((uint16_t)((e & 1) ? wd >> 16 : wd)));
+#pragma unroll
+                            for (int m = 0; m < kTok; ++m) a[m] = fmaf(__uint_as_float(v[gg][m]), sg, a[m]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int m = 0; m < kTok; ++m) ai[m] += __float2int_rn(__uint_as_float(v[0][m]));
+                    }
+                }
+                ++acc_i;
                 k = k_end;
             }
             const bool whole = b0 <= tb && b1 >= te;
@@ -599,6 +667,9 @@ cudaError_t gemv_tcq(const GemvParams& gp, Fmt f, unsigned spin, int grid_req, c
         const Segment& sg = gp.t.seg[g];
         if (!encode_2d(&p.wmap[g], sg.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, row_bytes, sg.rows, 128,
                        kRows, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaSuccess;
+        if (F != Q_W8A8 && !encode_2d(&p.smap[g], sg.scale, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, K / gp.group,
+                                      sg.rows, kQScWin, kRows, CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaSuccess;
         p.y[g] = sg.y;
         p.acc_out[g] = sg.acc_out;
