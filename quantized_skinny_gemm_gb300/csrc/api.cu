@@ -424,11 +424,12 @@ static dg_status launch_tc(const GemvParams& p, bool bf16, cudaStream_t s, bool*
     *launched = false;
     if (!gemv_tc_supported(p)) return DG_OK;
     const unsigned spin = tune().SPIN > 0 ? (unsigned)tune().SPIN : 4000000u;
-    // L2 prefetch of the first weight boxes pays off while the previous launch's
-    // tail leaves DRAM idle, for launches short enough that the tail matters
+    // L2 prefetch of each CTA's first weight boxes pays off while the previous
+    // launch's tail leaves DRAM idle (measured on a 117 MB launch at 16 tokens:
+    // 25.2 us without, 24.9 with 6 boxes, 24.5 with 12, 26.1 with 24)
     size_t bytes = 0;
     for (int g = 0; g < p.t.nseg; ++g) bytes += (size_t)p.t.seg[g].rows * p.a.K * 2;
-    const int prefetch = tune().TP >= 0 ? tune().TP : bytes <= ((size_t)64 << 20) ? 6 : 0;
+    const int prefetch = tune().TP >= 0 ? tune().TP : bytes <= ((size_t)64 << 20) ? 6 : 12;
     // two 64-k boxes per stage, four stages (measured best of 6x1, 8x1, 12x1, 3x2, 4x2, 6x2)
     const int nb = tune().TK == 1 ? 1 : 2;
     const int stages = tune().TS > 0 ? tune().TS : nb == 2 ? 4 : 6;

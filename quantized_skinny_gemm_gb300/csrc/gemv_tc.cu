@@ -14,7 +14,12 @@
 // range covers whole is rounded and stored by the CTA itself; a tile cut
 // between CTAs is finished by whichever of its CTAs arrives last, which adds
 // the pieces' fp32 partial sums in CTA order (so the result does not depend on
-// arrival order).  No CTA ever waits for another one.
+// arrival order).  No CTA ever waits for another one.  A CTA whose range ends
+// inside a tile processes that tile first, so the pieces of a cut tile are
+// published early and the CTA holding its last k block, which takes that
+// piece last, usually finds them all there: one acquire load tells it so, and
+// it finishes the tile without publishing its own piece (measured on a
+// 14336 x 4096 launch at 16 tokens: 26.3 -> 25.2 us).
 //
 // CTA roles (6 warps): warp 0 lane 0 issues TMA loads into a ring of stages of
 // NB 64-k boxes (16 KB of weights + 2 KB of tokens per box, 128-byte swizzle;
@@ -71,6 +76,27 @@ __device__ __forceinline__ int seg_of_tile(const TcParams& p, int tile) {
     while (g + 1 < p.nseg && tile >= p.tile_begin[g + 1]) ++g;
     return g;
 }
+
+// This CTA's tiles in processing order.  A range that ends inside a tile
+// takes that tile first: its piece is the start of the tile, whose other
+// pieces belong to later CTAs, and those take their cut tile ends last; so the
+// pieces of a cut tile are published early, and its last piece (whose CTA
+// finishes the tile when it finds all the others there) ends the range.
+struct TileOrder {
+    int t0, t1, kb_first, kb_end, nkb;  // kb_end: one past the last k block of t1
+    bool rot;
+    __device__ TileOrder(long long b0, long long b1, int nkb_) : nkb(nkb_) {
+        t0 = (int)(b0 / nkb);
+        kb_first = (int)(b0 % nkb);
+        t1 = (int)((b1 - 1) / nkb);
+        kb_end = (int)((b1 - 1) % nkb) + 1;
+        rot = t1 > t0 && kb_end < nkb;
+    }
+    __device__ int count() const { return t1 - t0 + 1; }
+    __device__ int tile(int i) const { return rot ? (i == 0 ? t1 : t0 + i - 1) : t0 + i; }
+    __device__ int kb_lo(int t) const { return t == t0 ? kb_first : 0; }
+    __device__ int kb_hi(int t) const { return t == t1 ? kb_end : nkb; }
+};
 
 template <bool BF16>
 __device__ __forceinline__ void store_tokens(const TcParams& p, int g, int row, const float (&a)[16]) {
@@ -133,19 +159,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemv_tc(const __grid_constant
         // warm L2 with this CTA's first weight boxes while the previous launch
         // drains (a prefetch never changes what a later load returns)
         if (p.prefetch) {
-            const int nb = (int)(b1 - b0) < p.prefetch ? (int)(b1 - b0) : p.prefetch;
-            int tile = (int)(b0 / nkb), kb = (int)(b0 % nkb), g = seg_of_tile(p, tile);
-            for (int n = 0; n < nb; ++n) {
+            const TileOrder ord(b0, b1, nkb);
+            int n = 0;
+            for (int i = 0; i < ord.count() && n < p.prefetch; ++i) {
+                const int tile = ord.tile(i), g = seg_of_tile(p, tile);
+                for (int kb = ord.kb_lo(tile); kb < ord.kb_hi(tile) && n < p.prefetch; ++kb, ++n) {
 #pragma unroll
-                for (int b = 0; b < NB; ++b)
-                    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
-                                     reinterpret_cast<uint64_t>(&p.wmap[g])),
-                                 "r"(kb * kBlkK + kTcBK * b), "r"((tile - p.tile_begin[g]) * kTcRows)
-                                 : "memory");
-                if (++kb == nkb) {
-                    kb = 0;
-                    ++tile;
-                    if (g + 1 < p.nseg && tile >= p.tile_begin[g + 1]) ++g;
+                    for (int b = 0; b < NB; ++b)
+                        asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
+                                         reinterpret_cast<uint64_t>(&p.wmap[g])),
+                                     "r"(kb * kBlkK + kTcBK * b), "r"((tile - p.tile_begin[g]) * kTcRows)
+                                     : "memory");
                 }
             }
         }
@@ -163,31 +187,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemv_tc(const __grid_constant
     const uint32_t tmem = *tmem_slot;
     griddep_wait();  // the tokens (and the outputs) belong to the previous launch until here
 
-    const int nblk = (int)(b1 - b0);          // k blocks of this CTA
-    const int t0 = (int)(b0 / nkb), kb_first = (int)(b0 % nkb);
+    const TileOrder ord(b0, b1, nkb);
     if (warp == 0 && lane == 0) {
         // ---- TMA producer ----
-        int tile = t0, kb = kb_first, g = seg_of_tile(p, t0), s = 0, issued = 0;
+        int s = 0, issued = 0;
         uint32_t ph = 0;  // parity of the ring's current lap
-        for (int n = 0; n < nblk; ++n) {
-            if (n >= kTcStages && !mbar_wait(smem_addr(&empty[s]), ph ^ 1u, p.spin, p.err)) break;
-            mbar_expect_tx(smem_addr(&full[s]), kStA + kStB);
+        bool ok = true;
+        for (int i = 0; i < ord.count() && ok; ++i) {
+            const int tile = ord.tile(i), g = seg_of_tile(p, tile);
+            for (int kb = ord.kb_lo(tile); kb < ord.kb_hi(tile); ++kb) {
+                if (issued >= kTcStages && !mbar_wait(smem_addr(&empty[s]), ph ^ 1u, p.spin, p.err)) {
+                    ok = false;
+                    break;
+                }
+                mbar_expect_tx(smem_addr(&full[s]), kStA + kStB);
 #pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                tma_load_2d(smem_addr(sA + s * kStA + b * kTcABytes), &p.wmap[g], kb * kBlkK + kTcBK * b,
-                            (tile - p.tile_begin[g]) * kTcRows, smem_addr(&full[s]));
-                tma_load_2d(smem_addr(sB + s * kStB + b * kTcBBytes), &p.xmap, kb * kBlkK + kTcBK * b, 0,
-                            smem_addr(&full[s]));
-            }
-            issued = n + 1;
-            if (++kb == nkb) {
-                kb = 0;
-                ++tile;
-                if (g + 1 < p.nseg && tile >= p.tile_begin[g + 1]) ++g;
-            }
-            if (++s == kTcStages) {
-                s = 0;
-                ph ^= 1u;
+                for (int b = 0; b < NB; ++b) {
+                    tma_load_2d(smem_addr(sA + s * kStA + b * kTcABytes), &p.wmap[g], kb * kBlkK + kTcBK * b,
+                                (tile - p.tile_begin[g]) * kTcRows, smem_addr(&full[s]));
+                    tma_load_2d(smem_addr(sB + s * kStB + b * kTcBBytes), &p.xmap, kb * kBlkK + kTcBK * b, 0,
+                                smem_addr(&full[s]));
+                }
+                ++issued;
+                if (++s == kTcStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
         }
         // the copies still in flight land before the CTA can leave
@@ -196,33 +221,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemv_tc(const __grid_constant
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer ----
         constexpr uint32_t idesc = idesc_f16<BF16>();
-        int kb = kb_first, s = 0, seg_i = 0;  // seg_i: tiles started by this CTA
+        int s = 0;
         uint32_t ph = 0;
-        for (int n = 0; n < nblk; ++n) {
-            const bool first = n == 0 || kb == 0;
-            const bool last = n == nblk - 1 || kb == nkb - 1;
-            const int buf = seg_i & 1;
-            if (first && seg_i >= 2 &&
-                !mbar_wait(smem_addr(&acc_empty[buf]), (uint32_t)((seg_i / 2 - 1) & 1), p.spin, p.err))
+        bool ok = true;
+        for (int i = 0; i < ord.count() && ok; ++i) {  // i: tiles started by this CTA
+            const int tile = ord.tile(i), buf = i & 1;
+            const int lo = ord.kb_lo(tile), hi = ord.kb_hi(tile);
+            if (i >= 2 && !mbar_wait(smem_addr(&acc_empty[buf]), (uint32_t)((i / 2 - 1) & 1), p.spin, p.err))
                 break;
-            if (!mbar_wait(smem_addr(&full[s]), ph, p.spin, p.err)) break;
-            tc_fence_after();
-            const uint64_t da = sw128_desc(smem_addr(sA + s * kStA)), db = sw128_desc(smem_addr(sB + s * kStB));
+            for (int kb = lo; kb < hi; ++kb) {
+                if (!mbar_wait(smem_addr(&full[s]), ph, p.spin, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t da = sw128_desc(smem_addr(sA + s * kStA)), db = sw128_desc(smem_addr(sB + s * kStB));
 #pragma unroll
-            for (int kk = 0; kk < 4 * NB; ++kk)  // box kk / 4, 32 bytes per 16-k step inside it
-                tc_mma(tmem + (uint32_t)(buf * kTcTok),
-                       da + (uint64_t)(((kk >> 2) * kTcABytes + (kk & 3) * 32) >> 4),
-                       db + (uint64_t)(((kk >> 2) * kTcBBytes + (kk & 3) * 32) >> 4), idesc,
-                       (first && kk == 0) ? 0u : 1u);
-            tc_commit(smem_addr(&empty[s]));
-            if (last) {
-                tc_commit(smem_addr(&acc_full[buf]));
-                ++seg_i;
-            }
-            if (++kb == nkb) kb = 0;
-            if (++s == kTcStages) {
-                s = 0;
-                ph ^= 1u;
+                for (int kk = 0; kk < 4 * NB; ++kk)  // box kk / 4, 32 bytes per 16-k step inside it
+                    tc_mma(tmem + (uint32_t)(buf * kTcTok),
+                           da + (uint64_t)(((kk >> 2) * kTcABytes + (kk & 3) * 32) >> 4),
+                           db + (uint64_t)(((kk >> 2) * kTcBBytes + (kk & 3) * 32) >> 4), idesc,
+                           (kb == lo && kk == 0) ? 0u : 1u);
+                tc_commit(smem_addr(&empty[s]));
+                if (kb == hi - 1) tc_commit(smem_addr(&acc_full[buf]));
+                if (++s == kTcStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
         }
         tc_commit(smem_addr(mma_done));
@@ -231,11 +256,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemv_tc(const __grid_constant
         // ---- epilogue: 128 threads, thread <-> weight row of the tile ----
         const int q = warp & 3;                 // TMEM lanes 32q .. 32q + 31
         const int rl = 32 * q + lane;           // row within the tile
-        const int t1 = (int)((b1 - 1) / nkb);
-        for (int tile = t0; tile <= t1; ++tile) {
-            const int si = tile - t0, buf = si & 1;
+        for (int i = 0; i < ord.count(); ++i) {
+            const int tile = ord.tile(i), buf = i & 1;
             float a[16];
-            if (mbar_wait_sleep(smem_addr(&acc_full[buf]), (uint32_t)((si / 2) & 1), p.spin, p.err)) {
+            if (mbar_wait_sleep(smem_addr(&acc_full[buf]), (uint32_t)((i / 2) & 1), p.spin, p.err)) {
                 tc_fence_after();
                 tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * kTcTok), a);
             } else {
@@ -251,35 +275,66 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemv_tc(const __grid_constant
                 store_tokens<BF16>(p, g, row, a);
                 continue;
             }
-            // a piece of a tile shared with other CTAs: publish it (one release
+            // A piece of a tile shared with other CTAs.  The CTA holding the
+            // tile's last k block first looks whether every other piece has
+            // arrived (one acquire load); if so it finishes the tile without
+            // publishing its own.  Otherwise it publishes its piece (one release
             // by one thread after the epilogue's barrier covers the 128 threads'
-            // stores), and the last of the tile's CTAs to arrive sums the pieces
-            // in CTA order
-            float4* dst = reinterpret_cast<float4*>(
-                p.part + ((size_t)(2 * c + (si == 0 ? 0 : 1)) * kTcPiece + (size_t)rl * kTcTok));
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                __stcg(dst + j, make_float4(a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3]));
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            // stores) and the last of the tile's CTAs to arrive finishes it.
+            // Either way the pieces are added in CTA order.
             const int fc = cta_of_block(tb, p.total, G), lc = cta_of_block(te - 1, p.total, G);
+            asm volatile("bar.sync 1, 128;" ::: "memory");  // every thread has read the last flag
             if (threadIdx.x == 64) {
-                unsigned old;
-                asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
-                             : "=r"(old)
-                             : "l"(p.count + tile)
-                             : "memory");
-                *last_flag = old == (unsigned)(lc - fc) ? 1 : 0;
+                int mode = 0;
+                if (b1 >= te) {
+                    unsigned arrived;
+                    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];"
+                                 : "=r"(arrived)
+                                 : "l"(p.count + tile)
+                                 : "memory");
+                    mode = arrived == (unsigned)(lc - fc) ? 2 : 0;
+                }
+                *last_flag = mode;
             }
             asm volatile("bar.sync 1, 128;" ::: "memory");
-            if (*last_flag) {
+            int mode = *last_flag;
+            if (mode == 0) {
+                float4* dst = reinterpret_cast<float4*>(
+                    p.part + ((size_t)(2 * c + (tile == ord.t0 ? 0 : 1)) * kTcPiece + (size_t)rl * kTcTok));
 #pragma unroll
-                for (int j = 0; j < 16; ++j) a[j] = 0.f;
+                for (int j = 0; j < 4; ++j)
+                    __stcg(dst + j, make_float4(a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3]));
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (threadIdx.x == 64) {
+                    unsigned old;
+                    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
+                                 : "=r"(old)
+                                 : "l"(p.count + tile)
+                                 : "memory");
+                    *last_flag = old == (unsigned)(lc - fc) ? 1 : 0;
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                mode = *last_flag;
+            }
+            if (mode) {
+                float own[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    own[j] = a[j];
+                    a[j] = 0.f;
+                }
                 for (int c0 = fc; c0 <= lc; c0 += 4) {  // four pieces in flight at a time
                     float4 v[4][4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int cc = c0 + u;
                         if (cc > lc) break;
+                        if (cc == (int)c) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                v[u][j] = make_float4(own[4 * j], own[4 * j + 1], own[4 * j + 2], own[4 * j + 3]);
+                            continue;
+                        }
                         const int first_tile = (int)(range_begin(cc, p.total, G) / nkb);
                         const float4* src = reinterpret_cast<const float4*>(
                             p.part + ((size_t)(2 * cc + (tile == first_tile ? 0 : 1)) * kTcPiece +
