@@ -322,11 +322,21 @@ __global__ void __launch_bounds__(NW * 32, 1)
             {
                 const int first = r0 + rg * R;
                 const RowRef f = active ? locate_step<EPI>(ph, first, g.rb) : RowRef{};
+                // the group's rows in the first row's matrix (segments are
+                // contiguous; SwiGLU pairs interleave two): the next rows of it
+                const bool one_seg = !(EPI && ph.pair) && f.local + R <= f.seg_rows;
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     const int gr = first + r;
                     if (active && gr < r1) {
-                        rows[r] = locate_step<EPI>(ph, gr, g.rb);
+                        if (one_seg) {
+                            rows[r] = f;
+                            rows[r].w = f.w + (size_t)r * g.rb;
+                            rows[r].local = f.local + r;
+                            rows[r].global = gr;
+                        } else {
+                            rows[r] = locate_step<EPI>(ph, gr, g.rb);
+                        }
                     } else {
                         rows[r] = f;
                         rows[r].valid = false;
