@@ -546,14 +546,24 @@ __device__ __forceinline__ RowGeom row_geom(int K, int group, int ks) {
 
 // Fills rows[] for row group rg of table t; invalid rows alias the first row
 // (loaded but dropped) so every load stays in bounds.
+// When the group's rows all lie in the first row's matrix (segments are
+// contiguous; SwiGLU pairs interleave two), the next rows follow from it.
 template <int R>
 __device__ __forceinline__ void rows_of(const SegTable& t, int rg, bool active, size_t rb,
                                         RowRef (&rows)[R]) {
     RowRef z{};
     const RowRef first = active ? locate(t, rg * R, rb, z) : z;
+    const bool one_seg = R > 1 && active && first.valid && !t.pair && first.local + R <= first.seg_rows;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-        rows[r] = active ? locate(t, rg * R + r, rb, first) : first;
+        if (one_seg) {
+            rows[r] = first;
+            rows[r].w = first.w + (size_t)r * rb;
+            rows[r].local = first.local + r;
+            rows[r].global = first.global + r;
+        } else {
+            rows[r] = active ? locate(t, rg * R + r, rb, first) : first;
+        }
         if (!rows[r].valid) rows[r].w = first.w;
     }
 }
