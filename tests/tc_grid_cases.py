@@ -45,3 +45,30 @@ def test_forced_grid_against_the_oracle(N, K, M, dtype):
     assert torch.all(buf[M] == 3.0)
     yr, A = oracle.gemv_fp(bits(W), bits(x), _fmt(dtype))
     tol.assert_close(y.float().cpu().double().numpy(), yr, A, _fmt(dtype), "grid %dx%d M=%d" % (N, K, M))
+
+
+@pytest.mark.parametrize("M", [8, 16])
+def test_forced_grid_fused_segments(M):
+    """q|k|v as one launch of three matrices (tiles never straddle two) under
+    the forced grid, through the per-group path of dg_decode_step_weights."""
+    need_gpu()
+    K = 2048
+    Ns = (2048, 256, 384)
+    g = synth.generator(90 + M)
+    Ws = [synth.normal((n, K), synth.W_STD, g) for n in Ns]
+    x = synth.normal((M, K), 1.0, g)
+    xd = x.to(DEV)
+    ys = [torch.empty(M, n, dtype=torch.float16, device=DEV) for n in Ns]
+    Wd = [W.to(DEV) for W in Ws]
+    ops = [dg.linear(dg.LINEAR_F16, W, M, n, K, x=xd, y=y) for W, n, y in zip(Wd, Ns, ys)]
+    plan = dg.StepPlan(ops, Wd + ys + [xd])
+    ws = torch.empty(max(plan.workspace_bytes(), 16), dtype=torch.uint8, device=DEV)
+    dg.decode_step_weights(plan, ws)
+    sync()
+    first = [y.clone() for y in ys]
+    dg.decode_step_weights(plan, ws)
+    sync()
+    for W, y, y0, n in zip(Ws, ys, first, Ns):
+        assert torch.equal(y, y0)
+        yr, A = oracle.gemv_fp(bits(W), bits(x), "f16")
+        tol.assert_close(y.float().cpu().double().numpy(), yr, A, "f16", "segment N=%d M=%d" % (n, M))
