@@ -696,7 +696,7 @@ def main():
                              "decode_int4_4l_a16", "decode_int4_4l_a8", "lm_head",
                              "gateup_fp16", "gateup_w4a16", "gateup_w4a8", "decode_fp16_4l",
                              "gemv_f16_2048", "w8a8_m1",
-                             "w8a8_m4", "w8a8_m16", "fp16_m8", "fp16_m16", "block_fp16_fused",
+                             "w8a8_m4", "w8a8_m8", "w8a8_m16", "fp16_m8", "fp16_m16", "block_fp16_fused",
                              "block_fp16_unfused", "decode_int4_a16_f16head", "conv1d",
                              "quant_w4", "quant_w8", "int4_m8", "int4_m16", "int4_a8_m16",
                              "int4_down_m8"])

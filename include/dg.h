@@ -47,7 +47,8 @@
  *    SM count, and is still the same on every call.  The same holds for int4
  *    calls on the int8 / int4 tcgen05 tile (by default 8+ tokens with K >
  *    8192; one fp32 accumulator per group, scaled as in the scalar
- *    definition); W8A8 there keeps exact int32 sums.  Such a call keeps a small
+ *    definition); W8A8 calls with 8+ tokens also run there by default and
+ *    keep exact int32 sums.  Such a call keeps a small
  *    fixup scratch per (device, stream) (about 4.3 MB, allocated on the
  *    stream's first such call); a stream first used inside graph capture runs
  *    the mma.sync tile instead (K split by a rule on K alone).
@@ -59,7 +60,8 @@
  *    parity bound; KS (warps per row), KP (split-K ranges), MMA (tensor-core
  *    tiles off / int8 tile), TC (fewest tokens on the fp16 / bf16 tcgen05
  *    tile, 0 = off), TQ (fewest tokens on the int8 / int4 tcgen05 tile, 0 =
- *    off; by default only int4 with 8+ tokens and K > 8192 goes there) and TG
+ *    off; by default W8A8 with 8+ tokens and int4 with 8+ tokens and K > 8192
+ *    go there) and TG
  *    (the tcgen05 tiles' CTA count) change a row's summation order, the others
  *    (TK: 64-k boxes per stage of the fp16 tile, 1 or 2; TS: its ring stages,
  *    6 / 8 / 12 with one box, 3 / 4 / 6 with two; TP: stages it prefetches to

@@ -37,10 +37,14 @@
 // -> epilogue, two widened slots), about 2200 cycles per box per SM; no unit
 // is saturated (ncu: issue 39 %, shared-memory wavefronts 16 %, DRAM 14 %).
 //
-// CTA roles (14 warps): warp 0 lane 0 TMA producer; warp 1 TMEM owner and (lane
-// 0) MMA issuer; warps 2-5 epilogue (thread <-> weight row, reading TMEM lane
-// quarter warp % 4); warps 6-13 converters (two per row, each widening half of
-// the row's box).
+// CTA roles (warp w runs on scheduler w % 4): warp 0 lane 0 TMA producer;
+// warp 1 TMEM owner and (lane 0) MMA issuer; warps 2-5 epilogue (thread <->
+// weight row, reading TMEM lane quarter warp % 4); eight converter warps (two
+// per row, each widening half of the row's box).  int4: 14 warps, converters
+// 6-13, two on every scheduler.  W8A8: 16 warps, converters 6, 7 and 10-15, so
+// that the schedulers of the producer and the MMA issuer carry one each and
+// the other two three (warps 8 and 9 idle): measured 24.4 -> 23.3 us at 16
+// tokens, while the same layout made int4 slower (25.9 -> 26.4 us).
 // Every wait is bounded; a timeout records the library's timeout error.
 #include "tc_common.cuh"
 
@@ -52,9 +56,15 @@ namespace {
 
 enum QFmt : int { Q_W8A8 = 0, Q_W4A16 = 1, Q_W4A8 = 2 };
 
-constexpr int kQThreads = 14 * 32;
 constexpr int kQConv = 8 * 32;          // converter threads
-constexpr int kQEpiWarp0 = 2, kQConvWarp0 = 6;
+constexpr int kQEpiWarp0 = 2;
+
+// Converter index 0..7 of warp w, or -1 (the layouts above).
+template <bool INT4>
+__device__ __forceinline__ int q_conv_of_warp(int w) {
+    if (INT4) return w >= 6 && w < 14 ? w - 6 : -1;
+    return w == 6 ? 0 : w == 7 ? 1 : (w >= 10 && w <= 15) ? w - 8 : -1;
+}
 constexpr int kQRawA = kRows * 128;     // 16 KB weight box
 constexpr int kQAccSlots = 16;          // TMEM accumulators (16 columns each)
 constexpr int kQRun8 = 1024;            // W8A8: k per exact fp32 run
@@ -75,6 +85,7 @@ struct QTraits {
     static constexpr int kStage = kQRawA + kRawB;
     static constexpr int kStages = kInt4 ? 3 : 4;          // raw ring
     static constexpr int kTmemCols = kQAccSlots * kTok;    // accumulators only
+    static constexpr int kThreads = (kInt4 ? 14 : 16) * 32;
     static constexpr int kScRing = kInt4 ? kQScSlots * kQScBytes : 0;
     static size_t smem() {
         return (size_t)kStages * kStage + 2 * (size_t)(kWideA + kConvB) + kScRing + 1024 + 1024;
@@ -140,7 +151,7 @@ __device__ __forceinline__ uint32_t widen_int8_pair(uint32_t wf /* w ^ 0x8080808
 
 // RS: MMAs (16-k steps) per int4 group (2, 4, 8, 16); unused for W8A8.
 template <int F, int RS>
-__global__ void __launch_bounds__(kQThreads, 1) k_gemv_tcq(const __grid_constant__ TcqParams p) {
+__global__ void __launch_bounds__(QTraits<F>::kThreads, 1) k_gemv_tcq(const __grid_constant__ TcqParams p) {
     using T = QTraits<F>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -344,9 +355,9 @@ __global__ void __launch_bounds__(kQThreads, 1) k_gemv_tcq(const __grid_constant
         }
         tc_commit(smem_addr(mma_done));
         mbar_wait(smem_addr(mma_done), 0, p.spin, p.err);
-    } else if (warp >= kQConvWarp0) {
+    } else if (q_conv_of_warp<T::kInt4>(warp) >= 0) {
         // ---- converters: widen the weight box (and int8 tokens) into the MMA's layout ----
-        const int cw = warp - kQConvWarp0;          // 0..7
+        const int cw = q_conv_of_warp<T::kInt4>(warp);  // 0..7
         const int half = cw >> 2;                   // which half of the row's 8 raw chunks
         const int row = 32 * (cw & 3) + lane;
         const int ct = cw * 32 + lane;              // 0..255
@@ -412,7 +423,7 @@ __global__ void __launch_bounds__(kQThreads, 1) k_gemv_tcq(const __grid_constant
                 ph ^= 1u;
             }
         }
-    } else if (warp >= kQEpiWarp0) {
+    } else if (warp >= kQEpiWarp0 && warp < kQEpiWarp0 + 4) {
         // ---- epilogue: 128 threads, thread <-> weight row ----
         const int q = warp & 3;
         const int rl = 32 * q + lane;
@@ -609,7 +620,7 @@ cudaError_t launch_tcq(TcqParams& p, int grid, cudaStream_t s) {
     cudaError_t e = smem_attr_once(fn, smem);
     if (e != cudaSuccess) return e;
     void* args[] = {&p};
-    return launch_pdl(fn, dim3((unsigned)grid), dim3(kQThreads), smem, s, args);
+    return launch_pdl(fn, dim3((unsigned)grid), dim3(QTraits<F>::kThreads), smem, s, args);
 }
 
 // The int4 kernels by MMAs per group (groups of 32, 64, 128 or 256 k).
