@@ -156,7 +156,7 @@ static int pick_ks(Fmt f, int K) {
 }
 
 // Rows per slot.  At one token: W4A16 four (its MAC loads each activation
-// piece once for all rows of the slot), W4A8 two, fp16 / bf16 and int8 one.
+// piece once for all rows of the slot), W4A8 and int8 two, fp16 / bf16 one.
 static int pick_r(Fmt f, int MT, int K) {
     (void)K;
     const int t = tune().R;
